@@ -1,0 +1,329 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each test checks the oracle against something other than itself: published
+known-answer vectors, a worked example derived from them by hand, closed forms,
+library routines (numpy, scipy), invariants and brute force on tiny inputs.
+"""
+import itertools
+import os
+
+import numpy as np
+import pytest
+import scipy.sparse as sp
+from scipy import stats
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_rows(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as fh:
+        for line in fh:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+# ------------------------------------------------------------------ Philox
+def test_philox_known_answers():
+    rows = _read_rows("philox4x32_10_kat.txt")
+    assert len(rows) == 3
+    for r in rows:
+        words = [int(x, 16) for x in r]
+        ctr, key, want = words[:4], words[4:6], words[6:10]
+        assert [int(x) for x in oracle.philox4x32_10(ctr, key)] == want
+
+
+def test_sample_key_uses_word_j_mod_4():
+    # keys of positions 0..3 of (v=0, hop=0, seed=0) are the first KAT vector
+    want = [int(x, 16) for x in _read_rows("philox4x32_10_kat.txt")[0][6:10]]
+    assert [oracle.sample_key(0, 0, 0, j) for j in range(4)] == want
+
+
+def test_sample_worked_example():
+    indptr = np.array([0, 4], np.int64)
+    for row in _read_rows("sample_worked_example.txt"):
+        f, want = int(row[0]), [int(x) for x in row[1:]]
+        assert oracle.sample_positions(indptr, 0, f, 0, 0).tolist() == want
+
+
+# ---------------------------------------------------------------- sampling
+def _random_graph(rng, n, max_deg):
+    deg = rng.integers(0, max_deg + 1, size=n)
+    indptr = np.concatenate([[0], np.cumsum(deg)]).astype(np.int64)
+    indices = rng.integers(0, n, size=int(indptr[-1])).astype(np.int32)
+    return indptr, indices
+
+
+def test_sample_size_and_full_rows_brute_force():
+    rng = np.random.default_rng(1)
+    indptr, _ = _random_graph(rng, 60, 40)
+    for v in range(60):
+        deg = int(indptr[v + 1] - indptr[v])
+        for f in (1, 3, 5, 10, 25):
+            for hop in (1, 2):
+                p = oracle.sample_positions(indptr, v, f, hop, 12345)
+                assert len(p) == min(deg, f)
+                assert len(set(p.tolist())) == len(p)
+                assert np.all(np.diff(p) > 0) and (len(p) == 0 or (p[0] >= 0 and p[-1] < deg))
+                if deg <= f:
+                    assert p.tolist() == list(range(deg))
+
+
+def _inclusion_stat(counts, R, f, deg):
+    # inclusion counts of a uniform f-subset: covariance R*p(1-p)*d/(d-1)*(I - 11^T/d)
+    p = f / deg
+    expect = R * p
+    scale = R * p * (1 - p) * deg / (deg - 1)
+    t = float(((counts - expect) ** 2).sum() / scale)
+    return stats.chi2.sf(t, deg - 1)
+
+
+@pytest.mark.parametrize("deg,f", [(20, 5), (50, 10), (7, 6)])
+def test_inclusion_uniform_chi_square(deg, f):
+    # GARDEN page, Section IV-C: the sampler must not alter sampling
+    # probabilities: every position is kept with probability f/deg
+    indptr = np.array([0, deg], np.int64)
+    R = 20000
+    counts = np.zeros(deg)
+    for s in range(R):
+        counts[oracle.sample_positions(indptr, 0, f, 1, 0x1234_0000_0000 + s)] += 1
+    assert counts.sum() == R * f
+    assert _inclusion_stat(counts, R, f, deg) > 1e-3
+
+
+def test_subsets_equiprobable_chi_square():
+    # uniform without replacement: all C(5,2) = 10 subsets equally likely
+    indptr = np.array([0, 5], np.int64)
+    R = 20000
+    subsets = {c: 0 for c in itertools.combinations(range(5), 2)}
+    for s in range(R):
+        subsets[tuple(oracle.sample_positions(indptr, 0, 2, 2, 977 * s + 3).tolist())] += 1
+    obs = np.array(list(subsets.values()), float)
+    assert stats.chisquare(obs).pvalue > 1e-3
+
+
+def test_hub_row_spanning_many_counter_blocks():
+    # a star hub with 1000 leaves: positions cover 250 Philox counter blocks
+    deg, f, R = 1000, 15, 4000
+    indptr = np.array([0, deg], np.int64)
+    counts = np.zeros(deg)
+    for s in range(R):
+        counts[oracle.sample_positions(indptr, 0, f, 3, s)] += 1
+    assert _inclusion_stat(counts, R, f, deg) > 1e-3
+    # the four words of one counter block are all used
+    by_word = counts.reshape(-1, 4).sum(axis=0)
+    assert stats.chisquare(by_word).pvalue > 1e-3
+
+
+def test_sample_depends_on_hop_node_and_seed():
+    indptr = np.array([0, 100, 200], np.int64)
+    a = oracle.sample_positions(indptr, 0, 5, 1, 7).tolist()
+    assert a != oracle.sample_positions(indptr, 0, 5, 2, 7).tolist()
+    assert a != oracle.sample_positions(indptr, 1, 5, 1, 7).tolist()
+    assert a != oracle.sample_positions(indptr, 0, 5, 1, 8).tolist()
+    assert a == oracle.sample_positions(indptr, 0, 5, 1, 7).tolist()
+
+
+# ------------------------------------------------------- multi-hop + relabel
+def _first_occurrence(prefix, ids):
+    seen = set(int(x) for x in prefix)
+    out = []
+    for x in ids:
+        x = int(x)
+        if x not in seen:
+            seen.add(x)
+            out.append(x)
+    return out
+
+
+def _check_blocks(indptr, indices, seeds, fanouts, seed, b):
+    B = len(seeds)
+    assert b.unique[:B].tolist() == list(seeds)                   # seeds first
+    assert len(set(b.unique.tolist())) == len(b.unique)          # bijection
+    for h in range(1, len(fanouts) + 1):
+        f = fanouts[h - 1]
+        n_prev, n_cur = b.hop_off[h - 1], b.hop_off[h]
+        assert n_prev <= n_cur                                   # V_{h-1} is a prefix of V_h
+        bp, idx, nbr, pos = b.indptr[h - 1], b.idx[h - 1], b.nbr[h - 1], b.pos[h - 1]
+        assert len(bp) == n_prev + 1 and bp[0] == 0 and bp[-1] == len(idx)
+        assert np.all(idx >= 0) and np.all(idx < n_cur)
+        assert np.array_equal(b.unique[idx], nbr)                 # round trip
+        for d in range(n_prev):
+            v = int(b.unique[d])
+            deg = int(indptr[v + 1] - indptr[v])
+            lo, hi = int(bp[d]), int(bp[d + 1])
+            assert hi - lo == min(deg, f)
+            assert np.array_equal(nbr[lo:hi], indices[indptr[v] + pos[lo:hi]])
+            assert np.array_equal(pos[lo:hi], oracle.sample_positions(indptr, v, f, h, seed))
+        # the new nodes of the hop, in order of first occurrence
+        assert b.unique[n_prev:n_cur].tolist() == _first_occurrence(b.unique[:n_prev], nbr)
+
+
+def test_sampler_run_invariants_tiny():
+    w = synth.workload("tiny")
+    g = synth.chung_lu(2000, w.mean_deg, w.gamma, 200.0, 0)
+    seeds = synth.batch_seeds(g.n, 1.0, 0, 64)
+    b = oracle.sampler_run(g.indptr, g.indices, seeds, [10, 5], 99)
+    _check_blocks(g.indptr, g.indices, seeds.tolist(), [10, 5], 99, b)
+    assert b.hop_off[2] > b.hop_off[1] > b.hop_off[0] == 64
+
+
+def test_sampler_run_hand_graph():
+    # path 0->1->2->3 plus node 0 -> {1,2,3}: seeds [0]; fanout 5 keeps all
+    indptr = np.array([0, 3, 4, 5, 5], np.int64)
+    indices = np.array([1, 2, 3, 2, 3], np.int32)
+    b = oracle.sampler_run(indptr, indices, [0], [5, 5], 1)
+    assert b.unique.tolist() == [0, 1, 2, 3]
+    assert b.hop_off == [1, 4, 4]
+    assert b.indptr[0].tolist() == [0, 3] and b.idx[0].tolist() == [1, 2, 3]
+    # hop 2 samples every node of V_1 = {0,1,2,3}
+    assert b.indptr[1].tolist() == [0, 3, 4, 5, 5]
+    assert b.idx[1].tolist() == [1, 2, 3, 2, 3]
+
+
+def test_sampler_run_deterministic_over_threads():
+    g = synth.chung_lu(5000, 12.0, 2.0, 300.0, 3)
+    seeds = synth.batch_seeds(g.n, 1.0, 2, 100)
+    n0 = oracle.num_threads()
+    try:
+        oracle.set_threads(1)
+        a = oracle.sampler_run(g.indptr, g.indices, seeds, [8, 4, 2], 5)
+        oracle.set_threads(max(2, n0))
+        b = oracle.sampler_run(g.indptr, g.indices, seeds, [8, 4, 2], 5)
+    finally:
+        oracle.set_threads(n0)
+    assert np.array_equal(a.unique, b.unique)
+    for h in range(3):
+        assert np.array_equal(a.idx[h], b.idx[h]) and np.array_equal(a.indptr[h], b.indptr[h])
+
+
+def test_super_batch_layout():
+    g = synth.chung_lu(3000, 10.0, 2.1, 200.0, 1)
+    seed_lists = [synth.batch_seeds(g.n, 1.0, k, 32) for k in range(4)]
+    sb = oracle.super_batch_run(g.indptr, g.indices, seed_lists, [6, 3], 11)
+    tot = sb.totals()
+    assert len(sb.unique) == tot[-1]
+    for h in range(1, 3):
+        bp, idx = sb.indptr[h - 1], sb.idx[h - 1]
+        assert len(bp) == tot[h - 1] + 1 and bp[-1] == len(idx) == sb.edge_counts[:, h - 1].sum()
+        # each concatenated row maps back to its sub-batch's own block
+        row = 0
+        s_off = 0
+        for k, r in enumerate(sb.runs):
+            for d in range(r.hop_off[h - 1]):
+                lo, hi = bp[row], bp[row + 1]
+                rl, rh = r.indptr[h - 1][d], r.indptr[h - 1][d + 1]
+                assert np.array_equal(idx[lo:hi] - s_off, r.idx[h - 1][rl:rh])
+                row += 1
+            s_off += r.hop_off[h]
+
+
+def test_relabel_standalone():
+    rng = np.random.default_rng(4)
+    prefix = rng.permutation(1000)[:50].astype(np.int32)
+    ids = rng.integers(0, 1000, size=3000).astype(np.int32)
+    unique, local = oracle.relabel(ids, prefix)
+    assert unique[:50].tolist() == prefix.tolist()
+    assert len(set(unique.tolist())) == len(unique)
+    assert np.array_equal(unique[local], ids)
+    assert unique[50:].tolist() == _first_occurrence(prefix, ids)
+    with pytest.raises(ValueError):
+        oracle.relabel(ids, np.array([1, 1], np.int32))
+
+
+# ------------------------------------------------------------------ gather
+def test_gather_matches_take():
+    rng = np.random.default_rng(5)
+    feat = synth.features(500, 24, "f32", 1)
+    ids = rng.integers(0, 500, size=2000).astype(np.int32)
+    assert np.array_equal(oracle.gather(feat, ids).view(np.uint32), np.take(feat, ids, axis=0).view(np.uint32))
+    fb = synth.features(500, 64, "bf16", 1)
+    assert np.array_equal(oracle.gather(fb, ids), np.take(fb, ids, axis=0))
+
+
+# --------------------------------------------------------------- aggregate
+def test_aggregate_star_closed_form():
+    # hub 0 aggregates leaves 1..n with x_v[c] = v + c: mean = (n+1)/2 + c
+    n, dim = 40, 6
+    indptr = np.array([0, n], np.int64)
+    idx = np.arange(1, n + 1, dtype=np.int32)
+    h = (np.arange(n + 1)[:, None] + np.arange(dim)[None, :]).astype(np.float32)
+    out, _ = oracle.aggregate_fwd(indptr, idx, h)
+    assert np.array_equal(out[0], (n + 1) / 2 + np.arange(dim))
+
+
+def test_aggregate_complete_graph_closed_form():
+    # K_n without self-loops, x_v[c] = v + c: mean over the others = (S - x_v)/(n-1)
+    n, dim = 9, 5
+    indptr = np.arange(0, n * (n - 1) + 1, n - 1, dtype=np.int64)
+    idx = np.array([u for v in range(n) for u in range(n) if u != v], np.int32)
+    x = (np.arange(n)[:, None] + np.arange(dim)[None, :]).astype(np.float32)
+    out, _ = oracle.aggregate_fwd(indptr, idx, x)
+    want = (x.astype(np.float64).sum(axis=0)[None, :] - x) / (n - 1)
+    assert np.array_equal(out, want)
+    # backward of all-ones: every node is named by n-1 rows of weight 1/(n-1)
+    g, _ = oracle.aggregate_bwd(indptr, idx, n, np.ones((n, dim), np.float32))
+    assert np.allclose(g, 1.0, rtol=0, atol=1e-15)
+
+
+def test_aggregate_empty_rows_are_zero():
+    indptr = np.array([0, 0, 2, 2], np.int64)
+    idx = np.array([0, 1], np.int32)
+    h = np.array([[1.0, 2.0], [3.0, 4.0]], np.float32)
+    out, _ = oracle.aggregate_fwd(indptr, idx, h)
+    assert out.tolist() == [[0, 0], [2, 3], [0, 0]]
+
+
+def _random_block(rng, n_dst, n_src, f):
+    c = rng.integers(0, f + 1, size=n_dst)
+    indptr = np.concatenate([[0], np.cumsum(c)]).astype(np.int64)
+    idx = rng.integers(0, n_src, size=int(indptr[-1])).astype(np.int32)
+    return indptr, idx
+
+
+def test_aggregate_matches_scipy_sparse():
+    rng = np.random.default_rng(6)
+    indptr, idx = _random_block(rng, 300, 900, 12)
+    c = np.diff(indptr)
+    A = sp.csr_matrix((np.ones(len(idx)), idx, indptr), shape=(300, 900))
+    x = rng.standard_normal((900, 16)).astype(np.float32)
+    out, am = oracle.aggregate_fwd(indptr, idx, x)
+    want = (A @ x.astype(np.float64)) / np.maximum(c, 1)[:, None]
+    assert np.allclose(out, want, rtol=1e-13, atol=1e-13)
+    assert np.allclose(am, (A @ np.abs(x.astype(np.float64))) / np.maximum(c, 1)[:, None])
+    g = rng.standard_normal((300, 16)).astype(np.float32)
+    gs, _ = oracle.aggregate_bwd(indptr, idx, 900, g)
+    wantb = A.T @ (g.astype(np.float64) / np.maximum(c, 1)[:, None])
+    assert np.allclose(gs, wantb, rtol=1e-13, atol=1e-13)
+
+
+def test_aggregate_adjoint_identity():
+    rng = np.random.default_rng(7)
+    indptr, idx = _random_block(rng, 200, 500, 9)
+    x = rng.standard_normal((500, 8)).astype(np.float32)
+    y = rng.standard_normal((200, 8)).astype(np.float32)
+    ax, _ = oracle.aggregate_fwd(indptr, idx, x)
+    aty, _ = oracle.aggregate_bwd(indptr, idx, 500, y)
+    lhs = float((ax * y.astype(np.float64)).sum())
+    rhs = float((x.astype(np.float64) * aty).sum())
+    assert abs(lhs - rhs) <= 1e-10 * (1 + abs(lhs))
+
+
+def test_aggregate_bf16_input():
+    rng = np.random.default_rng(8)
+    indptr, idx = _random_block(rng, 50, 80, 6)
+    xb = synth.features(80, 32, "bf16", 2)
+    out, _ = oracle.aggregate_fwd(indptr, idx, xb)
+    out32, _ = oracle.aggregate_fwd(indptr, idx, oracle.bf16_to_f32(xb).reshape(80, 32))
+    assert np.array_equal(out, out32)
+
+
+def test_bf16_decode_exact():
+    bits = np.array([0x3F80, 0xBF80, 0x4049, 0x0000, 0x8000, 0x7F80], np.uint16)
+    assert oracle.bf16_to_f32(bits).tolist()[:5] == [1.0, -1.0, 3.140625, 0.0, -0.0]
+    assert np.isinf(oracle.bf16_to_f32(bits)[5])
