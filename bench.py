@@ -1,0 +1,519 @@
+"""Benchmark of the mini-batch pipeline (sample -> relabel -> cached gather ->
+mean aggregation forward + backward) on the Mid workload: 2.4M-node
+Chung-Lu graph (exponent 2.0, mean degree 26, max 20,000), 100-dim fp32
+features in pinned host memory, an HBM cache of 50% of the feature bytes
+ranked by presampled access frequency, 3 hops with fanouts [15, 10, 5],
+1024 seeds per batch from an 8% training mask.
+
+One step = one mini-batch through every stage.  Prints one JSON line.
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config mid]
+Under torchrun (N > 1) every rank runs its own batches on its own GPU
+(replicas, no collective on the data path); the slowest rank's time counts.
+--impl reference times the CPU oracle on the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "sampled edges/s, gathered feature GB/s, batch latency; % of memory roofline"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="mid")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="bound on the CPU-baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            p = json.load(fh)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = "clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown," \
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown," \
+             "clocks_event_reasons.sw_power_cap"
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ workload
+class Workload:
+    """Graph, features and batches of one config, built once per process."""
+
+    def __init__(self, name: str, pinned_features: bool):
+        import torch
+        self.w = synth.workload(name)
+        w = self.w
+        t0 = time.time()
+        self.g = synth.chung_lu(w.n_nodes, w.mean_deg, w.gamma, w.wmax, w.rng_seed)
+        self.t_graph = time.time() - t0
+        dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+        t0 = time.time()
+        self.feat = torch.empty((w.n_nodes, w.dim), dtype=dt, pin_memory=pinned_features)
+        synth.features_into(self.feat.data_ptr(), 0, w.n_nodes, w.dim, w.dtype, w.rng_seed)
+        self.t_feat = time.time() - t0
+
+    def seeds(self, batch: int) -> np.ndarray:
+        return synth.batch_seeds(self.g.n, self.w.p_mask, batch, self.w.batch, self.w.rng_seed)
+
+
+def kernels_per_step(H: int, n_sub: int) -> int:
+    """Kernels one step launches: sampler 1 + 6 per hop (+1 compaction for a
+    super-batch), gather 1, forward 1 per hop, backward 7 per hop."""
+    return (1 + 6 * H + (1 if n_sub > 1 else 0)) + 1 + H + 7 * H
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    from sampling_gnn_mini_gb300 import binding as sg
+    from sampling_gnn_mini_gb300.pipeline import MiniBatchPipeline
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    sg.load(build_if_missing=True)
+    W = Workload(args.config, pinned_features=True)
+    w, g = W.w, W.g
+    H = w.n_hops
+    R = w.row_bytes
+    hbm_peak, peak_kind = peaks()
+
+    # graph into HBM; int64 offsets where the config calls for them
+    G = sg.sg_graph_load(g.indptr if w.offset_bits == 64 else g.indptr.astype(np.int32), g.indices, w.offset_bits)
+    cache_rows = w.cache_rows
+    # rank nodes by presampled frequency in V_H: batches disjoint from the measured ones
+    if cache_rows < w.n_nodes:
+        full = sg.sg_cache_build(W.feat, None, sg.SG_F32 if w.dtype == "f32" else sg.SG_BF16, w.n_nodes, w.dim,
+                                 np.zeros(0, np.int32), 0)
+        pre = MiniBatchPipeline(G, full, w.fanouts, w.batch, backward=False, device=dev)
+        freq = np.zeros(w.n_nodes, np.int64)
+        for b in range(w.presample_batches):
+            s = W.seeds(100000 + b)
+            pre.set_batch(torch.from_numpy(s).to(dev), w.sampler_seed(100000 + b))
+            pre.sample()
+            n_h = int(pre.counts[H].item())
+            np.add.at(freq, pre.buf.unique[:n_h].cpu().numpy(), 1)
+        ranked = np.lexsort((np.arange(w.n_nodes), -freq))[:cache_rows].astype(np.int32)
+        del pre, full
+    else:
+        ranked = None
+    dtype_code = sg.SG_F32 if w.dtype == "f32" else sg.SG_BF16
+    cache = sg.sg_cache_build(W.feat if w.host_features else None,
+                              None if w.host_features else W.feat.to(dev), dtype_code, w.n_nodes, w.dim,
+                              ranked, cache_rows)
+    pipe = MiniBatchPipeline(G, cache, w.fanouts, w.batch, device=dev)
+
+    # batches of this rank (replicas: disjoint batch indices per rank)
+    n_batches = args.warmup + args.steps
+    bidx = [rank + world * i for i in range(n_batches)]
+    seeds_host = np.stack([W.seeds(b) for b in bidx]).astype(np.int32)
+    seeds_pool = torch.from_numpy(seeds_host).to(dev)
+    hseed_pool = torch.tensor([w.sampler_seed(b) for b in bidx], dtype=torch.int64, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    # stage graphs: sample, gather, forward per hop, backward per hop
+    stages = [("sample", pipe.sample), ("gather", pipe.gather)]
+    nb = pipe.bounds.max_nodes
+
+    def fwd_hop(h):
+        return lambda: sg.sg_aggregate_fwd(pipe.buf.indptr[h - 1], pipe.buf.idx[h - 1], nb[h - 1], nb[h],
+                                           pipe.buf.dims(h), pipe.h_feat[h], pipe.h_feat[h - 1])
+
+    def bwd_hop(h):
+        return lambda: sg.sg_aggregate_bwd(pipe.buf.indptr[h - 1], pipe.buf.idx[h - 1], nb[h - 1], nb[h],
+                                           pipe.bounds.max_edges[h - 1], pipe.buf.dims(h), pipe.g_feat[h - 1],
+                                           pipe.g_feat[h], pipe.bwd_ws)
+
+    for h in range(H, 0, -1):
+        stages.append(("fwd%d" % h, fwd_hop(h)))
+    for h in range(1, H + 1):
+        stages.append(("bwd%d" % h, bwd_hop(h)))
+
+    def load_batch(i):
+        pipe.seeds[: w.batch].copy_(seeds_pool[i], non_blocking=True)
+        pipe.d_seed.copy_(hseed_pool[i: i + 1], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        load_batch(0)
+        for _, fn in stages:
+            fn()
+    torch.cuda.synchronize(dev)
+    sg.sg_stream_check(stream)
+    graphs = []
+    for name, fn in stages:
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg, stream=stream):
+            fn()
+        graphs.append((name, cg))
+    torch.cuda.synchronize(dev)
+    counts_log = torch.zeros((n_batches, pipe.buf.counts.numel()), dtype=torch.int32, device=dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(graphs) + 1)] for _ in range(args.steps)]
+
+    def one_step(i, events=None):
+        load_batch(i)
+        if events:
+            events[0].record(stream)
+        for j, (_, cg) in enumerate(graphs):
+            cg.replay()
+            if events:
+                events[j + 1].record(stream)
+        counts_log[i].copy_(pipe.buf.counts, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            one_step(i)
+    torch.cuda.synchronize(dev)
+    sg.sg_stream_check(stream)
+    pipe.stats.zero_()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks = Clocks(local)
+    clocks.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for s in range(args.steps):
+            one_step(args.warmup + s, ev[s])
+        t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    sg.sg_stream_check(stream)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    stage_ms = {name: 0.0 for name, _ in graphs}
+    for s in range(args.steps):
+        for j, (name, _) in enumerate(graphs):
+            stage_ms[name] += ev[s][j].elapsed_time(ev[s][j + 1]) / args.steps
+    counts = counts_log[args.warmup:].cpu().numpy()
+    nodes = counts[:, : H + 1].astype(np.int64)
+    edges = counts[:, H + 1: 2 * H + 1].astype(np.int64)
+    hits, misses = [int(x) for x in pipe.stats.cpu().tolist()]
+    total_edges = int(edges.sum())
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_edges, hits, misses], dtype=torch.int64, device=dev)
+        dist.all_reduce(t)
+        total_edges_all = int(t[0].item())
+    else:
+        total_edges_all = total_edges
+    value = total_edges_all / (elapsed_ms / 1e3)
+
+    # ---- roofline bookkeeping (outside the timed region) ----
+    link_gbs = measure_link(sg, torch, dev, stream) if w.host_features else None
+    hash_rate = measure_hash(sg, torch, dev, stream)
+    deg = np.diff(g.indptr)
+    # exact algorithmic bytes need the distinct srcs of each block: rerun the
+    # measured batches' sampling (deterministic) and count them on the host
+    uniq_src = np.zeros((args.steps, H), np.int64)
+    hashed = np.zeros((args.steps, H), np.int64)
+    for s in range(args.steps):
+        i = args.warmup + s
+        with torch.cuda.stream(stream):
+            load_batch(i)
+            pipe.sample()
+        torch.cuda.synchronize(dev)
+        uq = pipe.buf.unique[: nodes[s, H]].cpu().numpy()
+        for h in range(1, H + 1):
+            idx = pipe.buf.idx[h - 1][: edges[s, h - 1]].cpu().numpy()
+            uniq_src[s, h - 1] = len(np.unique(idx))
+            d = deg[uq[: nodes[s, h - 1]]]
+            hashed[s, h - 1] = int(d[d > w.fanouts[h - 1]].sum())
+    n_H = nodes[:, H].astype(np.float64)
+    gather_hbm = (8.0 * n_H).sum() + hits * R + n_H.sum() * R
+    gather_host = misses * R
+    t_gather = stage_ms["gather"] * args.steps / 1e3
+    roof_gather_t = max(gather_hbm / (hbm_peak * 1e9), gather_host / (link_gbs * 1e9) if link_gbs else 0.0)
+    stage_roof = {}
+    stage_roof["gather"] = {"bound": "host_link" if link_gbs and gather_host / link_gbs > gather_hbm / hbm_peak else "hbm",
+                            "achieved_hbm_gbs": gather_hbm / t_gather / 1e9,
+                            "achieved_host_gbs": gather_host / t_gather / 1e9,
+                            "frac": roof_gather_t / t_gather}
+    for h in range(H, 0, -1):
+        byt = ((nodes[:, h - 1] + 1) * 4 + edges[:, h - 1] * 4 + uniq_src[:, h - 1] * R + nodes[:, h - 1] * R).sum()
+        t = stage_ms["fwd%d" % h] * args.steps / 1e3
+        stage_roof["fwd%d" % h] = {"bound": "hbm", "bytes_per_launch": float(byt) / args.steps,
+                                   "achieved_gbs": byt / t / 1e9, "frac": byt / t / 1e9 / hbm_peak,
+                                   "per_edge_gbs": float((edges[:, h - 1] * R).sum()) / t / 1e9}
+    for h in range(1, H + 1):
+        byt = ((nodes[:, h] + 1) * 4 + edges[:, h - 1] * 4 + nodes[:, h - 1] * R + nodes[:, h] * R).sum()
+        t = stage_ms["bwd%d" % h] * args.steps / 1e3
+        stage_roof["bwd%d" % h] = {"bound": "hbm", "bytes_per_launch": float(byt) / args.steps,
+                                   "achieved_gbs": byt / t / 1e9, "frac": byt / t / 1e9 / hbm_peak,
+                                   "note": "stage time includes building the transposed block"}
+    t_sample = stage_ms["sample"] * args.steps / 1e3
+    stage_roof["sample"] = {"bound": "alu", "hash_calls_per_s": hashed.sum() / 4.0 / t_sample,
+                            "peak_hash_calls_per_s": hash_rate,
+                            "frac": (hashed.sum() / 4.0 / t_sample) / hash_rate}
+    dom = max(stage_ms, key=lambda k: stage_ms[k])
+    if dom == "gather":
+        ach_bytes = (gather_host if stage_roof["gather"]["bound"] == "host_link" else gather_hbm) / args.steps
+        peak = link_gbs if stage_roof["gather"]["bound"] == "host_link" else hbm_peak
+        roof = {"kernel": "k_gather", "bound": stage_roof["gather"]["bound"],
+                "achieved": ach_bytes / (stage_ms["gather"] / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
+                "frac": stage_roof["gather"]["frac"], "traffic": None,
+                "peak_kind": "measured link (same run)" if stage_roof["gather"]["bound"] == "host_link" else "of " + peak_kind}
+    elif dom.startswith("fwd") or dom.startswith("bwd"):
+        r = stage_roof[dom]
+        roof = {"kernel": dom, "bound": "hbm", "achieved": r["achieved_gbs"], "peak": hbm_peak, "unit": "GB/s",
+                "frac": r["frac"], "traffic": None, "peak_kind": "of " + peak_kind}
+    else:
+        r = stage_roof["sample"]
+        roof = {"kernel": "sampler (k_sample and its scans)", "bound": "alu", "achieved": r["hash_calls_per_s"] / 1e9,
+                "peak": hash_rate / 1e9, "unit": "G Philox calls/s", "frac": r["frac"], "traffic": None,
+                "peak_kind": "measured Philox throughput (same run)"}
+
+    result = {
+        "metric": METRIC, "value": value, "unit": "sampled edges/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int32 sampling / " + w.dtype + " features, fp32 accumulation",
+        "data": "synthetic Chung-Lu graph and N(0,1) features (seeded); no dataset",
+        "config": {"workload": "%s: %d nodes, %d edges, exponent %.1f, mean %.0f, dim %d %s, fanouts %s, batch %d, "
+                               "cache %d rows (%.0f%%)" % (w.name, g.n, g.m, w.gamma, w.mean_deg, w.dim, w.dtype,
+                                                          w.fanouts, w.batch, cache_rows, 100.0 * cache_rows / w.n_nodes),
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (CSR %.0f MB, features %.0f MB); a new batch every step"
+                         % ((g.indptr.nbytes + g.indices.nbytes) / 1e6, w.n_nodes * R / 1e6)},
+        "batch_latency_ms": elapsed_ms / args.steps,
+        "gathered_feature_gbs": n_H.sum() * R / (elapsed_ms / 1e3) / 1e9,
+        "gather_kernel_gbs": n_H.sum() * R / t_gather / 1e9,
+        "memory_roofline_frac": {k: v["frac"] for k, v in stage_roof.items()},
+        "hit_rate": hits / max(1, hits + misses),
+        "stage_ms": stage_ms,
+        "stages": stage_roof,
+        "roofline": roof,
+        "host_link_gbs": link_gbs,
+        "per_step": {"nodes": nodes.mean(axis=0).tolist(), "edges": edges.mean(axis=0).tolist()},
+        "gpu_launches": kernels_per_step(H, 1) * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_e2e:
+        result["e2e"] = measure_e2e(sg, torch, pipe, seeds_host, [w.sampler_seed(b) for b in bidx], dev, args, H, w)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return result, W
+
+
+def measure_link(sg, torch, dev, stream, nbytes=4 << 30):
+    """Zero-copy read bandwidth of pinned host memory (16-byte loads)."""
+    host = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    host.fill_(1)
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+    best = None
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            sg.sg_read_probe(host.data_ptr(), nbytes, sink, stream)
+            b.record(stream)
+            b.synchronize()
+            gbs = nbytes / (a.elapsed_time(b) / 1e3) / 1e9
+            best = gbs if best is None else max(best, gbs)
+    del host
+    return best
+
+
+def measure_hash(sg, torch, dev, stream, n_calls=1 << 30):
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+    best = None
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            sg.sg_hash_probe(n_calls, 7, sink, stream)
+            b.record(stream)
+            b.synchronize()
+            r = n_calls / (a.elapsed_time(b) / 1e3)
+            best = r if best is None else max(best, r)
+    return best
+
+
+def measure_e2e(sg, torch, pipe, seeds_host, hseeds, dev, args, H, w):
+    """Same metric through the public API with host buffers: per step the
+    seeds go host -> device from pinned memory and the step's result (the
+    seed rows H_0 and the counts) comes back device -> host."""
+    stream = torch.cuda.Stream(device=dev)
+    B = w.batch
+    h_seeds = torch.from_numpy(seeds_host).pin_memory()
+    h_hseed = torch.tensor(hseeds, dtype=torch.int64).pin_memory()
+    out_rows = torch.empty((B, w.dim), dtype=pipe.dtype, pin_memory=True)
+    out_counts = torch.empty(pipe.buf.counts.numel(), dtype=torch.int32, pin_memory=True)
+    with torch.cuda.stream(stream):
+        pipe.step()
+    torch.cuda.synchronize(dev)
+    cg = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(cg, stream=stream):
+        pipe.step()
+    torch.cuda.synchronize(dev)
+    n = len(seeds_host)
+    edges = 0
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            pipe.seeds[:B].copy_(h_seeds[i], non_blocking=True)
+            pipe.d_seed.copy_(h_hseed[i: i + 1], non_blocking=True)
+            cg.replay()
+            out_rows.copy_(pipe.h_feat[0][:B], non_blocking=True)
+            out_counts.copy_(pipe.buf.counts, non_blocking=True)
+            stream.synchronize()
+            edges += int(out_counts[H + 1: 2 * H + 1].sum())
+    dt = time.perf_counter() - t0
+    sg.sg_stream_check(stream)
+    return {"value": edges / dt, "unit": "sampled edges/s", "ms_per_step": dt / n * 1e3, "steps": n,
+            "h2d_bytes_per_step": B * 4 + 8, "d2h_bytes_per_step": B * w.row_bytes + pipe.buf.counts.numel() * 4,
+            "note": "single CUDA-graph replay per step; host sync per step to read the result"}
+
+
+# -------------------------------------------------------------- CPU baseline
+def run_oracle_steps(W, batches, budget_s):
+    """The oracle's whole step (sample+relabel, gather, forward and backward
+    chains in fp64) on the given batches, stopping once budget_s is spent."""
+    import oracle
+    w, g = W.w, W.g
+    feat = W.feat.numpy() if w.dtype == "f32" else W.feat.view(__import__("torch").int16).numpy().view(np.uint16)
+    edges, done, t0 = 0, 0, time.perf_counter()
+    for b in batches:
+        seeds = W.seeds(b)
+        r = oracle.sampler_run(g.indptr, g.indices, seeds, w.fanouts, w.sampler_seed(b))
+        x = oracle.gather(feat, r.unique)
+        hh = x
+        for h in range(w.n_hops, 0, -1):
+            hh, _ = oracle.aggregate_fwd(r.indptr[h - 1], r.idx[h - 1], hh.astype(np.float32) if hh.dtype != np.uint16 else hh)
+        gg = hh.astype(np.float32)
+        for h in range(1, w.n_hops + 1):
+            gg, _ = oracle.aggregate_bwd(r.indptr[h - 1], r.idx[h - 1], r.hop_off[h], gg.astype(np.float32))
+        edges += sum(len(i) for i in r.idx)
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return edges, done, dt
+
+
+def cpu_baseline(W, budget_s):
+    import oracle
+    edges, done, dt = run_oracle_steps(W, range(10 ** 6, 10 ** 6 + 1000), budget_s)
+    return {"value": edges / dt, "unit": "sampled edges/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "%d %s batches, whole step (sample+relabel, gather, %d-hop forward and backward), %.1f s"
+                      % (done, W.w.name, W.w.n_hops, dt)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    W = Workload(args.config, pinned_features=False)
+    w = W.w
+    per_step = max(1.0, 120.0 / max(1, args.steps + args.warmup))
+    run_oracle_steps(W, range(args.warmup), per_step * args.warmup)
+    edges, done, dt = 0, 0, 0.0
+    for s in range(args.steps):
+        e, d, t = run_oracle_steps(W, [args.warmup + s], per_step)
+        edges, done, dt = edges + e, done + d, dt + t
+    value = edges / dt
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "sampled edges/s", "n_gpus": world,
+            "steps": done, "warmup": args.warmup, "ms_per_step": dt / done * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int32 sampling / fp64 sums (CPU oracle)",
+            "data": "synthetic Chung-Lu graph and N(0,1) features (seeded); no dataset",
+            "config": {"workload": "%s (same graph, features and batches as the GPU arm)" % w.name},
+            "cpu_baseline": {"value": value, "unit": "sampled edges/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": "%d batches, one whole step each" % done},
+            "e2e": {"value": value, "unit": "sampled edges/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    res, W = run_ours(args, rank, world, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(W, args.cpu_seconds)
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,279 @@
+/*
+ * sg.h - C ABI of the GB300 mini-batch pipeline for sampling-based GNN
+ * training: multi-hop neighbour sampling, ID dedup + relabel into per-hop
+ * blocks, feature gather through an HBM hot-node cache, and mean
+ * aggregation forward and backward.
+ *
+ * The operations follow the GARDEN page ("GARDEN: Efficient GPU-Accelerated
+ * Billion-Scale GNN Training via Caching-Sampling-Batching Co-Design"):
+ * Section II-A Eq. (1)-(2) (message passing; AGGREGATE = mean here), Section
+ * II-B and Fig. 1 (layer-wise blocks: V_l = V_{l-1} u N_l(V_{l-1}), seeds are
+ * the output nodes, V_k the input nodes), Section II-B Fig. 2 (Nfeat-Cache in
+ * GPU memory, misses read zero-copy from pinned host memory), Section IV-C
+ * (fixed-fanout uniform sampling; degree <= fanout keeps every neighbour),
+ * Section IV-D (super-batch of K mini-batches with a BatchPtr and a GPU hash
+ * table for dedup).  The sync-free ID map follows the FastGL explainer page
+ * ("Fused-Map").
+ *
+ * Conventions
+ *  - Every call returns sg_status (SG_OK = 0).  No exception crosses the ABI.
+ *    sg_last_error() gives a message for the calling thread's last failure.
+ *  - Pointers named d_* are device memory (or managed / device-accessible
+ *    memory) of the current CUDA device; h_* are host memory.  Every buffer is
+ *    OWNED BY THE CALLER except what sits behind an opaque handle (sg_graph,
+ *    sg_cache), which the library owns and frees in the matching *_destroy.
+ *  - Device work is asynchronous on the caller's stream (sg_stream_t is a
+ *    cudaStream_t; NULL is the legacy default stream).  Calls return before the
+ *    work finishes; no call synchronises the stream unless it says so.
+ *  - Bad arguments found on the host return SG_ERR_INVALID_ARG at once.
+ *    Problems found by a kernel (a node ID out of range, a full hash table,
+ *    a repeated seed) set a sticky device error word; sg_stream_check()
+ *    synchronises the stream, reads and clears it.
+ *  - Sizes that depend on the data (|V_h|, E_h) stay on the device.  Calls that
+ *    consume them take a host-side CAPACITY plus an optional device pointer to
+ *    the actual count (d_n / d_dims), so a whole mini-batch can run, and be
+ *    captured in a CUDA graph, without a host synchronisation.
+ */
+#ifndef SG_H
+#define SG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t sg_status;
+#define SG_OK 0
+#define SG_ERR_INVALID_ARG 1    /* a host-side argument is invalid */
+#define SG_ERR_INVALID_INDEX 2  /* a kernel met a node ID / index out of range */
+#define SG_ERR_CAPACITY 3       /* a table or buffer bound was exceeded */
+#define SG_ERR_OOM 4            /* the library could not allocate memory it owns */
+#define SG_ERR_CUDA 5           /* a CUDA runtime call failed (message has the name) */
+#define SG_ERR_TIMEOUT 6        /* a bounded device wait gave up */
+#define SG_ERR_UNSUPPORTED 7    /* valid request this build does not support */
+
+#define SG_F32 0                /* IEEE binary32 */
+#define SG_BF16 1               /* bfloat16, stored as uint16 bit patterns */
+
+#define SG_MAX_HOPS 8
+#define SG_MAX_SUB 64           /* mini-batches per super-batch */
+#define SG_MAX_FANOUT 256
+
+typedef void* sg_stream_t;      /* cudaStream_t */
+
+typedef struct sg_graph sg_graph;
+typedef struct sg_cache sg_cache;
+
+/* Library version (major*10000 + minor*100 + patch). */
+int32_t sg_version(void);
+
+/* Copies the calling thread's last error message into buf (NUL-terminated,
+ * truncated to n bytes); returns the full message length. */
+int32_t sg_last_error(char* buf, size_t n);
+
+/* Synchronises `stream`, then reads and clears the device error word that the
+ * library's kernels set.  Returns SG_OK, SG_ERR_INVALID_INDEX, SG_ERR_CAPACITY,
+ * SG_ERR_INVALID_ARG (repeated seed in one mini-batch) or SG_ERR_CUDA. */
+sg_status sg_stream_check(sg_stream_t stream);
+
+/* ------------------------------------------------------------------ graph */
+/* Loads a CSR graph into HBM (one-time, synchronous).  Row v lists the
+ * neighbours that node v aggregates from (the GARDEN page's N(u), Section
+ * II-A); sampling takes positions of this row.
+ *   h_indptr    host, n_nodes+1 offsets, int32 (offset_bits = 32) or int64
+ *               (offset_bits = 64); must start at 0, be non-decreasing and end
+ *               at n_edges.  int32 offsets need n_edges < 2^31.
+ *   h_indices   host, n_edges int32 node IDs in [0, n_nodes).
+ *   n_nodes     1 .. 2^31-1.
+ * The library copies both arrays (it keeps the offset width given) and
+ * validates them on the GPU; invalid input returns SG_ERR_INVALID_ARG and no
+ * handle.  *out receives a handle freed by sg_graph_destroy. */
+sg_status sg_graph_load(const void* h_indptr, int32_t offset_bits, const int32_t* h_indices,
+                        int64_t n_nodes, int64_t n_edges, sg_graph** out);
+
+/* Frees the graph's device memory (synchronous).  NULL is a no-op. */
+sg_status sg_graph_destroy(sg_graph* g);
+
+/* Shape of a loaded graph; any out pointer may be NULL. */
+sg_status sg_graph_info(const sg_graph* g, int64_t* n_nodes, int64_t* n_edges, int32_t* offset_bits,
+                        int64_t* max_degree);
+
+/* ---------------------------------------------------------------- sampling */
+/* Worst-case sizes of one sampler_run, so the caller can preallocate.
+ * Counts are totals over the n_sub mini-batches of a super-batch. */
+typedef struct sg_sample_bounds {
+    int64_t max_nodes[SG_MAX_HOPS + 1];  /* bound on sum_k |V_h^k|, h = 0..H */
+    int64_t max_edges[SG_MAX_HOPS];      /* bound on sum_k E_h^k, index h-1 */
+    int64_t counts_len;                  /* int32 entries of sg_blocks.counts */
+    size_t workspace_bytes;              /* device workspace sampler_run needs */
+} sg_sample_bounds;
+
+/*   h_batch_ptr  host, n_sub+1 non-decreasing offsets into the seed array
+ *                (GARDEN page Section IV-D "BatchPtr"); NULL means n_sub = 1
+ *                with n_seeds seeds.
+ *   h_fanouts    host, n_hops fanouts; h_fanouts[h-1] is the fanout of hop h,
+ *                hop 1 being the hop next to the seeds; 1..SG_MAX_FANOUT. */
+sg_status sg_sampler_bounds(const sg_graph* g, int32_t n_seeds, const int32_t* h_batch_ptr, int32_t n_sub,
+                            const int32_t* h_fanouts, int32_t n_hops, sg_sample_bounds* out);
+
+/* Output of sg_sampler_run: caller-allocated DEVICE arrays sized by
+ * sg_sampler_bounds.  With K = n_sub mini-batches laid back to back:
+ *   unique     [max_nodes[H]]  global IDs: mini-batch k's V_H^k occupies
+ *              unique[U_k, U_k + |V_H^k|), U_k = sum_{k'<k} |V_H^k'|; inside
+ *              it, its seeds come first (in the order given) and V_h^k is the
+ *              prefix of length |V_h^k|.
+ *   counts     [counts_len] int32, written on the device:
+ *                counts[h]           = sum_k |V_h^k|     (h = 0..H)
+ *                counts[H+1+h-1]     = sum_k E_h^k       (h = 1..H)
+ *                counts[(2H+1)(1+k) + h]       = |V_h^k|
+ *                counts[(2H+1)(1+k) + H+1+h-1] = E_h^k
+ *   indptr[h-1] [max_nodes[h-1]+1] block CSR of hop h over dst rows: mini-
+ *              batch k's dst d (its local ID, d < |V_{h-1}^k|) is row
+ *              D_k + d with D_k = sum_{k'<k} |V_{h-1}^k'|.
+ *   idx[h-1]   [max_edges[h-1]] src row of each edge: mini-batch k's local
+ *              src ID s (< |V_h^k|) is stored as S_k + s with
+ *              S_k = sum_{k'<k} |V_h^k'|.
+ * For K = 1 this is the plain per-batch block list: idx holds local IDs into
+ * V_h and rows are the local IDs of V_{h-1}.  A hop-h block maps H_h (rows in
+ * V_h order) to H_{h-1}, so aggregate_fwd can run hop H .. 1 on these arrays
+ * directly, with d_dims = counts + (h-1). */
+typedef struct sg_blocks {
+    int32_t* unique;
+    int32_t* counts;
+    int32_t* indptr[SG_MAX_HOPS];
+    int32_t* idx[SG_MAX_HOPS];
+} sg_blocks;
+
+/* Multi-hop sampling plus relabel (GARDEN page Section II-B and Fig. 1;
+ * Section IV-C; Section IV-D; FastGL explainer "Fused-Map").
+ * Hop h = 1..H samples every node v of V_{h-1}: with deg = the length of
+ * v's CSR row and f = h_fanouts[h-1], all positions when deg <= f, otherwise
+ * the f positions j with the smallest keys (r, j), where r is word (j mod 4)
+ * of Philox4x32-10 (Salmon et al., SC'11) with counter (j/4, v, h, 0) and key
+ * (seed & 0xffffffff, seed >> 32); positions are listed in ascending order.
+ * This is a uniform sample without replacement, identical on every device and
+ * on the CPU.  The sampled neighbours not yet in V_{h-1}^k join V_h^k in order
+ * of first occurrence in the hop's edge list, ordered by (dst, position).
+ * A super-batch (n_sub = K > 1) gives exactly the K results of K separate
+ * calls with the same seed; each distinct node is sampled once per hop.
+ *   d_seeds      device, n_seeds int32; seeds of one mini-batch must be
+ *                distinct (else the device error word reports
+ *                SG_ERR_INVALID_ARG) and in [0, n_nodes).
+ *   h_batch_ptr  host, as in sg_sampler_bounds.
+ *   seed / d_seed  the hash seed; when d_seed (device, one uint64) is not
+ *                NULL it overrides `seed` and is read when the kernels run, so
+ *                a captured CUDA graph can be replayed with a new seed.
+ *   d_workspace  device scratch of at least bounds.workspace_bytes, 256-byte
+ *                aligned; contents need no initialisation and are not kept.
+ * Asynchronous on `stream`; no host synchronisation inside. */
+sg_status sg_sampler_run(const sg_graph* g, const int32_t* d_seeds, int32_t n_seeds, const int32_t* h_batch_ptr,
+                         int32_t n_sub, const int32_t* h_fanouts, int32_t n_hops, uint64_t seed,
+                         const uint64_t* d_seed, void* d_workspace, size_t workspace_bytes, const sg_blocks* out,
+                         sg_stream_t stream);
+
+/* Standalone dedup + relabel (the step sampler_run fuses; FastGL explainer
+ * "Fused-Map", GARDEN page Section IV-D hash-table dedup).
+ *   d_prefix    device, n_prefix distinct IDs that keep local IDs 0..n_prefix-1
+ *   d_ids       device, n_ids IDs (non-negative int32)
+ * Output (device): d_unique[0 .. n_unique) = the prefix, then every ID of
+ * d_ids not in the prefix in order of first occurrence; d_local[i] = local ID
+ * of d_ids[i]; *d_n_unique (device int32) = n_unique.
+ *   d_unique    room for n_prefix + n_ids entries
+ *   workspace   sg_relabel_workspace(n_prefix, n_ids) bytes, 256-byte aligned
+ * A repeated prefix ID sets the device error word (SG_ERR_INVALID_ARG). */
+size_t sg_relabel_workspace(int64_t n_prefix, int64_t n_ids);
+sg_status sg_relabel(const int32_t* d_ids, int64_t n_ids, const int32_t* d_prefix, int64_t n_prefix,
+                     int32_t* d_unique, int32_t* d_local, int32_t* d_n_unique, void* d_workspace,
+                     size_t workspace_bytes, sg_stream_t stream);
+
+/* ------------------------------------------------------------------- cache */
+/* Builds the HBM feature cache (GARDEN page Section II-B Fig. 2, Nfeat-Cache;
+ * one-time, synchronous on `stream`).
+ *   h_feat        host feature table, n_nodes x dim, row-major, dtype SG_F32 or
+ *                 SG_BF16.  It must stay valid while the cache lives: rows not
+ *                 cached are read from it zero-copy.  Pinned memory
+ *                 (cudaHostAlloc / cudaHostRegister) is required unless the
+ *                 device can access pageable memory.  May be NULL when
+ *                 n_cache = n_nodes and d_feat gives the rows.
+ *   d_feat        optional device copy of the whole table to fill the cache
+ *                 from (NULL: read the rows from h_feat).
+ *   h_ranked      host, n_cache distinct node IDs; h_ranked[s] goes to cache
+ *                 slot s.  NULL with n_cache = n_nodes caches every node with
+ *                 slot = ID.
+ * The library allocates n_cache rows plus an n_nodes int32 slot map in HBM. */
+sg_status sg_cache_build(const void* h_feat, const void* d_feat, int32_t dtype, int64_t n_nodes, int32_t dim,
+                         const int32_t* h_ranked, int64_t n_cache, sg_cache** out, sg_stream_t stream);
+
+/* Frees the cache's device memory (synchronous).  NULL is a no-op. */
+sg_status sg_cache_destroy(sg_cache* c);
+
+/* Device view of a cache (for callers that want to inspect it). */
+sg_status sg_cache_info(const sg_cache* c, int64_t* n_nodes, int32_t* dim, int32_t* dtype, int64_t* n_cache,
+                        const int32_t** d_slot_of);
+
+typedef struct sg_gather_stats {
+    unsigned long long hits;     /* rows read from the HBM cache */
+    unsigned long long misses;   /* rows read zero-copy from host memory */
+} sg_gather_stats;
+
+/* Feature gather through the cache (GARDEN page Section II-B, Nfeat-
+ * Selecting): for i < n, out row i = feature row d_ids[i], byte for byte,
+ * taken from the HBM cache when the node is cached, else read zero-copy from
+ * the host table.
+ *   d_ids     device, n_cap node IDs
+ *   d_n       device int32 count (n = *d_n <= n_cap) or NULL (n = n_cap)
+ *   d_out     device, n_cap x dim in the cache's dtype (rows >= n untouched)
+ *   d_stats   device, accumulated (+=) hit/miss counters, or NULL
+ * An ID out of range sets the device error word and its row is zero-filled. */
+sg_status sg_gather(const sg_cache* c, const int32_t* d_ids, int64_t n_cap, const int32_t* d_n, void* d_out,
+                    sg_gather_stats* d_stats, sg_stream_t stream);
+
+/* -------------------------------------------------------------- aggregate */
+/* Mean aggregation over one block (GARDEN page Section II-A Eq. (1) with
+ * AGGREGATE = mean):
+ *   out[v,:] = (1/c_v) * sum_{e in row v} h[idx[e],:],  c_v = row length,
+ *   out[v,:] = 0 when c_v = 0,                          for v < n_dst.
+ * Sums are accumulated in fp32.  dtype_in/dtype_out: SG_F32 -> SG_F32, or
+ * SG_BF16 -> SG_BF16 (round to nearest even) / SG_F32.
+ *   d_indptr  device int32 [n_dst_cap+1], d_idx device int32 [E]
+ *   d_h       device [n_src_cap x dim]; d_out device [n_dst_cap x dim]
+ *   d_dims    device int32[2] = {n_dst, n_src} (each <= its cap) or NULL
+ * An idx outside [0, n_src) sets the device error word (the edge is skipped). */
+sg_status sg_aggregate_fwd(const int32_t* d_indptr, const int32_t* d_idx, int32_t n_dst_cap, int32_t n_src_cap,
+                           const int32_t* d_dims, const void* d_h, int32_t dtype_in, int32_t dim, void* d_out,
+                           int32_t dtype_out, sg_stream_t stream);
+
+/* Workspace of sg_aggregate_bwd for a block with these capacities. */
+size_t sg_aggregate_bwd_workspace(int32_t n_dst_cap, int32_t n_src_cap, int64_t n_edge_cap);
+
+/* Backward of the mean aggregation (the transpose of the map above):
+ *   gsrc[u,:] = sum over edges e = (v -> u) of gdst[v,:] / c_v,  u < n_src,
+ * zero for a u no edge names.  The block is transposed in the workspace (a
+ * sort of the edges by (src, edge), so the summation order is fixed and the
+ * result deterministic), then each src row is one fp32 sum: no float atomics.
+ *   d_gdst   device [n_dst_cap x dim]; d_gsrc device [n_src_cap x dim]
+ *   n_edge_cap  capacity bound on E = indptr[n_dst]
+ * dtypes as in sg_aggregate_fwd. */
+sg_status sg_aggregate_bwd(const int32_t* d_indptr, const int32_t* d_idx, int32_t n_dst_cap, int32_t n_src_cap,
+                           int64_t n_edge_cap, const int32_t* d_dims, const void* d_gdst, int32_t dtype_in,
+                           int32_t dim, void* d_gsrc, int32_t dtype_out, void* d_workspace, size_t workspace_bytes,
+                           sg_stream_t stream);
+
+/* ------------------------------------------------------------ measurement */
+/* Streams `bytes` of device-accessible memory at d_src with 16-byte loads
+ * (a read roofline probe: HBM when d_src is device memory, the host link when
+ * it is pinned host memory) and folds them into *d_sink (device uint32).
+ * bytes must be a multiple of 16 and d_src 16-byte aligned. */
+sg_status sg_read_probe(const void* d_src, int64_t bytes, uint32_t* d_sink, sg_stream_t stream);
+
+/* Evaluates n_calls Philox4x32-10 blocks (the sampler's hash, counters
+ * 0..n_calls-1 under `seed`) across the whole GPU and folds the outputs into
+ * *d_sink (device uint32): the integer-throughput roofline of sampling. */
+sg_status sg_hash_probe(int64_t n_calls, uint64_t seed, uint32_t* d_sink, sg_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SG_H */

@@ -1,0 +1,362 @@
+"""ctypes binding of ``libsg.so`` (declared in include/sg.h).
+
+Argument marshalling only: every function here hands raw device pointers,
+sizes and the current CUDA stream to the C ABI function of the same name;
+all computation runs in the library's kernels.  PyTorch is used for device
+and pinned memory and for streams.  If the library is missing or was not
+built for this machine, loading fails loudly: there is no other code path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+from typing import List, Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import build as _build
+
+SG_OK = 0
+SG_ERR_INVALID_ARG = 1
+SG_ERR_INVALID_INDEX = 2
+SG_ERR_CAPACITY = 3
+SG_ERR_OOM = 4
+SG_ERR_CUDA = 5
+SG_ERR_TIMEOUT = 6
+SG_ERR_UNSUPPORTED = 7
+SG_F32 = 0
+SG_BF16 = 1
+SG_MAX_HOPS = 8
+SG_MAX_SUB = 64
+SG_MAX_FANOUT = 256
+
+_STATUS_NAMES = {0: "SG_OK", 1: "SG_ERR_INVALID_ARG", 2: "SG_ERR_INVALID_INDEX", 3: "SG_ERR_CAPACITY",
+                 4: "SG_ERR_OOM", 5: "SG_ERR_CUDA", 6: "SG_ERR_TIMEOUT", 7: "SG_ERR_UNSUPPORTED"}
+
+# every symbol include/sg.h declares
+EXPORTS = ["sg_version", "sg_last_error", "sg_stream_check", "sg_graph_load", "sg_graph_destroy", "sg_graph_info",
+           "sg_sampler_bounds", "sg_sampler_run", "sg_relabel_workspace", "sg_relabel", "sg_cache_build",
+           "sg_cache_destroy", "sg_cache_info", "sg_gather", "sg_aggregate_fwd", "sg_aggregate_bwd_workspace",
+           "sg_aggregate_bwd", "sg_read_probe", "sg_hash_probe"]
+
+
+class SgError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__("%s: %s" % (_STATUS_NAMES.get(status, str(status)), message))
+        self.status = status
+
+
+class _Bounds(ctypes.Structure):
+    _fields_ = [("max_nodes", ctypes.c_int64 * (SG_MAX_HOPS + 1)),
+                ("max_edges", ctypes.c_int64 * SG_MAX_HOPS),
+                ("counts_len", ctypes.c_int64),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
+class _Blocks(ctypes.Structure):
+    _fields_ = [("unique", ctypes.c_void_p),
+                ("counts", ctypes.c_void_p),
+                ("indptr", ctypes.c_void_p * SG_MAX_HOPS),
+                ("idx", ctypes.c_void_p * SG_MAX_HOPS)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Loads libsg.so (building it first if it is missing or stale and nvcc
+    is available).  Raises if it cannot be loaded."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if build_if_missing and not _build.up_to_date():
+            _build.build()
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError("libsg.so is missing; run sampling_gnn_mini_gb300.build.build()")
+        lib = ctypes.CDLL(_build.LIB)
+        vp, i32, i64, u64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_size_t
+        sig = {
+            "sg_version": (i32, []),
+            "sg_last_error": (i32, [ctypes.c_char_p, sz]),
+            "sg_stream_check": (i32, [vp]),
+            "sg_graph_load": (i32, [vp, i32, vp, i64, i64, ctypes.POINTER(vp)]),
+            "sg_graph_destroy": (i32, [vp]),
+            "sg_graph_info": (i32, [vp, vp, vp, vp, vp]),
+            "sg_sampler_bounds": (i32, [vp, i32, vp, i32, vp, i32, ctypes.POINTER(_Bounds)]),
+            "sg_sampler_run": (i32, [vp, vp, i32, vp, i32, vp, i32, u64, vp, vp, sz, ctypes.POINTER(_Blocks), vp]),
+            "sg_relabel_workspace": (sz, [i64, i64]),
+            "sg_relabel": (i32, [vp, i64, vp, i64, vp, vp, vp, vp, sz, vp]),
+            "sg_cache_build": (i32, [vp, vp, i32, i64, i32, vp, i64, ctypes.POINTER(vp), vp]),
+            "sg_cache_destroy": (i32, [vp]),
+            "sg_cache_info": (i32, [vp, vp, vp, vp, vp, vp]),
+            "sg_gather": (i32, [vp, vp, i64, vp, vp, vp, vp]),
+            "sg_aggregate_fwd": (i32, [vp, vp, i32, i32, vp, vp, i32, i32, vp, i32, vp]),
+            "sg_aggregate_bwd_workspace": (sz, [i32, i32, i64]),
+            "sg_aggregate_bwd": (i32, [vp, vp, i32, i32, i64, vp, vp, i32, i32, vp, i32, vp, sz, vp]),
+            "sg_read_probe": (i32, [vp, i64, vp, vp]),
+            "sg_hash_probe": (i32, [i64, u64, vp, vp]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(lib, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = lib
+        return lib
+
+
+def exported_symbols() -> List[str]:
+    lib = load()
+    return [n for n in EXPORTS if hasattr(lib, n)]
+
+
+def sg_last_error() -> str:
+    buf = ctypes.create_string_buffer(1024)
+    load().sg_last_error(buf, 1024)
+    return buf.value.decode(errors="replace")
+
+
+def _check(st: int) -> None:
+    if st != SG_OK:
+        raise SgError(st, sg_last_error())
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, torch.Tensor):
+        return t.data_ptr()
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data
+    return int(t)
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def sg_version() -> int:
+    return int(load().sg_version())
+
+
+def sg_stream_check(stream=None) -> None:
+    _check(load().sg_stream_check(_stream(stream)))
+
+
+# ------------------------------------------------------------------- graph
+class Graph:
+    """Handle of a CSR graph loaded into HBM (freed with the object)."""
+
+    def __init__(self, handle):
+        self._h = handle
+        n, m, ob, md = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int64()
+        _check(load().sg_graph_info(handle, ctypes.byref(n), ctypes.byref(m), ctypes.byref(ob), ctypes.byref(md)))
+        self.n_nodes, self.n_edges, self.offset_bits, self.max_degree = n.value, m.value, ob.value, md.value
+
+    @property
+    def handle(self):
+        return self._h
+
+    def close(self):
+        h, self._h = self._h, None
+        if h and _lib is not None:
+            _lib.sg_graph_destroy(h)
+
+    def __del__(self):
+        self.close()
+
+
+def sg_graph_load(indptr: np.ndarray, indices: np.ndarray, offset_bits: Optional[int] = None) -> Graph:
+    """Copies a host CSR (numpy) into HBM.  offset_bits defaults to the
+    width of indptr's dtype."""
+    indptr = np.ascontiguousarray(indptr)
+    if offset_bits is None:
+        offset_bits = 64 if indptr.dtype == np.int64 else 32
+    indptr = np.ascontiguousarray(indptr, dtype=np.int64 if offset_bits == 64 else np.int32)
+    indices = np.ascontiguousarray(indices, dtype=np.int32)
+    out = ctypes.c_void_p()
+    _check(load().sg_graph_load(indptr.ctypes.data, offset_bits, indices.ctypes.data if len(indices) else None,
+                                len(indptr) - 1, len(indices), ctypes.byref(out)))
+    return Graph(out.value)
+
+
+# ---------------------------------------------------------------- sampling
+@dataclass
+class Bounds:
+    max_nodes: List[int]
+    max_edges: List[int]
+    counts_len: int
+    workspace_bytes: int
+
+
+def sg_sampler_bounds(graph: Graph, n_seeds: int, fanouts: Sequence[int], batch_ptr: Optional[Sequence[int]] = None) -> Bounds:
+    fo = np.ascontiguousarray(fanouts, dtype=np.int32)
+    bp = None if batch_ptr is None else np.ascontiguousarray(batch_ptr, dtype=np.int32)
+    b = _Bounds()
+    _check(load().sg_sampler_bounds(graph.handle, int(n_seeds), None if bp is None else bp.ctypes.data,
+                                    1 if bp is None else len(bp) - 1, fo.ctypes.data, len(fo), ctypes.byref(b)))
+    H = len(fo)
+    return Bounds([int(b.max_nodes[h]) for h in range(H + 1)], [int(b.max_edges[h]) for h in range(H)],
+                  int(b.counts_len), int(b.workspace_bytes))
+
+
+def _aligned_bytes(nbytes: int, device, align: int = 256) -> torch.Tensor:
+    raw = torch.empty(int(nbytes) + align, dtype=torch.uint8, device=device)
+    off = (-raw.data_ptr()) % align
+    return raw[off:off + int(nbytes)]
+
+
+class SampleBuffers:
+    """Caller-owned device arrays for sg_sampler_run, sized by the bounds."""
+
+    def __init__(self, bounds: Bounds, device="cuda"):
+        self.bounds = bounds
+        H = len(bounds.max_edges)
+        self.n_hops = H
+        self.unique = torch.empty(max(1, bounds.max_nodes[H]), dtype=torch.int32, device=device)
+        self.counts = torch.zeros(bounds.counts_len, dtype=torch.int32, device=device)
+        self.indptr = [torch.empty(bounds.max_nodes[h] + 1, dtype=torch.int32, device=device) for h in range(H)]
+        self.idx = [torch.empty(max(1, bounds.max_edges[h]), dtype=torch.int32, device=device) for h in range(H)]
+        self.workspace = _aligned_bytes(max(256, bounds.workspace_bytes), device)
+        self._blocks = _Blocks()
+        self._blocks.unique = self.unique.data_ptr()
+        self._blocks.counts = self.counts.data_ptr()
+        for h in range(H):
+            self._blocks.indptr[h] = self.indptr[h].data_ptr()
+            self._blocks.idx[h] = self.idx[h].data_ptr()
+
+    def dims(self, h: int) -> torch.Tensor:
+        """Device int32[2] = {|V_{h-1}|, |V_h|} totals for the hop-h block."""
+        return self.counts[h - 1:h + 1]
+
+
+def sg_sampler_run(graph: Graph, seeds: torch.Tensor, fanouts: Sequence[int], seed: int, buffers: SampleBuffers,
+                   batch_ptr: Optional[Sequence[int]] = None, stream=None, d_seed: Optional[torch.Tensor] = None) -> None:
+    fo = np.ascontiguousarray(fanouts, dtype=np.int32)
+    bp = None if batch_ptr is None else np.ascontiguousarray(batch_ptr, dtype=np.int32)
+    assert seeds.dtype == torch.int32 and seeds.is_cuda and seeds.is_contiguous()
+    _check(load().sg_sampler_run(graph.handle, seeds.data_ptr(), int(seeds.numel()),
+                                 None if bp is None else bp.ctypes.data, 1 if bp is None else len(bp) - 1,
+                                 fo.ctypes.data, len(fo), ctypes.c_uint64(seed & 0xFFFFFFFFFFFFFFFF), _ptr(d_seed),
+                                 buffers.workspace.data_ptr(), buffers.workspace.numel(),
+                                 ctypes.byref(buffers._blocks), _stream(stream)))
+
+
+def sg_relabel(ids: torch.Tensor, prefix: torch.Tensor, stream=None):
+    """Returns (unique, local, n_unique) device tensors; unique has room for
+    len(prefix) + len(ids) entries, of which the first n_unique are used."""
+    lib = load()
+    n_ids, n_pre = int(ids.numel()), int(prefix.numel())
+    dev = ids.device if n_ids else prefix.device
+    unique = torch.empty(max(1, n_ids + n_pre), dtype=torch.int32, device=dev)
+    local = torch.empty(max(1, n_ids), dtype=torch.int32, device=dev)
+    n_unique = torch.zeros(1, dtype=torch.int32, device=dev)
+    wsb = lib.sg_relabel_workspace(n_pre, n_ids)
+    if wsb == 0:
+        raise SgError(SG_ERR_INVALID_ARG, "sg_relabel: sizes out of range")
+    ws = _aligned_bytes(wsb, dev)
+    _check(lib.sg_relabel(ids.data_ptr() if n_ids else None, n_ids, prefix.data_ptr() if n_pre else None, n_pre,
+                          unique.data_ptr(), local.data_ptr(), n_unique.data_ptr(), ws.data_ptr(), ws.numel(),
+                          _stream(stream)))
+    return unique, local[:n_ids], n_unique
+
+
+# ------------------------------------------------------------------- cache
+class Cache:
+    """Handle of the HBM feature cache (freed with the object).  Keeps a
+    reference to the host table, which must outlive the cache."""
+
+    def __init__(self, handle, host_ref):
+        self._h = handle
+        self._host_ref = host_ref
+        n, d, dt, c = ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int64()
+        _check(load().sg_cache_info(handle, ctypes.byref(n), ctypes.byref(d), ctypes.byref(dt), ctypes.byref(c), None))
+        self.n_nodes, self.dim, self.dtype, self.n_cache = n.value, d.value, dt.value, c.value
+
+    @property
+    def handle(self):
+        return self._h
+
+    def slot_of_ptr(self) -> int:
+        p = ctypes.c_void_p()
+        _check(load().sg_cache_info(self._h, None, None, None, None, ctypes.byref(p)))
+        return p.value
+
+    def close(self):
+        h, self._h = self._h, None
+        if h and _lib is not None:
+            _lib.sg_cache_destroy(h)
+
+    def __del__(self):
+        self.close()
+
+
+def sg_cache_build(h_feat: Optional[torch.Tensor], d_feat: Optional[torch.Tensor], dtype: int, n_nodes: int, dim: int,
+                   ranked: Optional[np.ndarray], n_cache: int, stream=None) -> Cache:
+    rk = None if ranked is None else np.ascontiguousarray(ranked, dtype=np.int32)
+    out = ctypes.c_void_p()
+    _check(load().sg_cache_build(_ptr(h_feat), _ptr(d_feat), int(dtype), int(n_nodes), int(dim),
+                                 None if rk is None else rk.ctypes.data, int(n_cache), ctypes.byref(out),
+                                 _stream(stream)))
+    return Cache(out.value, h_feat)
+
+
+def sg_gather(cache: Cache, ids: torch.Tensor, n_cap: int, d_n: Optional[torch.Tensor], out: torch.Tensor,
+              stats: Optional[torch.Tensor] = None, stream=None) -> None:
+    _check(load().sg_gather(cache.handle, ids.data_ptr(), int(n_cap), _ptr(d_n), out.data_ptr(), _ptr(stats),
+                            _stream(stream)))
+
+
+# --------------------------------------------------------------- aggregate
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SG_F32
+    if t.dtype in (torch.bfloat16, torch.uint16, torch.int16):
+        return SG_BF16
+    raise TypeError("feature tensors must be float32 or bfloat16")
+
+
+def sg_aggregate_fwd(indptr: torch.Tensor, idx: torch.Tensor, n_dst_cap: int, n_src_cap: int,
+                     dims: Optional[torch.Tensor], h: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    dim = h.shape[1]
+    _check(load().sg_aggregate_fwd(indptr.data_ptr(), idx.data_ptr(), int(n_dst_cap), int(n_src_cap), _ptr(dims),
+                                   h.data_ptr(), _dtype_code(h), int(dim), out.data_ptr(), _dtype_code(out),
+                                   _stream(stream)))
+
+
+def sg_aggregate_bwd_workspace(n_dst_cap: int, n_src_cap: int, n_edge_cap: int) -> int:
+    return int(load().sg_aggregate_bwd_workspace(int(n_dst_cap), int(n_src_cap), int(n_edge_cap)))
+
+
+def sg_aggregate_bwd(indptr: torch.Tensor, idx: torch.Tensor, n_dst_cap: int, n_src_cap: int, n_edge_cap: int,
+                     dims: Optional[torch.Tensor], gdst: torch.Tensor, gsrc: torch.Tensor, workspace: torch.Tensor,
+                     stream=None) -> None:
+    dim = gdst.shape[1]
+    _check(load().sg_aggregate_bwd(indptr.data_ptr(), idx.data_ptr(), int(n_dst_cap), int(n_src_cap),
+                                   int(n_edge_cap), _ptr(dims), gdst.data_ptr(), _dtype_code(gdst), int(dim),
+                                   gsrc.data_ptr(), _dtype_code(gsrc), workspace.data_ptr(), workspace.numel(),
+                                   _stream(stream)))
+
+
+def aligned_workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    return _aligned_bytes(max(256, nbytes), device)
+
+
+def sg_read_probe(src_ptr: int, nbytes: int, sink: torch.Tensor, stream=None) -> None:
+    _check(load().sg_read_probe(int(src_ptr), int(nbytes), sink.data_ptr(), _stream(stream)))
+
+
+def sg_hash_probe(n_calls: int, seed: int, sink: torch.Tensor, stream=None) -> None:
+    _check(load().sg_hash_probe(int(n_calls), ctypes.c_uint64(seed), sink.data_ptr(), _stream(stream)))

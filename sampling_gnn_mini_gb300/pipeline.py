@@ -1,0 +1,98 @@
+"""One mini-batch of the pipeline, end to end, through the C ABI.
+
+Per step (GARDEN page, Section II-B, Fig. 1: sampling runs outward from the
+seeds, aggregation inward from the input nodes):
+  1. sg_sampler_run   V_0 .. V_H and the H blocks (sampling + relabel)
+  2. sg_gather        X = features of V_H through the HBM cache
+  3. sg_aggregate_fwd H_{h-1} = mean over block h of H_h, h = H .. 1 (H_H = X)
+  4. sg_aggregate_bwd G_h = transpose of block h applied to G_{h-1}, h = 1 .. H,
+                      with G_0 = H_0 (the gradient of 0.5 * ||H_0||^2)
+Every size that depends on the sample stays on the device (the calls read
+the counts the sampler wrote), so a step has no host synchronisation and can
+be captured in a CUDA graph and replayed with new seeds (written into the
+device seed buffers first).  This module only allocates buffers and orders
+the calls.
+"""
+from __future__ import annotations
+
+from typing import Optional, Sequence
+
+import torch
+
+from . import binding as sg
+
+
+class MiniBatchPipeline:
+    def __init__(self, graph: sg.Graph, cache: sg.Cache, fanouts: Sequence[int], n_seeds: int,
+                 batch_ptr: Optional[Sequence[int]] = None, backward: bool = True, device="cuda"):
+        self.graph, self.cache = graph, cache
+        self.fanouts = [int(f) for f in fanouts]
+        self.H = len(self.fanouts)
+        self.n_seeds = int(n_seeds)
+        self.batch_ptr = None if batch_ptr is None else [int(x) for x in batch_ptr]
+        self.backward = backward
+        self.bounds = sg.sg_sampler_bounds(graph, n_seeds, self.fanouts, self.batch_ptr)
+        self.buf = sg.SampleBuffers(self.bounds, device)
+        dt = torch.float32 if cache.dtype == sg.SG_F32 else torch.bfloat16
+        self.dtype = dt
+        d = cache.dim
+        nb = self.bounds.max_nodes
+        self.seeds = torch.zeros(max(1, n_seeds), dtype=torch.int32, device=device)
+        self.d_seed = torch.zeros(1, dtype=torch.int64, device=device)
+        # h_feat[h] holds H_h: rows V_h, h = 0..H (h = H is X)
+        self.h_feat = [torch.empty(max(1, nb[h]), d, dtype=dt, device=device) for h in range(self.H + 1)]
+        self.stats = torch.zeros(2, dtype=torch.int64, device=device)
+        if backward:
+            self.g_feat = [self.h_feat[0]] + [torch.empty(max(1, nb[h]), d, dtype=dt, device=device)
+                                              for h in range(1, self.H + 1)]
+            ws = max(sg.sg_aggregate_bwd_workspace(nb[h - 1], nb[h], self.bounds.max_edges[h - 1])
+                     for h in range(1, self.H + 1))
+            self.bwd_ws = sg.aligned_workspace(ws, device)
+
+    @property
+    def counts(self) -> torch.Tensor:
+        return self.buf.counts
+
+    @property
+    def x(self) -> torch.Tensor:
+        return self.h_feat[self.H]
+
+    def set_batch(self, seeds: torch.Tensor, seed: int) -> None:
+        """Copies a new batch's seeds and hash seed into the device buffers."""
+        self.seeds[: seeds.numel()].copy_(seeds, non_blocking=True)
+        self.d_seed.fill_(seed if seed < (1 << 63) else seed - (1 << 64))
+
+    def sample(self, stream=None) -> None:
+        sg.sg_sampler_run(self.graph, self.seeds[: self.n_seeds], self.fanouts, 0, self.buf, self.batch_ptr,
+                          stream=stream, d_seed=self.d_seed)
+
+    def gather(self, stream=None) -> None:
+        H = self.H
+        sg.sg_gather(self.cache, self.buf.unique, self.bounds.max_nodes[H], self.buf.counts[H:H + 1],
+                     self.h_feat[H], self.stats, stream=stream)
+
+    def forward(self, stream=None) -> None:
+        nb = self.bounds.max_nodes
+        for h in range(self.H, 0, -1):
+            sg.sg_aggregate_fwd(self.buf.indptr[h - 1], self.buf.idx[h - 1], nb[h - 1], nb[h], self.buf.dims(h),
+                                self.h_feat[h], self.h_feat[h - 1], stream=stream)
+
+    def backward_pass(self, stream=None) -> None:
+        nb = self.bounds.max_nodes
+        for h in range(1, self.H + 1):
+            sg.sg_aggregate_bwd(self.buf.indptr[h - 1], self.buf.idx[h - 1], nb[h - 1], nb[h],
+                                self.bounds.max_edges[h - 1], self.buf.dims(h), self.g_feat[h - 1], self.g_feat[h],
+                                self.bwd_ws, stream=stream)
+
+    def step(self, stream=None) -> None:
+        """Sample, gather, forward and (if enabled) backward of one batch."""
+        self.sample(stream)
+        self.gather(stream)
+        self.forward(stream)
+        if self.backward:
+            self.backward_pass(stream)
+
+    def host_counts(self):
+        c = self.buf.counts.cpu().tolist()
+        H = self.H
+        return {"nodes": c[: H + 1], "edges": c[H + 1: 2 * H + 1]}
