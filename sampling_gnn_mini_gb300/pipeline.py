@@ -59,6 +59,8 @@ class MiniBatchPipeline:
 
     def set_batch(self, seeds: torch.Tensor, seed: int) -> None:
         """Copies a new batch's seeds and hash seed into the device buffers."""
+        if seeds.numel() != self.n_seeds:
+            raise ValueError("set_batch: expected %d seeds, got %d" % (self.n_seeds, seeds.numel()))
         self.seeds[: seeds.numel()].copy_(seeds, non_blocking=True)
         self.d_seed.fill_(seed if seed < (1 << 63) else seed - (1 << 64))
 

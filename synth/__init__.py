@@ -160,3 +160,18 @@ def batch_seeds(n: int, p_mask: float, batch: int, bsize: int, seed: int = 0, ep
 
 def mask_count(n: int, p_mask: float, seed: int = 0) -> int:
     return int(_load().synth_mask_count(int(n), float(p_mask), int(seed)))
+
+
+class BatchStream:
+    """Seed batches of a workload, epoch after epoch: batch b is batch
+    (b mod n) of epoch epoch0 + b // n, n = batches per epoch (full batches
+    of the training mask only)."""
+
+    def __init__(self, w, epoch0: int = 0):
+        self.w = w
+        self.epoch0 = epoch0
+        self.per_epoch = max(1, mask_count(w.n_nodes, w.p_mask, w.rng_seed) // w.batch)
+
+    def seeds(self, b: int) -> np.ndarray:
+        ep, i = divmod(int(b), self.per_epoch)
+        return batch_seeds(self.w.n_nodes, self.w.p_mask, i, self.w.batch, self.w.rng_seed, self.epoch0 + ep)

@@ -47,7 +47,11 @@ class Workload:
 
     def sampler_seed(self, batch: int) -> int:
         """Hash seed of mini-batch (or super-batch) ``batch``."""
-        return ((self.rng_seed & 0xFFFFFFFF) << 32) | (batch & 0xFFFFFFFF)
+        return ((self.rng_seed & 0xFFFFFFFF) << 32) | (batch & 0x7FFFFFFF)
+
+    def presample_seed(self, batch: int) -> int:
+        """Hash seed of presampling batch ``batch`` (never a measured batch's)."""
+        return ((self.rng_seed & 0xFFFFFFFF) << 32) | 0x80000000 | (batch & 0x7FFFFFFF)
 
     def scaled(self, n_nodes: int, **kw) -> "Workload":
         """Same recipe on fewer nodes (for oracle-sized parity cases)."""
