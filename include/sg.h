@@ -188,6 +188,28 @@ sg_status sg_relabel(const int32_t* d_ids, int64_t n_ids, const int32_t* d_prefi
                      int32_t* d_unique, int32_t* d_local, int32_t* d_n_unique, void* d_workspace,
                      size_t workspace_bytes, sg_stream_t stream);
 
+/* Relabel that allocates nothing, for callers that cannot call cudaMalloc or
+ * hand the library a workspace: a plugin or kernel-launch hook inside another
+ * framework whose memory is owned by that framework's allocator, a process
+ * with a fixed device-memory budget, or a code path where an allocation would
+ * synchronise the device.  The pages have no counterpart of this call; it is
+ * an interface convenience of this library.
+ * Same inputs, outputs and result as sg_relabel, but its scratch is a static
+ * device array of SG_RELABEL_NOALLOC_SCRATCH_BYTES (11 MiB) inside the library,
+ * which every GPU that loads the library keeps until the process exits.
+ *   n_prefix + n_ids  at most SG_RELABEL_NOALLOC_MAX_IDS (262,144); larger
+ *                     requests return SG_ERR_INVALID_ARG (use sg_relabel).
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any CUDA stream capture.
+ * Every call on a device shares the one array: calls whose GPU work overlaps
+ * (on different streams) race and give wrong results; serialise them.  The
+ * array's previous contents are never relied on (the hash table is cleared
+ * at the start of each call). */
+#define SG_RELABEL_NOALLOC_MAX_IDS 262144
+#define SG_RELABEL_NOALLOC_SCRATCH_BYTES (11u << 20)
+sg_status sg_relabel_noalloc(const int32_t* d_ids, int64_t n_ids, const int32_t* d_prefix, int64_t n_prefix,
+                             int32_t* d_unique, int32_t* d_local, int32_t* d_n_unique, sg_stream_t stream);
+
 /* ------------------------------------------------------------------- cache */
 /* Builds the HBM feature cache (GARDEN page Section II-B Fig. 2, Nfeat-Cache;
  * one-time, synchronous on `stream`).

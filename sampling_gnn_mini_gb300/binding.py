@@ -40,7 +40,7 @@ _STATUS_NAMES = {0: "SG_OK", 1: "SG_ERR_INVALID_ARG", 2: "SG_ERR_INVALID_INDEX",
 EXPORTS = ["sg_version", "sg_last_error", "sg_stream_check", "sg_graph_load", "sg_graph_destroy", "sg_graph_info",
            "sg_sampler_bounds", "sg_sampler_run", "sg_relabel_workspace", "sg_relabel", "sg_cache_build",
            "sg_cache_destroy", "sg_cache_info", "sg_gather", "sg_aggregate_fwd", "sg_aggregate_bwd_workspace",
-           "sg_aggregate_bwd", "sg_read_probe", "sg_hash_probe"]
+           "sg_aggregate_bwd", "sg_read_probe", "sg_hash_probe", "sg_relabel_noalloc"]
 
 
 class SgError(RuntimeError):
@@ -104,6 +104,7 @@ def load(build_if_missing: bool = True):
             "sg_aggregate_bwd": (i32, [vp, vp, i32, i32, i64, vp, vp, i32, i32, vp, i32, vp, sz, vp]),
             "sg_read_probe": (i32, [vp, i64, vp, vp]),
             "sg_hash_probe": (i32, [i64, u64, vp, vp]),
+            "sg_relabel_noalloc": (i32, [vp, i64, vp, i64, vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -360,3 +361,15 @@ def sg_read_probe(src_ptr: int, nbytes: int, sink: torch.Tensor, stream=None) ->
 
 def sg_hash_probe(n_calls: int, seed: int, sink: torch.Tensor, stream=None) -> None:
     _check(load().sg_hash_probe(int(n_calls), ctypes.c_uint64(seed), sink.data_ptr(), _stream(stream)))
+
+
+SG_RELABEL_NOALLOC_MAX_IDS = 262144
+
+
+def sg_relabel_noalloc(ids: torch.Tensor, prefix: torch.Tensor, unique: torch.Tensor, local: torch.Tensor,
+                       n_unique: torch.Tensor, stream=None) -> None:
+    """Relabel into caller-provided outputs with no allocation by the library
+    (its scratch is a static device array; see include/sg.h)."""
+    n_ids, n_pre = int(ids.numel()), int(prefix.numel())
+    _check(load().sg_relabel_noalloc(ids.data_ptr() if n_ids else None, n_ids, prefix.data_ptr() if n_pre else None,
+                                     n_pre, unique.data_ptr(), local.data_ptr(), n_unique.data_ptr(), _stream(stream)))

@@ -865,3 +865,103 @@ extern "C" sg_status sg_relabel(const int32_t* d_ids, int64_t n_ids, const int32
     SG_CUDA(cudaMemcpyAsync(d_n_unique, a.counts + L.tot_n(1), sizeof(int32_t), cudaMemcpyDeviceToDevice, s));
     return SG_OK;
 }
+
+// ------------------------------------------- relabel without allocation
+// The scratch of sg_relabel_noalloc: a static device array, so callers that
+// cannot allocate device memory still get a relabel.  Host code must not use
+// the array's name as an address; the device address is looked up once per
+// device with cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_relabel_scratch[SG_RELABEL_NOALLOC_SCRATCH_BYTES];
+
+#include <mutex>
+
+namespace {
+std::mutex g_scratch_mu;
+void* g_scratch_addr[64] = {nullptr};
+
+sg_status relabel_scratch_address(void** out) {
+    int dev = 0;
+    SG_CUDA(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return fail(SG_ERR_UNSUPPORTED, "sg_relabel_noalloc: device ordinal %d >= 64", dev);
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_relabel_scratch);
+        if (e != cudaSuccess || !p) return cuda_fail(e, "sg_relabel_noalloc: cudaGetSymbolAddress of the static scratch");
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return SG_OK;
+}
+}  // namespace
+
+extern "C" sg_status sg_relabel_noalloc(const int32_t* d_ids, int64_t n_ids, const int32_t* d_prefix, int64_t n_prefix,
+                                        int32_t* d_unique, int32_t* d_local, int32_t* d_n_unique, sg_stream_t stream) {
+    if (n_ids < 0 || n_prefix < 0) return fail(SG_ERR_INVALID_ARG, "sg_relabel_noalloc: negative size");
+    if (n_ids + n_prefix > SG_RELABEL_NOALLOC_MAX_IDS)
+        return fail(SG_ERR_INVALID_ARG,
+                    "sg_relabel_noalloc: n_prefix + n_ids = %lld exceeds the static scratch limit of %d IDs; "
+                    "use sg_relabel with a caller workspace",
+                    (long long)(n_ids + n_prefix), SG_RELABEL_NOALLOC_MAX_IDS);
+    RelabelPlan p;
+    if (!relabel_plan(n_prefix, n_ids, &p) || p.total > SG_RELABEL_NOALLOC_SCRATCH_BYTES)
+        return fail(SG_ERR_INVALID_ARG, "sg_relabel_noalloc: sizes out of range");
+    if ((n_ids > 0 && (!d_ids || !d_local)) || (n_prefix > 0 && !d_prefix) || !d_unique || !d_n_unique)
+        return fail(SG_ERR_INVALID_ARG, "sg_relabel_noalloc: NULL array");
+    void* scratch = nullptr;
+    sg_status st = relabel_scratch_address(&scratch);
+    if (st != SG_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    char* ws = (char*)scratch;
+    CountsLayout L{1};
+    HopArgs a;
+    a.indptr = nullptr;
+    a.indices = nullptr;
+    a.n_nodes = 2147483647LL;
+    a.K = 1;
+    a.logT = p.logT;
+    a.capU = p.capU;
+    a.key0 = a.key1 = 0;
+    a.d_seed = nullptr;
+    a.lambda_num = 0;
+    a.pos_base = (int32_t)p.capU;
+    a.L = L;
+    a.counts = (int32_t*)(ws + p.o_counts);
+    a.ustr = d_unique;
+    a.table = (uint2*)(ws + p.o_table);
+    a.dst_gid = nullptr;
+    a.dbin = nullptr;
+    a.order = nullptr;
+    a.enbr = (int32_t*)(ws + p.o_enbr);
+    a.eslot = (int32_t*)(ws + p.o_eslot);
+    a.eflag = (uint8_t*)(ws + p.o_eflag);
+    a.bsum = (int32_t*)(ws + p.o_bsum);
+    a.epre = (int32_t*)(ws + p.o_epre);
+    a.h = 1;
+    a.fanout = 1;
+    a.bindptr = nullptr;
+    a.bidx = d_local;
+    // the array keeps the previous call's contents: the table must start empty
+    SG_CUDA(cudaMemsetAsync(a.table, 0xFF, ((size_t)1 << p.logT) * sizeof(uint2), s));
+    SubPtr bp;
+    bp.v[0] = 0;
+    bp.v[1] = (int32_t)n_prefix;
+    const int sms = num_sms();
+    k_seed_init<<<n_prefix > 0 ? (int)cdiv(n_prefix, 256) : 1, 256, 0, s>>>(d_prefix, (int32_t)n_prefix, bp, 1, a.n_nodes,
+                                                                          a.table, p.logT, a.ustr, p.capU, a.counts, L);
+    SG_CHECK_LAUNCH("k_seed_init");
+    int64_t ib = cdiv(n_ids, 256);
+    if (ib > (int64_t)sms * 8) ib = (int64_t)sms * 8;
+    if (ib < 1) ib = 1;
+    k_relabel_insert<<<(unsigned)ib, 256, 0, s>>>(d_ids, n_ids, a.table, p.logT, a.pos_base, a.enbr, a.eslot, a.epre);
+    SG_CHECK_LAUNCH("k_relabel_insert");
+    a.G_e = seg_blocks(n_ids, 4096);
+    k_flag<<<a.G_e, kNT, 0, s>>>(a);
+    SG_CHECK_LAUNCH("k_flag");
+    k_assign<<<a.G_e, kNT, 0, s>>>(a);
+    SG_CHECK_LAUNCH("k_assign");
+    k_map<<<(unsigned)ib, kNT, 0, s>>>(a);
+    SG_CHECK_LAUNCH("k_map");
+    SG_CUDA(cudaMemcpyAsync(d_n_unique, a.counts + L.tot_n(1), sizeof(int32_t), cudaMemcpyDeviceToDevice, s));
+    return SG_OK;
+}
