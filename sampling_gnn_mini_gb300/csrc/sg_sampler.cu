@@ -9,25 +9,34 @@
 //    ("random node") without altering the sampling distribution.  The draw is
 //    the bottom-f positions by the key (Philox word, position).
 //  - Section IV-D: mini-batches of a super-batch are stored back to back with a
-//    BatchPtr; dedup goes through a GPU hash table; node classification is
-//    turned into index arithmetic by a flag + exclusive scan (no atomics on the
-//    placement), generalised here from two classes to four degree bins.
-//  - FastGL explainer page, "Fused-Map": the hash insert and the local-ID
-//    bookkeeping share one pass; here the insert records the minimum edge
-//    position per node (atomicMin), so the numbering is the deterministic
-//    first-occurrence order instead of the atomic arrival order.
+//    BatchPtr; dedup goes through GPU hash tables; node classification is
+//    turned into index arithmetic (here: degree bins that order the work).
+//    A node that appears in several mini-batches of the super-batch is
+//    sampled once per hop and its sample copied to the others.
+//  - FastGL explainer page, "Fused-Map": there one atomic pass builds the
+//    table and hands out local IDs in arrival order.  Here the insert pass
+//    keeps the minimum edge position per node (atomicMin) and one flag + scan
+//    pass turns that into the deterministic first-occurrence numbering.
 //
-// Per hop the kernels are:
-//   dst_count  c_v = min(deg, f) and the degree bin of every dst row
-//   dst_scan   block row pointer (exclusive scan of c_v) and bin order
-//              (largest rows first), per mini-batch edge offsets
-//   sample     one warp per dst row in bin order: copy a full row, or hash
-//              every position of a random row with Philox, keep the positions
-//              under a threshold as candidates, and pick the f smallest keys
-//              exactly; each emitted neighbour is inserted in the table
-//   flag       is edge e the first occurrence of its node in this hop?
-//   assign     local IDs of new nodes = |V_{h-1}^k| + rank of first occurrence
-//   map        src ID of every edge
+// Per hop h four kernels run (five for a super-batch):
+//   k_rows     [the map of hop h-1's edges, fused] and one pass over the dst
+//              rows V_{h-1}: c_v = min(deg, f), the block row pointer by a
+//              single-pass exclusive scan (decoupled look-back), per-row
+//              metadata, and the rows' degree bins (work order, largest first)
+//   k_sample   rows by bin: a warp per large row, an 8-lane group per small
+//              row; full rows are copied, random rows hashed with Philox;
+//              keys under a threshold are candidates and the f smallest are
+//              picked exactly
+//   k_copy     (super-batch only) rows whose node another row samples copy it
+//   k_insert   every sampled neighbour goes into its mini-batch's table with
+//              value = its edge position (atomicMin keeps the first)
+//   k_relabel  first-occurrence flags, ranked by a single-pass scan per
+//              mini-batch: new local IDs into the table and into V_h
+// and k_finish maps the last hop's edges (and lays a super-batch out).
+#include <string.h>
+
+#include <mutex>
+
 #include "sg_internal.cuh"
 #include "sg_objects.cuh"
 
@@ -37,25 +46,19 @@ using namespace sgi;
 
 namespace {
 
-constexpr int kNT = 256;            // threads of the segmented scan kernels
-constexpr int kSampleNT = 256;      // threads of the sample kernel (8 warps)
-constexpr int kCandCap = 256;       // candidate slots per warp
-constexpr int kMaxSeg = 1024;       // blocks of a segmented pass
+constexpr int kNT = 256;             // threads of every sampler kernel (8 warps)
+constexpr int kTile = 1024;          // rows / edges per scan tile (4 per thread)
+constexpr int kWarpCap = 256;        // candidate slots of a warp
+constexpr int kGroupCap = 128;       // candidate slots of an 8-lane group
+constexpr int kGroupLambdaMax = 64;  // groups take random rows only when f + 2 sqrt(f) + 4 <= this
 constexpr uint32_t kEmpty = 0xFFFFFFFFu;
-
-// bins: 0 full row, 1 random deg <= 256, 2 random deg <= 4096, 3 random larger
-__device__ __forceinline__ int degree_bin(int64_t deg, int f) {
-    if (deg <= f) return 0;
-    if (deg <= 256) return 1;
-    if (deg <= 4096) return 2;
-    return 3;
-}
+constexpr int kSpinLimit = 1 << 22;  // bound of a look-back wait (then the error word is set)
 
 struct SubPtr {
     int32_t v[SG_MAX_SUB + 1];
 };
 
-// Where the counts of hop h live (see sg_blocks in sg.h).
+// Where the counts live (see sg_blocks in sg.h).
 struct CountsLayout {
     int H;
     __host__ __device__ __forceinline__ int tot_n(int h) const { return h; }
@@ -91,7 +94,7 @@ __device__ __forceinline__ int table_insert(uint2* tab, int logT, int32_t key, u
 // index k with sp[k] <= x < sp[k+1] over a non-decreasing sp[0..K]; for ties
 // (empty mini-batches) the last k with sp[k] <= x.
 __device__ __forceinline__ int find_sub(const int32_t* sp, int K, int64_t x) {
-    int lo = 0, hi = K;  // answer in [0, K-1]
+    int lo = 0, hi = K;
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
         if ((int64_t)sp[mid] <= x) lo = mid; else hi = mid;
@@ -99,11 +102,7 @@ __device__ __forceinline__ int find_sub(const int32_t* sp, int K, int64_t x) {
     return lo;
 }
 
-template <typename Off>
-__device__ __forceinline__ int64_t row_start(const Off* indptr, int32_t v) { return (int64_t)indptr[v]; }
-
-// Loads the per-mini-batch sizes of hop h into shared memory as an exclusive
-// prefix: pre[k] = sum_{k'<k} counts[sub_n(k', h)], pre[K] = total.
+// pre[k] = sum_{k'<k} counts[sub_n(k', h)], pre[K] = total (shared memory).
 __device__ void load_prefix_sub_n(const int32_t* counts, CountsLayout L, int K, int h, int32_t* pre) {
     if (threadIdx.x == 0) {
         int32_t acc = 0;
@@ -116,7 +115,60 @@ __device__ void load_prefix_sub_n(const int32_t* counts, CountsLayout L, int K, 
     __syncthreads();
 }
 
-// ----------------------------------------------------------------- seeds
+// ------------------------------------------------- single-pass scan chains
+// Tile status words: (state << 32) | value, state 0 empty, 1 aggregate,
+// 2 inclusive prefix.  A block publishes its tile's aggregate, then walks back
+// over its predecessors until one has an inclusive prefix (decoupled
+// look-back).  Tiles are handed out in increasing order by an atomic counter,
+// so every predecessor belongs to a block that is already running; each wait
+// is still bounded and, if the bound is hit, reports ERR_TIMEOUT.
+__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Exclusive prefix of tile t in the chain whose first tile is t0.  Called by
+// all 32 lanes of one warp: the warp reads 32 predecessors at once, adds the
+// aggregates up to the closest inclusive prefix, and moves the window back by
+// 32 only while none is inclusive.
+__device__ int32_t chain_lookback(unsigned long long* status, int t, int t0, int32_t agg) {
+    const int lane = (int)lane_id();
+    if (t == t0) {
+        if (lane == 0) st_release(status + t, (2ull << 32) | (uint32_t)agg);
+        return 0;
+    }
+    if (lane == 0) st_release(status + t, (1ull << 32) | (uint32_t)agg);
+    int32_t excl = 0;
+    for (int top = t - 1;; top -= 32) {
+        const int p = top - lane;
+        unsigned long long s = 2ull << 32;  // before the chain: an inclusive zero
+        if (p >= t0) {
+            int spins = 0;
+            while (true) {
+                s = ld_acquire(status + p);
+                if ((s >> 32) != 0 || ++spins >= kSpinLimit) break;
+                __nanosleep(32);
+            }
+            if ((s >> 32) == 0) {
+                dev_err(ERR_TIMEOUT);
+                s = 2ull << 32;
+            }
+        }
+        const unsigned incl = __ballot_sync(0xffffffffu, (s >> 32) == 2);
+        const int first = incl ? __ffs(incl) - 1 : 31;
+        excl += warp_sum(lane <= first ? (int32_t)(uint32_t)s : 0);
+        if (incl) break;
+    }
+    if (lane == 0) st_release(status + t, (2ull << 32) | (uint32_t)(excl + agg));
+    return excl;
+}
+
+// ------------------------------------------------------------------ seeds
 // Seeds take local IDs 0..B_k-1 of their mini-batch.  A repeated seed inside
 // one mini-batch or an ID out of range is reported through the error word.
 __global__ void k_seed_init(const int32_t* __restrict__ seeds, int32_t n_seeds, SubPtr bptr, int K, int64_t n_nodes,
@@ -140,7 +192,7 @@ __global__ void k_seed_init(const int32_t* __restrict__ seeds, int32_t n_seeds, 
     if (present) dev_err(ERR_ARG);
 }
 
-// --------------------------------------------------------------- dst_count
+// ---------------------------------------------------------------- hop args
 struct HopArgs {
     const void* indptr;
     const int32_t* indices;
@@ -155,158 +207,180 @@ struct HopArgs {
     int32_t* counts;
     int32_t* ustr;
     uint2* table;
-    int32_t* dst_gid;
-    uint8_t* dbin;
-    int32_t* order;
+    // this hop's rows
+    int4* rmeta;             // per row: start lo, start hi, degree, node ID
+    int32_t* bins;           // 4 lists of row indices, stride bin_stride
+    int64_t bin_stride;
+    uint32_t* ctr;           // [0] row tiles, [1] edge tiles, [2..5] bin sizes
+    unsigned long long* row_status;
+    unsigned long long* edge_status;
     int32_t* bindptr;
-    int32_t* bidx;
     int32_t* epre;           // [K+1] edge offset of each mini-batch in this hop
     int32_t* enbr;
     int32_t* eslot;
-    uint8_t* eflag;
-    int32_t* bsum;           // [kMaxSeg * 8]
-    int G_d, G_e;
+    // super-batch owner rows
+    uint2* utab;
+    int logU;
+    int32_t* rslot;
+    // the previous hop's edges (mapped by k_rows)
+    int32_t* prev_bidx;
+    const int32_t* prev_epre;
+    const int32_t* prev_eslot;
+    int map_blocks;
 };
 
-template <typename Off>
-__global__ void __launch_bounds__(kNT) k_dst_count(HopArgs a) {
-    __shared__ int32_t pre[SG_MAX_SUB + 1];
-    __shared__ int32_t red[kNT / 32 + 1];
-    load_prefix_sub_n(a.counts, a.L, a.K, a.h - 1, pre);
-    const int64_t T = pre[a.K];
-    int64_t lo, hi;
-    segment_of(T, blockIdx.x, gridDim.x, lo, hi);
-    const Off* indptr = (const Off*)a.indptr;
-    int32_t csum = 0, nb[4] = {0, 0, 0, 0};
-    for (int64_t r = lo + threadIdx.x; r < hi; r += kNT) {
-        const int k = find_sub(pre, a.K, r);
-        const int32_t v = a.ustr[(int64_t)k * a.capU + (r - pre[k])];
-        int64_t deg = 0;
-        if (v >= 0 && (int64_t)v < a.n_nodes) deg = (int64_t)indptr[v + 1] - (int64_t)indptr[v];
-        else dev_err(ERR_INDEX);
-        const int32_t c = (int32_t)(deg < a.fanout ? deg : a.fanout);
-        const int b = degree_bin(deg, a.fanout);
-        a.dst_gid[r] = v;
-        a.dbin[r] = (uint8_t)b;
-        a.bindptr[r] = c;  // row length for now; dst_scan turns it into offsets
-        csum += c;
-        nb[b]++;
-    }
-    int32_t t;
-    t = block_sum<kNT>(csum, red);
-    if (threadIdx.x == 0) a.bsum[blockIdx.x * 8 + 0] = t;
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-        t = block_sum<kNT>(nb[b], red);
-        if (threadIdx.x == 0) a.bsum[blockIdx.x * 8 + 1 + b] = t;
+// bins: 0 full row, 1 small random row (group path), 2 random row (warp),
+// 3 random row longer than 4096 (warp, first)
+__device__ __forceinline__ int degree_bin(int64_t deg, int f, bool group_ok) {
+    if (deg <= f) return 0;
+    if (deg <= 256 && group_ok) return 1;
+    if (deg <= 4096) return 2;
+    return 3;
+}
+
+// Edge e of the previous hop gets its src row (mini-batch offset + local ID).
+// spre holds the prefix of the mini-batches' node counts of that hop.
+__device__ void map_prev_edges(const HopArgs& a, int blk, int nblk, int32_t* ep, const int32_t* spre) {
+    const int K = a.K;
+    for (int k = threadIdx.x; k <= K; k += kNT) ep[k] = a.prev_epre[k];
+    __syncthreads();
+    const int64_t E = ep[K];
+    for (int64_t e = (int64_t)blk * kNT + threadIdx.x; e < E; e += (int64_t)nblk * kNT) {
+        const int32_t s = a.prev_eslot[e];
+        int32_t out = -1;
+        if (s >= 0) {
+            const int k = K == 1 ? 0 : find_sub(ep, K, e);
+            out = spre[k] + (int32_t)a.table[s].y;
+        }
+        a.prev_bidx[e] = out;
     }
 }
 
-// ---------------------------------------------------------------- dst_scan
-__global__ void __launch_bounds__(kNT) k_dst_scan(HopArgs a) {
+template <typename Off>
+__global__ void __launch_bounds__(kNT) k_rows(HopArgs a) {
     __shared__ int32_t pre[SG_MAX_SUB + 1];
+    __shared__ int32_t ep[SG_MAX_SUB + 1];
     __shared__ int32_t red[kNT / 32 + 1];
-    __shared__ unsigned long long red64[kNT / 32 + 1];
-    __shared__ int32_t carry[5], base[4], total_c;
-    load_prefix_sub_n(a.counts, a.L, a.K, a.h - 1, pre);
+    __shared__ int32_t s_tile, s_excl, s_bcnt[4], s_bbase[4];
+    load_prefix_sub_n(a.counts, a.L, a.K, a.h - 1, pre);  // V_{h-1} per mini-batch
     const int64_t T = pre[a.K];
-    // prefixes over earlier blocks and totals over all blocks
-    int32_t my[5] = {0, 0, 0, 0, 0}, all[5] = {0, 0, 0, 0, 0};
-    for (int b = threadIdx.x; b < (int)gridDim.x; b += kNT) {
-#pragma unroll
-        for (int q = 0; q < 5; ++q) {
-            const int32_t x = a.bsum[b * 8 + q];
-            all[q] += x;
-            if (b < (int)blockIdx.x) my[q] += x;
-        }
-    }
-#pragma unroll
-    for (int q = 0; q < 5; ++q) {
-        const int32_t s1 = block_sum<kNT>(my[q], red);
-        const int32_t s2 = block_sum<kNT>(all[q], red);
-        if (threadIdx.x == 0) {
-            carry[q] = s1;
-            if (q == 0) total_c = s2;
-            else my[q] = s2;  // thread 0 keeps the bin totals
-        }
-    }
-    if (threadIdx.x == 0) {
-        // bin order: largest rows first (bin 3, 2, 1, then full rows)
-        base[3] = 0;
-        base[2] = my[4];
-        base[1] = my[4] + my[3];
-        base[0] = my[4] + my[3] + my[2];
-    }
-    __syncthreads();
-    int64_t lo, hi;
-    segment_of(T, blockIdx.x, gridDim.x, lo, hi);
-    for (int64_t t0 = lo; t0 < hi; t0 += kNT) {
-        const int64_t r = t0 + threadIdx.x;
-        const bool in = r < hi;
-        const int32_t c = in ? a.bindptr[r] : 0;
-        const int b = in ? (int)a.dbin[r] : 0;
-        int32_t tc;
-        const int32_t ex = block_excl_scan<kNT>(c, red, tc);
-        const unsigned long long bits = in ? (1ull << (16 * b)) : 0ull;
-        unsigned long long tb;
-        const unsigned long long exb = block_excl_scan<kNT>(bits, red64, tb);
-        if (in) {
-            const int32_t off = carry[0] + ex;
-            a.bindptr[r] = off;
-            const int32_t rank = (int32_t)((exb >> (16 * b)) & 0xFFFFull);
-            a.order[base[b] + carry[1 + b] + rank] = (int32_t)r;
-            // edge offset of every mini-batch whose first dst row is r
-            int k = find_sub(pre, a.K, r);
-            while (k >= 0 && pre[k] == r) {
-                a.epre[k] = off;
-                --k;
-            }
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            carry[0] += tc;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) carry[1 + q] += (int32_t)((tb >> (16 * q)) & 0xFFFFull);
-        }
-        __syncthreads();
-    }
     if (blockIdx.x == 0 && threadIdx.x == 0) {
-        a.bindptr[T] = total_c;
-        a.counts[a.L.tot_e(a.h)] = total_c;
-        for (int k = a.K; k >= 0 && pre[k] == T; --k) a.epre[k] = total_c;
+        a.counts[a.L.tot_n(a.h - 1)] = (int32_t)T;
+        if (T == 0) {
+            a.bindptr[0] = 0;
+            a.counts[a.L.tot_e(a.h)] = 0;
+            for (int k = 0; k <= a.K; ++k) a.epre[k] = 0;
+        }
+    }
+    if ((int)blockIdx.x < a.map_blocks) {  // the previous hop's edges
+        map_prev_edges(a, blockIdx.x, a.map_blocks, ep, pre);
+        return;
+    }
+    const Off* indptr = (const Off*)a.indptr;
+    const int f = a.fanout;
+    const bool group_ok = a.lambda_num <= (uint32_t)kGroupLambdaMax;
+    const int64_t n_tiles = (T + kTile - 1) / kTile;
+    while (true) {
+        if (threadIdx.x == 0) s_tile = (int32_t)atomicAdd(a.ctr + 0, 1u);
+        __syncthreads();
+        const int64_t tile = s_tile;
+        if (tile >= n_tiles) break;
+        const int64_t r0 = tile * kTile + (int64_t)threadIdx.x * 4;
+        int32_t c[4];
+        int b[4];
+        int32_t mysum = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int64_t r = r0 + q;
+            c[q] = 0;
+            b[q] = -1;
+            if (r < T) {
+                const int k = find_sub(pre, a.K, r);
+                const int32_t v = a.ustr[(int64_t)k * a.capU + (r - pre[k])];
+                int64_t start = 0, deg = 0;
+                if (v >= 0 && (int64_t)v < a.n_nodes) {
+                    start = (int64_t)indptr[v];
+                    deg = (int64_t)indptr[v + 1] - start;
+                } else {
+                    dev_err(ERR_INDEX);
+                }
+                c[q] = (int32_t)(deg < f ? deg : f);
+                b[q] = degree_bin(deg, f, group_ok);
+                a.rmeta[r] = make_int4((int32_t)(uint32_t)start, (int32_t)(start >> 32), (int32_t)deg, v);
+                if (a.utab) {  // super-batch: the first row of a node samples it
+                    a.rslot[r] = (v >= 0 && (int64_t)v < a.n_nodes)
+                                     ? table_insert(a.utab, a.logU, v, (uint32_t)r, nullptr) : -1;
+                }
+            }
+            mysum += c[q];
+        }
+        int32_t tile_total;
+        const int32_t ex = block_excl_scan<kNT>(mysum, red, tile_total);
+        if (threadIdx.x < 32) {
+            const int32_t x = chain_lookback(a.row_status, (int)tile, 0, tile_total);
+            if (threadIdx.x == 0) s_excl = x;
+        }
+        // bin sizes of the tile, then one global atomic per bin
+        if (threadIdx.x < 4) s_bcnt[threadIdx.x] = 0;
+        __syncthreads();
+        int brank[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) brank[q] = b[q] >= 0 ? atomicAdd(&s_bcnt[b[q]], 1) : 0;
+        __syncthreads();
+        if (threadIdx.x < 4) s_bbase[threadIdx.x] = s_bcnt[threadIdx.x] ? (int32_t)atomicAdd(a.ctr + 2 + threadIdx.x, (uint32_t)s_bcnt[threadIdx.x]) : 0;
+        __syncthreads();
+        int32_t off = s_excl + ex;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int64_t r = r0 + q;
+            if (r < T) {
+                a.bindptr[r] = off;
+                int k = find_sub(pre, a.K, r);
+                while (k >= 0 && pre[k] == r) {  // first row of mini-batch k (and of empty ones before it)
+                    a.epre[k] = off;
+                    --k;
+                }
+            }
+            off += c[q];
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (b[q] >= 0) a.bins[b[q] * a.bin_stride + s_bbase[b[q]] + brank[q]] = (int32_t)(r0 + q);
+        if (tile == n_tiles - 1 && threadIdx.x == kNT - 1) {
+            const int32_t E = s_excl + tile_total;
+            a.bindptr[T] = E;
+            a.counts[a.L.tot_e(a.h)] = E;
+            for (int k = a.K; k >= 0 && pre[k] == T; --k) a.epre[k] = E;
+        }
+        __syncthreads();
     }
 }
 
 // ------------------------------------------------------------------ sample
-__device__ __forceinline__ void emit_edge(const HopArgs& a, uint2* tab, int64_t e, int32_t u) {
-    a.enbr[e] = u;
-    const int s = table_insert(tab, a.logT, u, (uint32_t)(a.pos_base + e), nullptr);
-    a.eslot[e] = s < 0 ? -1 : (int32_t)((int64_t)(tab - a.table) + s);
-}
+__device__ __forceinline__ void emit_edge(const HopArgs& a, int64_t e, int32_t u) { a.enbr[e] = u; }
 
-__device__ __forceinline__ unsigned long long warp_min_u64(unsigned long long x) {
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) {
-        const unsigned long long o = __shfl_xor_sync(0xffffffffu, x, d);
+__device__ __forceinline__ unsigned long long min_u64_xor(unsigned long long x, unsigned mask, int width) {
+    for (int d = width >> 1; d > 0; d >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(mask, x, d, width);
         x = o < x ? o : x;
     }
     return x;
 }
 
-// Exact bottom-f by f passes of a warp-wide minimum over all positions
-// (rarely used: only when the threshold filter cannot hold or find f keys).
-template <typename Off>
-__device__ void sample_exact(const HopArgs& a, uint2* tab, int32_t v, int64_t start, int64_t deg, int64_t out0,
-                             int32_t* cj) {
-    const unsigned lane = lane_id();
+// Exact bottom-f by f passes of a group-wide minimum over all positions;
+// used only when the threshold filter cannot hold or find f keys.  A group is
+// W lanes (8 or 32) named by `mask`; cj has room for f entries.
+template <int W>
+__device__ void sample_exact(const HopArgs& a, uint32_t k0, uint32_t k1, int32_t v, int64_t start,
+                             int64_t deg, int64_t out0, int32_t* cj, unsigned mask, int gl) {
     const int f = a.fanout;
     unsigned long long prev = 0;
     for (int s = 0; s < f; ++s) {
         unsigned long long best = ~0ull;
-        for (int64_t base = 0; base < deg; base += 128) {
-            const int64_t q = (base >> 2) + lane;
+        for (int64_t base = 0; base < deg; base += 4 * W) {
+            const int64_t q = (base >> 2) + gl;
             if (4 * q < deg) {
-                const uint4 w = philox4x32_10(make_uint4((uint32_t)q, (uint32_t)v, (uint32_t)a.h, 0u), a.key0, a.key1);
+                const uint4 w = philox4x32_10(make_uint4((uint32_t)q, (uint32_t)v, (uint32_t)a.h, 0u), k0, k1);
                 const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
@@ -318,78 +392,61 @@ __device__ void sample_exact(const HopArgs& a, uint2* tab, int32_t v, int64_t st
                 }
             }
         }
-        best = warp_min_u64(best);
-        if (lane == 0) cj[s] = (int32_t)(best & 0xFFFFFFFFull);
+        best = min_u64_xor(best, mask, W);
+        if (gl == 0) cj[s] = (int32_t)(best & 0xFFFFFFFFull);
         prev = best;
     }
-    __syncwarp();
-    // list the f positions in ascending order (rank among distinct values)
-    for (int i = lane; i < f; i += 32) {
+    __syncwarp(mask);
+    for (int i = gl; i < f; i += W) {  // list the f positions in ascending order
         const int32_t x = cj[i];
         int rank = 0;
         for (int t = 0; t < f; ++t) rank += cj[t] < x;
-        const int32_t u = a.indices[start + x];
-        emit_edge(a, tab, out0 + rank, u);
+        emit_edge(a, out0 + rank, a.indices[start + x]);
     }
-    __syncwarp();
+    __syncwarp(mask);
 }
 
-template <typename Off>
-__global__ void __launch_bounds__(kSampleNT) k_sample(HopArgs a) {
-    __shared__ int32_t pre[SG_MAX_SUB + 1];
-    __shared__ uint32_t cand_r[kSampleNT / 32][kCandCap];
-    __shared__ int32_t cand_j[kSampleNT / 32][kCandCap];
-    load_prefix_sub_n(a.counts, a.L, a.K, a.h - 1, pre);
-    const int64_t T = pre[a.K];
-    const unsigned lane = lane_id();
-    const int wib = threadIdx.x >> 5;
-    uint32_t* cr = cand_r[wib];
-    int32_t* cj = cand_j[wib];
-    const Off* indptr = (const Off*)a.indptr;
+// One random row by a group of W lanes (W = 8 or 32) named by `mask`:
+// hash every position (4 per lane per step), keep keys <= tau in position
+// order (candidate buffer of CAP), rank them by (key, position) and emit the
+// f smallest in position order.  Falls back to sample_exact when the filter
+// overflows the buffer or, after two widenings, still holds fewer than f keys.
+template <int W, int CAP>
+__device__ void sample_random_row(const HopArgs& a, uint32_t k0, uint32_t k1, int32_t v, int64_t start,
+                                  int64_t deg, int64_t out0, uint32_t* cr, int32_t* cj, unsigned mask, int gl) {
     const int f = a.fanout;
-    const int64_t nwarps = (int64_t)gridDim.x * (kSampleNT / 32);
-    if (a.d_seed) {
-        const uint64_t sd = *a.d_seed;
-        a.key0 = (uint32_t)(sd & 0xFFFFFFFFull);
-        a.key1 = (uint32_t)(sd >> 32);
-    }
-    for (int64_t i = blockIdx.x * (int64_t)(kSampleNT / 32) + wib; i < T; i += nwarps) {
-        const int32_t r = a.order[i];
-        const int32_t v = a.dst_gid[r];
-        if (v < 0 || (int64_t)v >= a.n_nodes) continue;  // reported by dst_count
-        const int64_t start = (int64_t)indptr[v];
-        const int64_t deg = (int64_t)indptr[v + 1] - start;
-        const int64_t out0 = a.bindptr[r];
-        const int k = find_sub(pre, a.K, r);
-        uint2* tab = a.table + ((int64_t)k << a.logT);
-        if (deg <= f) {  // full node: every neighbour, in row order
-            for (int64_t t = lane; t < deg; t += 32) emit_edge(a, tab, out0 + t, a.indices[start + t]);
-            continue;
-        }
-        // random node: candidates are the positions whose key is <= tau
-        const unsigned long long lam = a.lambda_num;
-        unsigned long long tau64 = (lam << 32) / (unsigned long long)deg;
-        uint32_t tau = tau64 > 0xFFFFFFFFull ? 0xFFFFFFFFu : (uint32_t)tau64;
-        bool done = false;
-        for (int attempt = 0; attempt < 3 && !done; ++attempt) {
-            int n = 0;
-            bool overflow = false;
-            for (int64_t base = 0; base < deg; base += 128) {
-                const int64_t q = (base >> 2) + lane;
-                uint4 w = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty);
-                if (4 * q < deg)
-                    w = philox4x32_10(make_uint4((uint32_t)q, (uint32_t)v, (uint32_t)a.h, 0u), a.key0, a.key1);
-                const int64_t j0 = 4 * q;
+    const int shift = (int)(lane_id() & ~(unsigned)(W - 1));  // first lane of the group
+    const unsigned ltg = (1u << gl) - 1u;
+    const unsigned long long tau64 = ((unsigned long long)a.lambda_num << 32) / (unsigned long long)deg;
+    uint32_t tau = tau64 > 0xFFFFFFFFull ? 0xFFFFFFFFu : (uint32_t)tau64;
+    for (int attempt = 0; attempt < 3; ++attempt) {
+        int n = 0;
+        bool overflow = false;
+        // each step covers 8W positions: counter blocks q (first half) and
+        // q + W (second half) of every lane; appending is skipped unless some
+        // key of the step passes the threshold
+        for (int64_t base = 0; base < deg && !overflow; base += 8 * W) {
+            const int64_t qa = (base >> 2) + gl, qb = qa + W;
+            uint4 wa = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty), wb = wa;
+            if (4 * qa < deg) wa = philox4x32_10(make_uint4((uint32_t)qa, (uint32_t)v, (uint32_t)a.h, 0u), k0, k1);
+            if (4 * qb < deg) wb = philox4x32_10(make_uint4((uint32_t)qb, (uint32_t)v, (uint32_t)a.h, 0u), k0, k1);
+            const uint32_t lo = min(min(wa.x, wa.y), min(wa.z, wa.w)), hi = min(min(wb.x, wb.y), min(wb.z, wb.w));
+            // lanes past the row end hold kEmpty keys; a real key equal to
+            // kEmpty passes only when tau = kEmpty, and then the row is short
+            if (!__any_sync(mask, lo <= tau || hi <= tau)) continue;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const uint4 w = half ? wb : wa;
+                const int64_t j0 = 4 * (half ? qb : qa);
                 const bool p0 = j0 + 0 < deg && w.x <= tau;
                 const bool p1 = j0 + 1 < deg && w.y <= tau;
                 const bool p2 = j0 + 2 < deg && w.z <= tau;
                 const bool p3 = j0 + 3 < deg && w.w <= tau;
-                const unsigned m0 = __ballot_sync(0xffffffffu, p0), m1 = __ballot_sync(0xffffffffu, p1);
-                const unsigned m2 = __ballot_sync(0xffffffffu, p2), m3 = __ballot_sync(0xffffffffu, p3);
-                const unsigned lt = lanemask_lt();
-                const int before = __popc(m0 & lt) + __popc(m1 & lt) + __popc(m2 & lt) + __popc(m3 & lt);
+                const unsigned m0 = __ballot_sync(mask, p0) >> shift, m1 = __ballot_sync(mask, p1) >> shift;
+                const unsigned m2 = __ballot_sync(mask, p2) >> shift, m3 = __ballot_sync(mask, p3) >> shift;
+                const int before = __popc(m0 & ltg) + __popc(m1 & ltg) + __popc(m2 & ltg) + __popc(m3 & ltg);
                 const int tot = __popc(m0) + __popc(m1) + __popc(m2) + __popc(m3);
-                if (n + tot > kCandCap) {
+                if (n + tot > CAP) {
                     overflow = true;
                     break;
                 }
@@ -400,151 +457,317 @@ __global__ void __launch_bounds__(kSampleNT) k_sample(HopArgs a) {
                 if (p3) { cr[p] = w.w; cj[p] = (int32_t)(j0 + 3); ++p; }
                 n += tot;
             }
-            __syncwarp();
-            if (overflow) break;
-            if (n < f) {  // too few under the threshold: widen it and retry
-                tau = tau > 0x3FFFFFFFu ? 0xFFFFFFFFu : (tau << 2) | 3u;
-                __syncwarp();
+        }
+        __syncwarp(mask);
+        if (overflow) break;
+        if (n < f) {  // too few under the threshold: widen it and retry
+            tau = tau > 0x3FFFFFFFu ? 0xFFFFFFFFu : (tau << 2) | 3u;
+            __syncwarp(mask);
+            continue;
+        }
+        int sel_before = 0;
+        for (int c0 = 0; c0 < n; c0 += W) {
+            const int ci = c0 + gl;
+            bool sel = false;
+            if (ci < n) {
+                const uint32_t ri = cr[ci];
+                int rank = 0;
+                for (int t = 0; t < n; ++t) {
+                    const uint32_t rt = cr[t];
+                    rank += (rt < ri) || (rt == ri && t < ci);
+                }
+                sel = rank < f;
+            }
+            const unsigned m = __ballot_sync(mask, sel) >> shift;
+            if (sel) emit_edge(a, out0 + sel_before + __popc(m & ltg), a.indices[start + cj[ci]]);
+            sel_before += __popc(m);
+        }
+        __syncwarp(mask);
+        return;
+    }
+    sample_exact<W>(a, k0, k1, v, start, deg, out0, cj, mask, gl);
+}
+
+// Row r of the frontier, by a group of W lanes.
+template <int W, int CAP>
+__device__ void sample_row(const HopArgs& a, int32_t r, const int32_t* pre, uint32_t k0, uint32_t k1, uint32_t* cr,
+                           int32_t* cj, unsigned mask, int gl) {
+    const int4 m = a.rmeta[r];
+    const int32_t v = m.w;
+    const int64_t deg = m.z;
+    if (v < 0 || (int64_t)v >= a.n_nodes || deg == 0) return;
+    if (a.utab && (a.rslot[r] < 0 || (int32_t)a.utab[a.rslot[r]].y != r)) return;  // another row samples this node
+    const int64_t start = (int64_t)(uint32_t)m.x | ((int64_t)m.y << 32);
+    const int64_t out0 = a.bindptr[r];
+    if (deg <= a.fanout) {  // full node: every neighbour, in row order
+        for (int64_t t = gl; t < deg; t += W) emit_edge(a, out0 + t, a.indices[start + t]);
+        return;
+    }
+    sample_random_row<W, CAP>(a, k0, k1, v, start, deg, out0, cr, cj, mask, gl);
+}
+
+// A random row longer than 4096 by the whole block: each thread hashes one
+// counter block (4 positions) per step, candidates gather in shared memory
+// (order across warps is arbitrary, so the pick ranks by (key, position) and
+// the output is ordered by position afterwards).
+__device__ void sample_big_row(const HopArgs& a, int32_t r, uint32_t k0, uint32_t k1, uint32_t* cr, int32_t* cj,
+                               int32_t* s_n, int32_t* s_over) {
+    constexpr int CAPB = 2048;  // candidates; cr[CAPB..2*CAPB) holds the pick flags
+    const int4 m = a.rmeta[r];
+    const int32_t v = m.w;
+    const int64_t deg = m.z;
+    if (v < 0 || (int64_t)v >= a.n_nodes || deg <= a.fanout) return;
+    if (a.utab && (a.rslot[r] < 0 || (int32_t)a.utab[a.rslot[r]].y != r)) return;
+    const int64_t start = (int64_t)(uint32_t)m.x | ((int64_t)m.y << 32);
+    const int64_t out0 = a.bindptr[r];
+    const int f = a.fanout;
+    const unsigned lane = lane_id();
+    const unsigned long long tau64 = ((unsigned long long)a.lambda_num << 32) / (unsigned long long)deg;
+    uint32_t tau = tau64 > 0xFFFFFFFFull ? 0xFFFFFFFFu : (uint32_t)tau64;
+    for (int attempt = 0; attempt < 3; ++attempt) {
+        if (threadIdx.x == 0) {
+            *s_n = 0;
+            *s_over = 0;
+        }
+        __syncthreads();
+        for (int64_t base = 0; base < deg; base += 4 * kNT) {
+            const int64_t q = (base >> 2) + threadIdx.x;
+            uint4 w = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty);
+            if (4 * q < deg) w = philox4x32_10(make_uint4((uint32_t)q, (uint32_t)v, (uint32_t)a.h, 0u), k0, k1);
+            const uint32_t mn = min(min(w.x, w.y), min(w.z, w.w));
+            if (!__any_sync(0xffffffffu, mn <= tau)) continue;
+            const int64_t j0 = 4 * q;
+            const bool p0 = j0 + 0 < deg && w.x <= tau;
+            const bool p1 = j0 + 1 < deg && w.y <= tau;
+            const bool p2 = j0 + 2 < deg && w.z <= tau;
+            const bool p3 = j0 + 3 < deg && w.w <= tau;
+            const unsigned m0 = __ballot_sync(0xffffffffu, p0), m1 = __ballot_sync(0xffffffffu, p1);
+            const unsigned m2 = __ballot_sync(0xffffffffu, p2), m3 = __ballot_sync(0xffffffffu, p3);
+            const unsigned lt = lanemask_lt();
+            const int before = __popc(m0 & lt) + __popc(m1 & lt) + __popc(m2 & lt) + __popc(m3 & lt);
+            const int tot = __popc(m0) + __popc(m1) + __popc(m2) + __popc(m3);
+            if (tot == 0) continue;
+            int wbase = 0;
+            if (lane == 0) wbase = atomicAdd(s_n, tot);
+            wbase = __shfl_sync(0xffffffffu, wbase, 0);
+            if (wbase + tot > CAPB) {
+                if (lane == 0) *s_over = 1;
                 continue;
             }
-            // exact bottom-f among the candidates: rank by (key, position)
-            int sel_before = 0;
-            for (int c0 = 0; c0 < n; c0 += 32) {
-                const int ci = c0 + lane;
-                bool sel = false;
-                if (ci < n) {
-                    const uint32_t ri = cr[ci];
-                    int rank = 0;
-                    for (int t = 0; t < n; ++t) {
-                        const uint32_t rt = cr[t];
-                        rank += (rt < ri) || (rt == ri && t < ci);
-                    }
-                    sel = rank < f;
-                }
-                const unsigned m = __ballot_sync(0xffffffffu, sel);
-                if (sel) {
-                    const int o = sel_before + __popc(m & lanemask_lt());
-                    emit_edge(a, tab, out0 + o, a.indices[start + cj[ci]]);
-                }
-                sel_before += __popc(m);
-            }
-            __syncwarp();
-            done = true;
+            int p = wbase + before;
+            if (p0) { cr[p] = w.x; cj[p] = (int32_t)(j0 + 0); ++p; }
+            if (p1) { cr[p] = w.y; cj[p] = (int32_t)(j0 + 1); ++p; }
+            if (p2) { cr[p] = w.z; cj[p] = (int32_t)(j0 + 2); ++p; }
+            if (p3) { cr[p] = w.w; cj[p] = (int32_t)(j0 + 3); ++p; }
         }
-        if (!done) sample_exact<Off>(a, tab, v, start, deg, out0, cj);
+        __syncthreads();
+        const int n = *s_n;
+        const bool over = *s_over != 0;
+        __syncthreads();
+        if (over) break;
+        if (n < f) {  // too few under the threshold: widen it and retry
+            tau = tau > 0x3FFFFFFFu ? 0xFFFFFFFFu : (tau << 2) | 3u;
+            continue;
+        }
+        uint32_t* picked = cr + CAPB;
+        for (int i = threadIdx.x; i < n; i += kNT) {  // rank by (key, position)
+            const uint32_t ri = cr[i];
+            const int32_t ji = cj[i];
+            int rank = 0;
+            for (int t = 0; t < n; ++t) rank += cr[t] < ri || (cr[t] == ri && cj[t] < ji);
+            picked[i] = rank < f;
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < n; i += kNT) {  // the picks, by position
+            if (!picked[i]) continue;
+            const int32_t ji = cj[i];
+            int pos = 0;
+            for (int t = 0; t < n; ++t) pos += picked[t] && cj[t] < ji;
+            emit_edge(a, out0 + pos, a.indices[start + ji]);
+        }
+        __syncthreads();
+        return;
     }
+    if (threadIdx.x < 32) sample_exact<32>(a, k0, k1, v, start, deg, out0, cj, 0xffffffffu, (int)lane);
+    __syncthreads();
 }
 
-// -------------------------------------------------------------------- flag
-__global__ void __launch_bounds__(kNT) k_flag(HopArgs a) {
-    __shared__ int32_t red[kNT / 32 + 1];
-    const int64_t E = a.epre[a.K];
-    int64_t lo, hi;
-    segment_of(E, blockIdx.x, gridDim.x, lo, hi);
-    int32_t cnt = 0;
-    for (int64_t e = lo + threadIdx.x; e < hi; e += kNT) {
-        const int32_t s = a.eslot[e];
-        const bool first = s >= 0 && a.table[s].y == (uint32_t)(a.pos_base + e);
-        a.eflag[e] = first;
-        cnt += first;
+__global__ void __launch_bounds__(kNT) k_sample(HopArgs a) {
+    __shared__ int32_t pre[SG_MAX_SUB + 1];
+    __shared__ uint32_t cand_r[kNT / 32][2 * kWarpCap];
+    __shared__ int32_t cand_j[kNT / 32][2 * kWarpCap];
+    __shared__ int32_t s_n, s_over;
+    load_prefix_sub_n(a.counts, a.L, a.K, a.h - 1, pre);
+    uint32_t k0 = a.key0, k1 = a.key1;
+    if (a.d_seed) {
+        const uint64_t sd = *a.d_seed;
+        k0 = (uint32_t)(sd & 0xFFFFFFFFull);
+        k1 = (uint32_t)(sd >> 32);
     }
-    const int32_t t = block_sum<kNT>(cnt, red);
-    if (threadIdx.x == 0) a.bsum[blockIdx.x] = t;
-}
-
-// ------------------------------------------------------------------ assign
-__global__ void __launch_bounds__(kNT) k_assign(HopArgs a) {
-    __shared__ int32_t npre[SG_MAX_SUB + 1];   // |V_{h-1}^k| prefix
-    __shared__ int32_t ep[SG_MAX_SUB + 1];     // edge offset of each mini-batch
-    __shared__ int32_t fpre[SG_MAX_SUB + 1];   // first occurrences before ep[k]
-    __shared__ int32_t red[kNT / 32 + 1];
-    __shared__ int32_t carry;
-    const int K = a.K;
-    load_prefix_sub_n(a.counts, a.L, K, a.h - 1, npre);
-    for (int k = threadIdx.x; k <= K; k += kNT) ep[k] = a.epre[k];
-    __syncthreads();
-    const int64_t E = ep[K];
-    const int G = gridDim.x;
-    const int64_t seglen = (E + G - 1) / G;
-    // fpre[k] = number of flags in [0, ep[k]): whole blocks before the one
-    // holding ep[k], plus the part of that block's segment before ep[k]
-    for (int k = threadIdx.x >> 5; k <= K; k += kNT / 32) {
-        const int64_t ek = ep[k];
-        const int bk = seglen > 0 ? (int)(ek / seglen) : 0;
-        int32_t s = 0;
-        for (int b = lane_id(); b < bk && b < G; b += 32) s += a.bsum[b];
-        const int64_t seg0 = (int64_t)bk * seglen;
-        for (int64_t e = seg0 + lane_id(); e < ek; e += 32) s += a.eflag[e];
-        s = warp_sum(s);
-        if (lane_id() == 0) fpre[k] = s;
-    }
-    int32_t mine = 0;
-    for (int b = threadIdx.x; b < (int)blockIdx.x; b += kNT) mine += a.bsum[b];
-    mine = block_sum<kNT>(mine, red);
-    if (threadIdx.x == 0) carry = mine;
-    __syncthreads();
-    int64_t lo, hi;
-    segment_of(E, blockIdx.x, G, lo, hi);
-    for (int64_t t0 = lo; t0 < hi; t0 += kNT) {
-        const int64_t e = t0 + threadIdx.x;
-        const int32_t fl = e < hi ? (int32_t)a.eflag[e] : 0;
-        int32_t tot;
-        const int32_t ex = block_excl_scan<kNT>(fl, red, tot);
-        if (fl) {
-            const int32_t rank = carry + ex;
-            const int k = find_sub(ep, K, e);
-            const int64_t lid = (int64_t)a.counts[a.L.sub_n(k, a.h - 1)] + (rank - fpre[k]);
-            if (lid >= a.capU) {
-                dev_err(ERR_CAPACITY);
+    const int64_t n0 = a.ctr[2], n1 = a.ctr[3], n2 = a.ctr[4], n3 = a.ctr[5];
+    // rows of bin 3 first, a block each
+    for (int64_t i = blockIdx.x; i < n3; i += gridDim.x)
+        sample_big_row(a, a.bins[3 * a.bin_stride + i], k0, k1, &cand_r[0][0], &cand_j[0][0], &s_n, &s_over);
+    // then work units: one per row of bin 2 (a warp each), one per four rows
+    // of bins 1 and 0 (an 8-lane group each)
+    const int64_t u32 = n2;
+    const int64_t u8a = (n1 + 3) / 4, u8b = (n0 + 3) / 4;
+    const int64_t units = u32 + u8a + u8b;
+    const unsigned lane = lane_id();
+    const int wib = threadIdx.x >> 5;
+    uint32_t* cr = cand_r[wib];
+    int32_t* cj = cand_j[wib];
+    const int64_t nwarps = (int64_t)gridDim.x * (kNT / 32);
+    for (int64_t u = blockIdx.x * (int64_t)(kNT / 32) + wib; u < units; u += nwarps) {
+        if (u < u32) {
+            const int32_t r = a.bins[2 * a.bin_stride + u];
+            sample_row<32, kWarpCap>(a, r, pre, k0, k1, cr, cj, 0xffffffffu, (int)lane);
+        } else {
+            const int g = (int)(lane >> 3), gl = (int)(lane & 7);
+            const unsigned gmask = 0xFFu << (8 * g);
+            int64_t i, n;
+            int bin;
+            if (u < u32 + u8a) {
+                i = (u - u32) * 4 + g;
+                bin = 1;
+                n = n1;
             } else {
-                a.table[a.eslot[e]].y = (uint32_t)lid;
-                a.ustr[(int64_t)k * a.capU + lid] = a.enbr[e];
+                i = (u - u32 - u8a) * 4 + g;
+                bin = 0;
+                n = n0;
+            }
+            if (i < n) {
+                const int32_t r = a.bins[bin * a.bin_stride + i];
+                sample_row<8, kGroupCap>(a, r, pre, k0, k1, cr + g * kGroupCap, cj + g * kGroupCap, gmask, gl);
             }
         }
-        __syncthreads();
-        if (threadIdx.x == 0) carry += tot;
-        __syncthreads();
-    }
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-        int32_t tot_n = 0;
-        for (int k = 0; k < K; ++k) {
-            const int32_t nk = (npre[k + 1] - npre[k]) + (fpre[k + 1] - fpre[k]);
-            a.counts[a.L.sub_n(k, a.h)] = nk;
-            a.counts[a.L.sub_e(k, a.h)] = ep[k + 1] - ep[k];
-            tot_n += nk;
-        }
-        a.counts[a.L.tot_n(a.h)] = tot_n;
+        __syncwarp();
     }
 }
 
-// --------------------------------------------------------------------- map
-__global__ void __launch_bounds__(kNT) k_map(HopArgs a) {
+// --------------------------------------------------------------------- copy
+// Super-batch: a row whose node was sampled by an earlier row (its owner)
+// copies the owner's neighbours into its own edge range.
+__global__ void __launch_bounds__(kNT) k_copy(HopArgs a) {
+    __shared__ int32_t pre[SG_MAX_SUB + 1];
+    load_prefix_sub_n(a.counts, a.L, a.K, a.h - 1, pre);
+    const int64_t T = pre[a.K];
+    const int64_t nwarps = (int64_t)gridDim.x * (kNT / 32);
+    const unsigned lane = lane_id();
+    for (int64_t r = (blockIdx.x * (int64_t)kNT + threadIdx.x) / 32; r < T; r += nwarps) {
+        const int32_t s = a.rslot[r];
+        if (s < 0) continue;
+        const int32_t owner = (int32_t)a.utab[s].y;
+        if (owner == (int32_t)r || owner < 0 || (int64_t)owner >= T) continue;
+        const int64_t o = a.bindptr[r], c = a.bindptr[r + 1] - o, so = a.bindptr[owner];
+        for (int64_t t = lane; t < c; t += 32) emit_edge(a, o + t, a.enbr[so + t]);
+    }
+}
+
+// ------------------------------------------------------------------ insert
+// Every edge's node goes into its mini-batch's table; the value kept is the
+// smallest edge position, i.e. the node's first occurrence in this hop.
+__global__ void __launch_bounds__(kNT) k_insert(HopArgs a) {
     __shared__ int32_t ep[SG_MAX_SUB + 1];
-    __shared__ int32_t spre[SG_MAX_SUB + 1];
     for (int k = threadIdx.x; k <= a.K; k += kNT) ep[k] = a.epre[k];
-    load_prefix_sub_n(a.counts, a.L, a.K, a.h, spre);
+    __syncthreads();
     const int64_t E = ep[a.K];
     for (int64_t e = blockIdx.x * (int64_t)kNT + threadIdx.x; e < E; e += (int64_t)gridDim.x * kNT) {
-        const int32_t s = a.eslot[e];
-        int32_t out = -1;
-        if (s >= 0) {
-            const int k = a.K == 1 ? 0 : find_sub(ep, a.K, e);
-            out = spre[k] + (int32_t)a.table[s].y;
-        }
-        a.bidx[e] = out;
+        const int32_t u = a.enbr[e];
+        const int k = a.K == 1 ? 0 : find_sub(ep, a.K, e);
+        const int s = table_insert(a.table + ((int64_t)k << a.logT), a.logT, u, (uint32_t)(a.pos_base + e), nullptr);
+        a.eslot[e] = s < 0 ? -1 : (int32_t)(((int64_t)k << a.logT) + s);
     }
 }
 
-// ----------------------------------------------------------------- compact
-// Lays the mini-batches' V_H regions out back to back.
-__global__ void k_compact(const int32_t* ustr, int64_t capU, int K, const int32_t* counts, CountsLayout L, int H,
-                          int32_t* unique) {
+// ----------------------------------------------------------------- relabel
+// First-occurrence flags and new local IDs; one scan chain per mini-batch.
+__global__ void __launch_bounds__(kNT) k_relabel(HopArgs a) {
+    __shared__ int32_t ep[SG_MAX_SUB + 1];
+    __shared__ int32_t tpre[SG_MAX_SUB + 1];
+    __shared__ int32_t red[kNT / 32 + 1];
+    __shared__ int32_t s_tile, s_excl;
+    const int K = a.K;
+    if (threadIdx.x == 0) {
+        int32_t acc = 0;
+        for (int k = 0; k <= K; ++k) {
+            ep[k] = a.epre[k];
+            tpre[k] = acc;
+            if (k < K) acc += (a.epre[k + 1] - a.epre[k] + kTile - 1) / kTile;
+        }
+        tpre[K] = acc;
+    }
+    __syncthreads();
+    if (blockIdx.x == 0) {  // mini-batches without edges keep V_{h-1}
+        for (int k = threadIdx.x; k < K; k += kNT) {
+            a.counts[a.L.sub_e(k, a.h)] = ep[k + 1] - ep[k];
+            if (ep[k + 1] == ep[k]) a.counts[a.L.sub_n(k, a.h)] = a.counts[a.L.sub_n(k, a.h - 1)];
+        }
+    }
+    const int n_tiles = tpre[K];
+    while (true) {
+        if (threadIdx.x == 0) s_tile = (int32_t)atomicAdd(a.ctr + 1, 1u);
+        __syncthreads();
+        const int t = s_tile;
+        if (t >= n_tiles) break;
+        const int k = find_sub(tpre, K, t);
+        const int64_t e_end = ep[k + 1];
+        const int64_t e0 = ep[k] + (int64_t)(t - tpre[k]) * kTile + (int64_t)threadIdx.x * 4;
+        bool fl[4];
+        int32_t mine = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int64_t e = e0 + q;
+            fl[q] = false;
+            if (e < e_end) {
+                const int32_t s = a.eslot[e];
+                fl[q] = s >= 0 && a.table[s].y == (uint32_t)(a.pos_base + e);
+            }
+            mine += fl[q];
+        }
+        int32_t tile_total;
+        const int32_t ex = block_excl_scan<kNT>(mine, red, tile_total);
+        if (threadIdx.x < 32) {
+            const int32_t x = chain_lookback(a.edge_status, t, tpre[k], tile_total);
+            if (threadIdx.x == 0) s_excl = x;
+        }
+        __syncthreads();
+        const int32_t n_prev = a.counts[a.L.sub_n(k, a.h - 1)];
+        int32_t rank = s_excl + ex;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (fl[q]) {
+                const int64_t e = e0 + q;
+                const int64_t lid = (int64_t)n_prev + rank;
+                if (lid >= a.capU) {
+                    dev_err(ERR_CAPACITY);
+                } else {
+                    a.table[a.eslot[e]].y = (uint32_t)lid;
+                    a.ustr[(int64_t)k * a.capU + lid] = a.enbr[e];
+                }
+                ++rank;
+            }
+        }
+        if (t == tpre[k + 1] - 1 && threadIdx.x == 0) a.counts[a.L.sub_n(k, a.h)] = n_prev + s_excl + tile_total;
+        __syncthreads();
+    }
+}
+
+// ------------------------------------------------------------------ finish
+// Maps the last hop's edges, writes the last total and, for a super-batch,
+// lays the mini-batches' V_H back to back.
+__global__ void __launch_bounds__(kNT) k_finish(HopArgs a, int32_t* unique_out) {
     __shared__ int32_t pre[SG_MAX_SUB + 1];
-    load_prefix_sub_n(counts, L, K, H, pre);
-    const int64_t n = pre[K];
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-        const int k = find_sub(pre, K, i);
-        unique[i] = ustr[(int64_t)k * capU + (i - pre[k])];
+    __shared__ int32_t ep[SG_MAX_SUB + 1];
+    load_prefix_sub_n(a.counts, a.L, a.K, a.h, pre);
+    if (blockIdx.x == 0 && threadIdx.x == 0) a.counts[a.L.tot_n(a.h)] = pre[a.K];
+    map_prev_edges(a, blockIdx.x, gridDim.x, ep, pre);
+    if (unique_out) {
+        const int64_t n = pre[a.K];
+        for (int64_t i = blockIdx.x * (int64_t)kNT + threadIdx.x; i < n; i += (int64_t)gridDim.x * kNT) {
+            const int k = find_sub(pre, a.K, i);
+            unique_out[i] = a.ustr[(int64_t)k * a.capU + (i - pre[k])];
+        }
     }
 }
 
@@ -568,6 +791,14 @@ __global__ void k_relabel_insert(const int32_t* __restrict__ ids, int64_t n_ids,
 }
 
 // ------------------------------------------------------------------- host
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+int pow2_log(int64_t atleast) {
+    int l = 6;
+    while (((int64_t)1 << l) < atleast) ++l;
+    return l;
+}
+
 struct Plan {
     int K, H;
     int32_t bptr[SG_MAX_SUB + 1];
@@ -575,12 +806,12 @@ struct Plan {
     int64_t nb_tot[SG_MAX_HOPS + 1], eb_tot[SG_MAX_HOPS];
     int64_t capU;      // per mini-batch bound on |V_H^k|
     int logT;          // table slots per mini-batch = 2^logT
+    int logU[SG_MAX_HOPS];
     int64_t nb_max, eb_max;
-    // workspace offsets
-    size_t o_table, o_ustr, o_gid, o_dbin, o_order, o_enbr, o_eslot, o_eflag, o_bsum, o_epre, total;
+    // workspace offsets; [o_table, o_zero) is set to 0xFF and [o_zero, o_rest) to 0 per call
+    size_t o_table, o_utab[SG_MAX_HOPS], o_zero, o_rstat[SG_MAX_HOPS], o_estat[SG_MAX_HOPS], o_ctr, o_rest;
+    size_t o_ustr, o_rmeta, o_rslot, o_bins, o_enbr[2], o_eslot[2], o_epre, total;
 };
-
-size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 sg_status make_plan(const sg_graph* g, int32_t n_seeds, const int32_t* h_bptr, int32_t n_sub, const int32_t* h_fan,
                     int32_t n_hops, Plan* p) {
@@ -632,36 +863,56 @@ sg_status make_plan(const sg_graph* g, int32_t n_seeds, const int32_t* h_bptr, i
     // table values hold local IDs (< capU) and edge positions capU + e
     if (p->capU + p->eb_max >= 2147483647LL || p->nb_tot[n_hops] >= 2147483647LL)
         return fail(SG_ERR_UNSUPPORTED, "sampler: a mini-batch this large needs 64-bit local IDs");
-    int logT = 6;
-    while (((int64_t)1 << logT) < 2 * p->capU) ++logT;
-    p->logT = logT;
+    p->logT = pow2_log(2 * p->capU);
     size_t o = 0;
-    p->o_table = o; o = align256(o + (size_t)K * ((size_t)1 << logT) * sizeof(uint2));
-    p->o_ustr = o;  o = align256(o + (K > 1 ? (size_t)K * (size_t)p->capU * 4 : 0));
-    p->o_gid = o;   o = align256(o + (size_t)p->nb_max * 4);
-    p->o_dbin = o;  o = align256(o + (size_t)p->nb_max);
-    p->o_order = o; o = align256(o + (size_t)p->nb_max * 4);
-    p->o_enbr = o;  o = align256(o + (size_t)p->eb_max * 4);
-    p->o_eslot = o; o = align256(o + (size_t)p->eb_max * 4);
-    p->o_eflag = o; o = align256(o + (size_t)p->eb_max);
-    p->o_bsum = o;  o = align256(o + (size_t)kMaxSeg * 8 * 4);
-    p->o_epre = o;  o = align256(o + (size_t)(SG_MAX_SUB + 1) * 4);
+    p->o_table = o;
+    o = align256(o + (size_t)K * ((size_t)1 << p->logT) * sizeof(uint2));
+    for (int h = 0; h < n_hops; ++h) {
+        p->logU[h] = K > 1 ? pow2_log(2 * p->nb_tot[h]) : 0;
+        p->o_utab[h] = o;
+        if (K > 1) o = align256(o + ((size_t)1 << p->logU[h]) * sizeof(uint2));
+    }
+    p->o_zero = o;
+    for (int h = 0; h < n_hops; ++h) {
+        p->o_rstat[h] = o;
+        o = align256(o + (size_t)(p->nb_tot[h] / kTile + 2) * 8);
+        p->o_estat[h] = o;
+        o = align256(o + (size_t)(p->eb_tot[h] / kTile + K + 2) * 8);
+    }
+    p->o_ctr = o;
+    o = align256(o + (size_t)n_hops * 8 * 4);
+    p->o_rest = o;
+    p->o_ustr = o;
+    o = align256(o + (K > 1 ? (size_t)K * (size_t)p->capU * 4 : 0));
+    p->o_rmeta = o;
+    o = align256(o + (size_t)p->nb_max * 16);
+    p->o_rslot = o;
+    o = align256(o + (K > 1 ? (size_t)p->nb_max * 4 : 0));
+    p->o_bins = o;
+    o = align256(o + 4 * (size_t)p->nb_max * 4);
+    for (int i = 0; i < 2; ++i) {  // edge arrays alternate between hops (k_rows maps the previous hop's)
+        p->o_enbr[i] = o;
+        o = align256(o + (size_t)p->eb_max * 4);
+        p->o_eslot[i] = o;
+        o = align256(o + (size_t)p->eb_max * 4);
+    }
+    p->o_epre = o;
+    o = align256(o + (size_t)(n_hops + 1) * (SG_MAX_SUB + 1) * 4);
     p->total = o;
     return SG_OK;
 }
 
-int seg_blocks(int64_t bound, int64_t per_block) {
-    int64_t b = cdiv(bound, per_block);
-    if (b < 1) b = 1;
-    if (b > kMaxSeg) b = kMaxSeg;
-    return (int)b;
+uint32_t lambda_for(int f) {
+    // expected candidates per random row: f + 2 sqrt(f) + 4 keeps a retry
+    // (fewer than f pass, about 1% of rows) cheap and the candidate set small
+    double lam = f + 2.0 * __builtin_sqrt((double)f) + 4.0;
+    return (uint32_t)lam;
 }
 
-uint32_t lambda_for(int f) {
-    // expected candidates per random row: f + 4 sqrt(f) + 16 keeps fewer than f
-    // (a retry) or more than the warp's 256 slots (the exact path) rare
-    double lam = f + 4.0 * __builtin_sqrt((double)f) + 16.0;
-    return (uint32_t)lam;
+int64_t clamp_blocks(int64_t want, int64_t cap) {
+    if (want > cap) want = cap;
+    if (want < 1) want = 1;
+    return want;
 }
 
 }  // namespace
@@ -696,8 +947,10 @@ extern "C" sg_status sg_sampler_run(const sg_graph* g, const int32_t* d_seeds, i
     cudaStream_t s = (cudaStream_t)stream;
     char* ws = (char*)d_workspace;
     const int K = p.K, H = p.H;
+    const int sms = num_sms();
     CountsLayout L{H};
     HopArgs a;
+    memset(&a, 0, sizeof(a));
     a.indptr = g->indptr;
     a.indices = g->indices;
     a.n_nodes = g->n_nodes;
@@ -712,62 +965,63 @@ extern "C" sg_status sg_sampler_run(const sg_graph* g, const int32_t* d_seeds, i
     a.counts = out->counts;
     a.ustr = K > 1 ? (int32_t*)(ws + p.o_ustr) : out->unique;
     a.table = (uint2*)(ws + p.o_table);
-    a.dst_gid = (int32_t*)(ws + p.o_gid);
-    a.dbin = (uint8_t*)(ws + p.o_dbin);
-    a.order = (int32_t*)(ws + p.o_order);
-    a.enbr = (int32_t*)(ws + p.o_enbr);
-    a.eslot = (int32_t*)(ws + p.o_eslot);
-    a.eflag = (uint8_t*)(ws + p.o_eflag);
-    a.bsum = (int32_t*)(ws + p.o_bsum);
-    a.epre = (int32_t*)(ws + p.o_epre);
+    a.rmeta = (int4*)(ws + p.o_rmeta);
+    a.bins = (int32_t*)(ws + p.o_bins);
+    a.bin_stride = p.nb_max;
+    a.rslot = K > 1 ? (int32_t*)(ws + p.o_rslot) : nullptr;
+    int32_t* epre_all = (int32_t*)(ws + p.o_epre);
 
-    SG_CUDA(cudaMemsetAsync(a.table, 0xFF, (size_t)K * ((size_t)1 << p.logT) * sizeof(uint2), s));
+    SG_CUDA(cudaMemsetAsync(ws + p.o_table, 0xFF, p.o_zero - p.o_table, s));
+    SG_CUDA(cudaMemsetAsync(ws + p.o_zero, 0, p.o_rest - p.o_zero, s));
     SubPtr bp;
     for (int k = 0; k <= K; ++k) bp.v[k] = p.bptr[k];
-    {
-        const int blocks = n_seeds > 0 ? (int)cdiv(n_seeds, 256) : 1;
-        k_seed_init<<<blocks, 256, 0, s>>>(d_seeds, n_seeds, bp, K, g->n_nodes, a.table, p.logT, a.ustr, p.capU,
-                                           out->counts, L);
-        SG_CHECK_LAUNCH("k_seed_init");
-    }
-    const int sms = num_sms();
+    k_seed_init<<<n_seeds > 0 ? (int)cdiv(n_seeds, 256) : 1, 256, 0, s>>>(d_seeds, n_seeds, bp, K, g->n_nodes, a.table,
+                                                                          p.logT, a.ustr, p.capU, out->counts, L);
+    SG_CHECK_LAUNCH("k_seed_init");
+    const int64_t cap_blocks = (int64_t)sms * 8;
     for (int h = 1; h <= H; ++h) {
+        const int cur = (h - 1) & 1, prv = h & 1;
         a.h = h;
         a.fanout = p.fan[h - 1];
         a.lambda_num = lambda_for(a.fanout);
         a.bindptr = out->indptr[h - 1];
-        a.bidx = out->idx[h - 1];
+        a.epre = epre_all + (size_t)h * (SG_MAX_SUB + 1);
+        a.enbr = (int32_t*)(ws + p.o_enbr[cur]);
+        a.eslot = (int32_t*)(ws + p.o_eslot[cur]);
+        a.ctr = (uint32_t*)(ws + p.o_ctr) + (size_t)(h - 1) * 8;
+        a.row_status = (unsigned long long*)(ws + p.o_rstat[h - 1]);
+        a.edge_status = (unsigned long long*)(ws + p.o_estat[h - 1]);
+        a.utab = K > 1 ? (uint2*)(ws + p.o_utab[h - 1]) : nullptr;
+        a.logU = p.logU[h - 1];
+        // the previous hop's edges are mapped inside this hop's row pass
+        a.prev_bidx = h > 1 ? out->idx[h - 2] : nullptr;
+        a.prev_epre = h > 1 ? epre_all + (size_t)(h - 1) * (SG_MAX_SUB + 1) : nullptr;
+        a.prev_eslot = h > 1 ? (const int32_t*)(ws + p.o_eslot[prv]) : nullptr;
         const int64_t nb = p.nb_tot[h - 1], eb = p.eb_tot[h - 1];
-        a.G_d = seg_blocks(nb, 2048);
-        a.G_e = seg_blocks(eb, 4096);
-        if (g->offset_bits == 32) k_dst_count<int32_t><<<a.G_d, kNT, 0, s>>>(a);
-        else k_dst_count<int64_t><<<a.G_d, kNT, 0, s>>>(a);
-        SG_CHECK_LAUNCH("k_dst_count");
-        k_dst_scan<<<a.G_d, kNT, 0, s>>>(a);
-        SG_CHECK_LAUNCH("k_dst_scan");
-        int64_t sb = cdiv(nb, kSampleNT / 32);
-        if (sb > (int64_t)sms * 8) sb = (int64_t)sms * 8;
-        if (sb < 1) sb = 1;
-        if (g->offset_bits == 32) k_sample<int32_t><<<(unsigned)sb, kSampleNT, 0, s>>>(a);
-        else k_sample<int64_t><<<(unsigned)sb, kSampleNT, 0, s>>>(a);
+        a.map_blocks = h > 1 ? (int)clamp_blocks(cdiv(p.eb_tot[h - 2], kNT * 8), cap_blocks) : 0;
+        const int64_t row_blocks = clamp_blocks(cdiv(nb, kTile), cap_blocks);
+        if (g->offset_bits == 32) k_rows<int32_t><<<(unsigned)(a.map_blocks + row_blocks), kNT, 0, s>>>(a);
+        else k_rows<int64_t><<<(unsigned)(a.map_blocks + row_blocks), kNT, 0, s>>>(a);
+        SG_CHECK_LAUNCH("k_rows");
+        k_sample<<<(unsigned)clamp_blocks(cdiv(nb, kNT / 32), cap_blocks), kNT, 0, s>>>(a);
         SG_CHECK_LAUNCH("k_sample");
-        k_flag<<<a.G_e, kNT, 0, s>>>(a);
-        SG_CHECK_LAUNCH("k_flag");
-        k_assign<<<a.G_e, kNT, 0, s>>>(a);
-        SG_CHECK_LAUNCH("k_assign");
-        int64_t mb = cdiv(eb, kNT * 4);
-        if (mb > (int64_t)sms * 8) mb = (int64_t)sms * 8;
-        if (mb < 1) mb = 1;
-        k_map<<<(unsigned)mb, kNT, 0, s>>>(a);
-        SG_CHECK_LAUNCH("k_map");
+        if (K > 1) {
+            k_copy<<<(unsigned)clamp_blocks(cdiv(nb, kNT / 32), cap_blocks), kNT, 0, s>>>(a);
+            SG_CHECK_LAUNCH("k_copy");
+        }
+        k_insert<<<(unsigned)clamp_blocks(cdiv(eb, kNT * 2), cap_blocks), kNT, 0, s>>>(a);
+        SG_CHECK_LAUNCH("k_insert");
+        k_relabel<<<(unsigned)clamp_blocks(cdiv(eb, kTile) + K, cap_blocks), kNT, 0, s>>>(a);
+        SG_CHECK_LAUNCH("k_relabel");
     }
-    if (K > 1) {
-        int64_t cb = cdiv(p.nb_tot[H], 256);
-        if (cb > (int64_t)sms * 8) cb = (int64_t)sms * 8;
-        if (cb < 1) cb = 1;
-        k_compact<<<(unsigned)cb, 256, 0, s>>>(a.ustr, p.capU, K, out->counts, L, H, out->unique);
-        SG_CHECK_LAUNCH("k_compact");
-    }
+    // the last hop's edges, the last total and the super-batch layout
+    a.prev_bidx = out->idx[H - 1];
+    a.prev_epre = epre_all + (size_t)H * (SG_MAX_SUB + 1);
+    a.prev_eslot = (const int32_t*)(ws + p.o_eslot[(H - 1) & 1]);
+    a.h = H;
+    const int64_t fin = p.eb_tot[H - 1] > p.nb_tot[H] ? p.eb_tot[H - 1] : p.nb_tot[H];
+    k_finish<<<(unsigned)clamp_blocks(cdiv(fin, kNT * 4), cap_blocks), kNT, 0, s>>>(a, K > 1 ? out->unique : nullptr);
+    SG_CHECK_LAUNCH("k_finish");
     return SG_OK;
 }
 
@@ -776,25 +1030,79 @@ namespace {
 struct RelabelPlan {
     int logT;
     int64_t capU;
-    size_t o_table, o_enbr, o_eslot, o_eflag, o_bsum, o_epre, o_counts, total;
+    size_t o_table, o_zero, o_estat, o_ctr, o_rest, o_enbr, o_eslot, o_epre, o_counts, total;
 };
 
 bool relabel_plan(int64_t n_prefix, int64_t n_ids, RelabelPlan* p) {
     if (n_prefix < 0 || n_ids < 0 || n_prefix + 2 * n_ids >= 2147483647LL) return false;
     p->capU = n_prefix + n_ids + 1;
-    int logT = 6;
-    while (((int64_t)1 << logT) < 2 * p->capU) ++logT;
-    p->logT = logT;
+    p->logT = pow2_log(2 * p->capU);
     size_t o = 0;
-    p->o_table = o; o = align256(o + ((size_t)1 << logT) * sizeof(uint2));
-    p->o_enbr = o; o = align256(o + (size_t)(n_ids + 1) * 4);
-    p->o_eslot = o; o = align256(o + (size_t)(n_ids + 1) * 4);
-    p->o_eflag = o; o = align256(o + (size_t)(n_ids + 1));
-    p->o_bsum = o; o = align256(o + (size_t)kMaxSeg * 8 * 4);
-    p->o_epre = o; o = align256(o + (size_t)(SG_MAX_SUB + 1) * 4);
-    p->o_counts = o; o = align256(o + 16 * 4);
+    p->o_table = o;
+    o = align256(o + ((size_t)1 << p->logT) * sizeof(uint2));
+    p->o_zero = o;
+    p->o_estat = o;
+    o = align256(o + (size_t)(n_ids / kTile + 3) * 8);
+    p->o_ctr = o;
+    o = align256(o + 8 * 4);
+    p->o_rest = o;
+    p->o_enbr = o;
+    o = align256(o + (size_t)(n_ids + 1) * 4);
+    p->o_eslot = o;
+    o = align256(o + (size_t)(n_ids + 1) * 4);
+    p->o_epre = o;
+    o = align256(o + (size_t)(SG_MAX_SUB + 1) * 4);
+    p->o_counts = o;
+    o = align256(o + 16 * 4);
     p->total = o;
     return true;
+}
+
+// Runs the standalone relabel with its scratch at ws (layout of relabel_plan).
+sg_status relabel_launch(const RelabelPlan& p, char* ws, const int32_t* d_ids, int64_t n_ids, const int32_t* d_prefix,
+                         int64_t n_prefix, int32_t* d_unique, int32_t* d_local, int32_t* d_n_unique, cudaStream_t s) {
+    CountsLayout L{1};
+    HopArgs a;
+    memset(&a, 0, sizeof(a));
+    a.n_nodes = 2147483647LL;
+    a.K = 1;
+    a.logT = p.logT;
+    a.capU = p.capU;
+    a.pos_base = (int32_t)p.capU;
+    a.L = L;
+    a.counts = (int32_t*)(ws + p.o_counts);
+    a.ustr = d_unique;
+    a.table = (uint2*)(ws + p.o_table);
+    a.enbr = (int32_t*)(ws + p.o_enbr);
+    a.eslot = (int32_t*)(ws + p.o_eslot);
+    a.epre = (int32_t*)(ws + p.o_epre);
+    a.ctr = (uint32_t*)(ws + p.o_ctr);
+    a.edge_status = (unsigned long long*)(ws + p.o_estat);
+    a.h = 1;
+    a.fanout = 1;
+    // the scratch may hold a previous call's contents: the table and the scan
+    // state are cleared before use, everything else is written before it is read
+    SG_CUDA(cudaMemsetAsync(ws + p.o_table, 0xFF, p.o_zero - p.o_table, s));
+    SG_CUDA(cudaMemsetAsync(ws + p.o_zero, 0, p.o_rest - p.o_zero, s));
+    SubPtr bp;
+    bp.v[0] = 0;
+    bp.v[1] = (int32_t)n_prefix;
+    const int sms = num_sms();
+    k_seed_init<<<n_prefix > 0 ? (int)cdiv(n_prefix, 256) : 1, 256, 0, s>>>(d_prefix, (int32_t)n_prefix, bp, 1, a.n_nodes,
+                                                                          a.table, p.logT, a.ustr, p.capU, a.counts, L);
+    SG_CHECK_LAUNCH("k_seed_init");
+    const int64_t ib = clamp_blocks(cdiv(n_ids, 256), (int64_t)sms * 8);
+    k_relabel_insert<<<(unsigned)ib, 256, 0, s>>>(d_ids, n_ids, a.table, p.logT, a.pos_base, a.enbr, a.eslot, a.epre);
+    SG_CHECK_LAUNCH("k_relabel_insert");
+    k_relabel<<<(unsigned)clamp_blocks(cdiv(n_ids, kTile) + 1, (int64_t)sms * 8), kNT, 0, s>>>(a);
+    SG_CHECK_LAUNCH("k_relabel");
+    a.prev_bidx = d_local;
+    a.prev_epre = a.epre;
+    a.prev_eslot = a.eslot;
+    k_finish<<<(unsigned)ib, kNT, 0, s>>>(a, nullptr);
+    SG_CHECK_LAUNCH("k_finish");
+    SG_CUDA(cudaMemcpyAsync(d_n_unique, a.counts + L.tot_n(1), sizeof(int32_t), cudaMemcpyDeviceToDevice, s));
+    return SG_OK;
 }
 }  // namespace
 
@@ -812,58 +1120,8 @@ extern "C" sg_status sg_relabel(const int32_t* d_ids, int64_t n_ids, const int32
         return fail(SG_ERR_INVALID_ARG, "sg_relabel: NULL array");
     if (!d_workspace || workspace_bytes < p.total) return fail(SG_ERR_INVALID_ARG, "sg_relabel: workspace needs %zu bytes", p.total);
     if (((uintptr_t)d_workspace) % 256) return fail(SG_ERR_INVALID_ARG, "sg_relabel: workspace must be 256-byte aligned");
-    cudaStream_t s = (cudaStream_t)stream;
-    char* ws = (char*)d_workspace;
-    CountsLayout L{1};
-    HopArgs a;
-    a.indptr = nullptr;
-    a.indices = nullptr;
-    a.n_nodes = 2147483647LL;
-    a.K = 1;
-    a.logT = p.logT;
-    a.capU = p.capU;
-    a.key0 = a.key1 = 0;
-    a.d_seed = nullptr;
-    a.lambda_num = 0;
-    a.pos_base = (int32_t)p.capU;
-    a.L = L;
-    a.counts = (int32_t*)(ws + p.o_counts);
-    a.ustr = d_unique;
-    a.table = (uint2*)(ws + p.o_table);
-    a.dst_gid = nullptr;
-    a.dbin = nullptr;
-    a.order = nullptr;
-    a.enbr = (int32_t*)(ws + p.o_enbr);
-    a.eslot = (int32_t*)(ws + p.o_eslot);
-    a.eflag = (uint8_t*)(ws + p.o_eflag);
-    a.bsum = (int32_t*)(ws + p.o_bsum);
-    a.epre = (int32_t*)(ws + p.o_epre);
-    a.h = 1;
-    a.fanout = 1;
-    a.bindptr = nullptr;
-    a.bidx = d_local;
-    SG_CUDA(cudaMemsetAsync(a.table, 0xFF, ((size_t)1 << p.logT) * sizeof(uint2), s));
-    SubPtr bp;
-    bp.v[0] = 0;
-    bp.v[1] = (int32_t)n_prefix;
-    const int sms = num_sms();
-    k_seed_init<<<n_prefix > 0 ? (int)cdiv(n_prefix, 256) : 1, 256, 0, s>>>(d_prefix, (int32_t)n_prefix, bp, 1, a.n_nodes,
-                                                                          a.table, p.logT, a.ustr, p.capU, a.counts, L);
-    SG_CHECK_LAUNCH("k_seed_init");
-    int64_t ib = cdiv(n_ids, 256);
-    if (ib > (int64_t)sms * 8) ib = (int64_t)sms * 8;
-    if (ib < 1) ib = 1;
-    k_relabel_insert<<<(unsigned)ib, 256, 0, s>>>(d_ids, n_ids, a.table, p.logT, a.pos_base, a.enbr, a.eslot, a.epre);
-    SG_CHECK_LAUNCH("k_relabel_insert");
-    a.G_e = seg_blocks(n_ids, 4096);
-    k_flag<<<a.G_e, kNT, 0, s>>>(a);
-    SG_CHECK_LAUNCH("k_flag");
-    k_assign<<<a.G_e, kNT, 0, s>>>(a);
-    SG_CHECK_LAUNCH("k_assign");
-    k_map<<<(unsigned)ib, kNT, 0, s>>>(a);
-    SG_CHECK_LAUNCH("k_map");
-    SG_CUDA(cudaMemcpyAsync(d_n_unique, a.counts + L.tot_n(1), sizeof(int32_t), cudaMemcpyDeviceToDevice, s));
-    return SG_OK;
+    return relabel_launch(p, (char*)d_workspace, d_ids, n_ids, d_prefix, n_prefix, d_unique, d_local, d_n_unique,
+                          (cudaStream_t)stream);
 }
 
 // ------------------------------------------- relabel without allocation
@@ -872,8 +1130,6 @@ extern "C" sg_status sg_relabel(const int32_t* d_ids, int64_t n_ids, const int32
 // the array's name as an address; the device address is looked up once per
 // device with cudaGetSymbolAddress.
 static __device__ __align__(256) unsigned char g_relabel_scratch[SG_RELABEL_NOALLOC_SCRATCH_BYTES];
-
-#include <mutex>
 
 namespace {
 std::mutex g_scratch_mu;
@@ -911,57 +1167,6 @@ extern "C" sg_status sg_relabel_noalloc(const int32_t* d_ids, int64_t n_ids, con
     void* scratch = nullptr;
     sg_status st = relabel_scratch_address(&scratch);
     if (st != SG_OK) return st;
-    cudaStream_t s = (cudaStream_t)stream;
-    char* ws = (char*)scratch;
-    CountsLayout L{1};
-    HopArgs a;
-    a.indptr = nullptr;
-    a.indices = nullptr;
-    a.n_nodes = 2147483647LL;
-    a.K = 1;
-    a.logT = p.logT;
-    a.capU = p.capU;
-    a.key0 = a.key1 = 0;
-    a.d_seed = nullptr;
-    a.lambda_num = 0;
-    a.pos_base = (int32_t)p.capU;
-    a.L = L;
-    a.counts = (int32_t*)(ws + p.o_counts);
-    a.ustr = d_unique;
-    a.table = (uint2*)(ws + p.o_table);
-    a.dst_gid = nullptr;
-    a.dbin = nullptr;
-    a.order = nullptr;
-    a.enbr = (int32_t*)(ws + p.o_enbr);
-    a.eslot = (int32_t*)(ws + p.o_eslot);
-    a.eflag = (uint8_t*)(ws + p.o_eflag);
-    a.bsum = (int32_t*)(ws + p.o_bsum);
-    a.epre = (int32_t*)(ws + p.o_epre);
-    a.h = 1;
-    a.fanout = 1;
-    a.bindptr = nullptr;
-    a.bidx = d_local;
-    // the array keeps the previous call's contents: the table must start empty
-    SG_CUDA(cudaMemsetAsync(a.table, 0xFF, ((size_t)1 << p.logT) * sizeof(uint2), s));
-    SubPtr bp;
-    bp.v[0] = 0;
-    bp.v[1] = (int32_t)n_prefix;
-    const int sms = num_sms();
-    k_seed_init<<<n_prefix > 0 ? (int)cdiv(n_prefix, 256) : 1, 256, 0, s>>>(d_prefix, (int32_t)n_prefix, bp, 1, a.n_nodes,
-                                                                          a.table, p.logT, a.ustr, p.capU, a.counts, L);
-    SG_CHECK_LAUNCH("k_seed_init");
-    int64_t ib = cdiv(n_ids, 256);
-    if (ib > (int64_t)sms * 8) ib = (int64_t)sms * 8;
-    if (ib < 1) ib = 1;
-    k_relabel_insert<<<(unsigned)ib, 256, 0, s>>>(d_ids, n_ids, a.table, p.logT, a.pos_base, a.enbr, a.eslot, a.epre);
-    SG_CHECK_LAUNCH("k_relabel_insert");
-    a.G_e = seg_blocks(n_ids, 4096);
-    k_flag<<<a.G_e, kNT, 0, s>>>(a);
-    SG_CHECK_LAUNCH("k_flag");
-    k_assign<<<a.G_e, kNT, 0, s>>>(a);
-    SG_CHECK_LAUNCH("k_assign");
-    k_map<<<(unsigned)ib, kNT, 0, s>>>(a);
-    SG_CHECK_LAUNCH("k_map");
-    SG_CUDA(cudaMemcpyAsync(d_n_unique, a.counts + L.tot_n(1), sizeof(int32_t), cudaMemcpyDeviceToDevice, s));
-    return SG_OK;
+    return relabel_launch(p, (char*)scratch, d_ids, n_ids, d_prefix, n_prefix, d_unique, d_local, d_n_unique,
+                          (cudaStream_t)stream);
 }
