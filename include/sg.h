@@ -283,6 +283,38 @@ sg_status sg_aggregate_bwd(const int32_t* d_indptr, const int32_t* d_idx, int32_
                            int32_t dim, void* d_gsrc, int32_t dtype_out, void* d_workspace, size_t workspace_bytes,
                            sg_stream_t stream);
 
+/* Transposed blocks of one sampler_run output, for the backward pass:
+ * caller-allocated DEVICE arrays, hop h at index h-1:
+ *   tptr[h-1]  [max_nodes[h] + 2] row pointer over the src rows of hop h
+ *   tdst[h-1]  [max_edges[h-1]]   dst row of each edge, edges of a src row in
+ *                                 ascending (dst, position) order
+ *   tw[h-1]    [max_edges[h-1]]   1 / c_dst (fp32) */
+typedef struct sg_transposed {
+    int32_t* tptr[SG_MAX_HOPS];
+    int32_t* tdst[SG_MAX_HOPS];
+    float* tw[SG_MAX_HOPS];
+} sg_transposed;
+
+/* Workspace of sg_transpose_blocks (max_nodes / max_edges as returned by
+ * sg_sampler_bounds); 0 on bad arguments. */
+size_t sg_transpose_workspace(const int64_t* max_nodes, const int64_t* max_edges, int32_t n_hops);
+
+/* Transposes every block of `blocks` (the output of sg_sampler_run with these
+ * bounds) in one set of launches; the counts are read on the device.  The
+ * transposed blocks feed sg_aggregate_bwd_t and do not depend on features, so
+ * the call can run on a second stream while gather and forward proceed.
+ * Edges of one src row are ordered by edge index: the result is deterministic. */
+sg_status sg_transpose_blocks(const sg_blocks* blocks, const int64_t* max_nodes, const int64_t* max_edges,
+                              int32_t n_hops, const sg_transposed* out, void* d_workspace, size_t workspace_bytes,
+                              sg_stream_t stream);
+
+/* Backward of the mean aggregation over a transposed block (see
+ * sg_aggregate_bwd): gsrc[u,:] = sum_p tw[p] * gdst[tdst[p],:] for u < n_src.
+ *   d_dims  device int32[2] = {n_dst, n_src} of the FORWARD block, or NULL */
+sg_status sg_aggregate_bwd_t(const int32_t* d_tptr, const int32_t* d_tdst, const float* d_tw, int32_t n_src_cap,
+                             int32_t n_dst_cap, const int32_t* d_dims, const void* d_gdst, int32_t dtype_in,
+                             int32_t dim, void* d_gsrc, int32_t dtype_out, sg_stream_t stream);
+
 /* ------------------------------------------------------------ measurement */
 /* Streams `bytes` of device-accessible memory at d_src with 16-byte loads
  * (a read roofline probe: HBM when d_src is device memory, the host link when

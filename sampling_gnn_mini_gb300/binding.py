@@ -40,7 +40,8 @@ _STATUS_NAMES = {0: "SG_OK", 1: "SG_ERR_INVALID_ARG", 2: "SG_ERR_INVALID_INDEX",
 EXPORTS = ["sg_version", "sg_last_error", "sg_stream_check", "sg_graph_load", "sg_graph_destroy", "sg_graph_info",
            "sg_sampler_bounds", "sg_sampler_run", "sg_relabel_workspace", "sg_relabel", "sg_cache_build",
            "sg_cache_destroy", "sg_cache_info", "sg_gather", "sg_aggregate_fwd", "sg_aggregate_bwd_workspace",
-           "sg_aggregate_bwd", "sg_read_probe", "sg_hash_probe", "sg_relabel_noalloc"]
+           "sg_aggregate_bwd", "sg_read_probe", "sg_hash_probe", "sg_relabel_noalloc", "sg_transpose_workspace",
+           "sg_transpose_blocks", "sg_aggregate_bwd_t"]
 
 
 class SgError(RuntimeError):
@@ -54,6 +55,12 @@ class _Bounds(ctypes.Structure):
                 ("max_edges", ctypes.c_int64 * SG_MAX_HOPS),
                 ("counts_len", ctypes.c_int64),
                 ("workspace_bytes", ctypes.c_size_t)]
+
+
+class _Transposed(ctypes.Structure):
+    _fields_ = [("tptr", ctypes.c_void_p * SG_MAX_HOPS),
+                ("tdst", ctypes.c_void_p * SG_MAX_HOPS),
+                ("tw", ctypes.c_void_p * SG_MAX_HOPS)]
 
 
 class _Blocks(ctypes.Structure):
@@ -105,6 +112,10 @@ def load(build_if_missing: bool = True):
             "sg_read_probe": (i32, [vp, i64, vp, vp]),
             "sg_hash_probe": (i32, [i64, u64, vp, vp]),
             "sg_relabel_noalloc": (i32, [vp, i64, vp, i64, vp, vp, vp, vp]),
+            "sg_transpose_workspace": (sz, [vp, vp, i32]),
+            "sg_transpose_blocks": (i32, [ctypes.POINTER(_Blocks), vp, vp, i32, ctypes.POINTER(_Transposed), vp, sz,
+                                          vp]),
+            "sg_aggregate_bwd_t": (i32, [vp, vp, vp, i32, i32, vp, vp, i32, i32, vp, i32, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -373,3 +384,41 @@ def sg_relabel_noalloc(ids: torch.Tensor, prefix: torch.Tensor, unique: torch.Te
     n_ids, n_pre = int(ids.numel()), int(prefix.numel())
     _check(load().sg_relabel_noalloc(ids.data_ptr() if n_ids else None, n_ids, prefix.data_ptr() if n_pre else None,
                                      n_pre, unique.data_ptr(), local.data_ptr(), n_unique.data_ptr(), _stream(stream)))
+
+
+class TransposedBuffers:
+    """Caller-owned device arrays of the transposed blocks of one
+    sampler_run output (sg_transposed), plus the transpose workspace."""
+
+    def __init__(self, bounds: Bounds, device="cuda"):
+        H = len(bounds.max_edges)
+        self.n_hops = H
+        self.bounds = bounds
+        self.tptr = [torch.empty(bounds.max_nodes[h] + 2, dtype=torch.int32, device=device) for h in range(1, H + 1)]
+        self.tdst = [torch.empty(max(1, bounds.max_edges[h]), dtype=torch.int32, device=device) for h in range(H)]
+        self.tw = [torch.empty(max(1, bounds.max_edges[h]), dtype=torch.float32, device=device) for h in range(H)]
+        self._mn = np.ascontiguousarray(bounds.max_nodes, dtype=np.int64)
+        self._me = np.ascontiguousarray(bounds.max_edges, dtype=np.int64)
+        wsb = load().sg_transpose_workspace(self._mn.ctypes.data, self._me.ctypes.data, H)
+        if wsb == 0:
+            raise SgError(SG_ERR_INVALID_ARG, "sg_transpose_workspace: bad bounds")
+        self.workspace = _aligned_bytes(wsb, device)
+        self._t = _Transposed()
+        for h in range(H):
+            self._t.tptr[h] = self.tptr[h].data_ptr()
+            self._t.tdst[h] = self.tdst[h].data_ptr()
+            self._t.tw[h] = self.tw[h].data_ptr()
+
+
+def sg_transpose_blocks(buffers: SampleBuffers, tbuf: TransposedBuffers, stream=None) -> None:
+    _check(load().sg_transpose_blocks(ctypes.byref(buffers._blocks), tbuf._mn.ctypes.data, tbuf._me.ctypes.data,
+                                      tbuf.n_hops, ctypes.byref(tbuf._t), tbuf.workspace.data_ptr(),
+                                      tbuf.workspace.numel(), _stream(stream)))
+
+
+def sg_aggregate_bwd_t(tptr: torch.Tensor, tdst: torch.Tensor, tw: torch.Tensor, n_src_cap: int, n_dst_cap: int,
+                       dims: Optional[torch.Tensor], gdst: torch.Tensor, gsrc: torch.Tensor, stream=None) -> None:
+    dim = gdst.shape[1]
+    _check(load().sg_aggregate_bwd_t(tptr.data_ptr(), tdst.data_ptr(), tw.data_ptr(), int(n_src_cap), int(n_dst_cap),
+                                     _ptr(dims), gdst.data_ptr(), _dtype_code(gdst), int(dim), gsrc.data_ptr(),
+                                     _dtype_code(gsrc), _stream(stream)))

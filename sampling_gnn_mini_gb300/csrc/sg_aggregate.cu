@@ -14,6 +14,7 @@
 // transpose is built by a sort of the edges by (src, edge index), so the
 // summation order, and the result, are fixed.
 #include <cuda_bf16.h>
+#include <string.h>
 
 #include "sg_internal.cuh"
 
@@ -24,7 +25,6 @@ using namespace sgi;
 namespace {
 
 constexpr int kNT = 256;
-constexpr int kMaxSeg = 1024;
 constexpr int kWarpSortCap = 256;   // longest segment a warp sorts in shared memory
 constexpr int kBlockSortCap = 4096; // longest segment a block sorts in shared memory
 
@@ -209,16 +209,45 @@ __global__ void __launch_bounds__(kNT) k_spmm_scalar(const int32_t* __restrict__
 }
 
 // --------------------------------------------------------------- transpose
-// Edge count of the block from its row pointer.
-__device__ __forceinline__ int32_t block_edges(const int32_t* indptr, int32_t n_dst_cap, const int32_t* dims) {
-    const int32_t n_dst = dims ? min(dims[0], n_dst_cap) : n_dst_cap;
-    return indptr[n_dst];
+// The backward pass needs each block's edges grouped by src row, in edge
+// order inside a group.  All blocks of a set (the hops of one mini-batch) are
+// transposed by the same five launches; blockIdx.y selects the block.
+//   k_tcount   edges per src row (integer atomics: the counts are exact)
+//   k_tscan    row pointer of the transposed block (single-pass look-back)
+//   k_tscatter every edge into its src segment (order fixed by the sort)
+//   k_tsort    short segments sorted by edge index by one warp; long ones listed
+//   k_tsort_long  long segments sorted by a block (bitonic network)
+// The outputs per edge are the dst row and the weight 1 / c_dst.
+struct TSet {
+    int nb;
+    const int32_t* indptr[SG_MAX_HOPS];
+    const int32_t* idx[SG_MAX_HOPS];
+    int32_t n_dst_cap[SG_MAX_HOPS], n_src_cap[SG_MAX_HOPS];
+    const int32_t* dims[SG_MAX_HOPS];          // device {n_dst, n_src} or NULL
+    int32_t* tcnt[SG_MAX_HOPS];                // [n_src_cap + 1], zeroed
+    int32_t* tptr[SG_MAX_HOPS];                // [n_src_cap + 1] output
+    int32_t* tkey[SG_MAX_HOPS];                // [edges] scratch
+    int32_t* dst_of[SG_MAX_HOPS];              // [edges] scratch
+    int32_t* tdst[SG_MAX_HOPS];                // [edges] output
+    float* tw[SG_MAX_HOPS];                    // [edges] output
+    unsigned long long* status[SG_MAX_HOPS];   // scan chain, zeroed
+    int32_t* long_list[SG_MAX_HOPS];           // [n_src_cap]
+    uint32_t* ctr;                             // [2 * SG_MAX_HOPS]: tile counter, long count; zeroed
+};
+
+__device__ __forceinline__ int32_t set_n_dst(const TSet& t, int b) {
+    return t.dims[b] ? min(t.dims[b][0], t.n_dst_cap[b]) : t.n_dst_cap[b];
+}
+__device__ __forceinline__ int32_t set_n_src(const TSet& t, int b) {
+    return t.dims[b] ? min(t.dims[b][1], t.n_src_cap[b]) : t.n_src_cap[b];
 }
 
-__global__ void k_tcount(const int32_t* __restrict__ indptr, const int32_t* __restrict__ idx, int32_t n_dst_cap,
-                         int32_t n_src_cap, const int32_t* dims, int32_t* tcnt) {
-    const int32_t E = block_edges(indptr, n_dst_cap, dims);
-    const int32_t n_src = dims ? min(dims[1], n_src_cap) : n_src_cap;
+__global__ void k_tcount(TSet t) {
+    const int b = blockIdx.y;
+    const int32_t E = t.indptr[b][set_n_dst(t, b)];
+    const int32_t n_src = set_n_src(t, b);
+    const int32_t* idx = t.idx[b];
+    int32_t* tcnt = t.tcnt[b];
     for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < E; e += (int64_t)gridDim.x * blockDim.x) {
         const int32_t u = idx[e];
         if (u >= 0 && u < n_src) atomicAdd(tcnt + u, 1);
@@ -226,60 +255,65 @@ __global__ void k_tcount(const int32_t* __restrict__ indptr, const int32_t* __re
     }
 }
 
-// Segmented exclusive scan of in[0, n) into out[0, n), n = (dims ? dims[1] :
-// cap) + 1: pass 1 writes one sum per block, pass 2 adds the sums of earlier
-// blocks and scans the block's segment in tiles.
-__global__ void __launch_bounds__(kNT) k_scan_sums(const int32_t* in, int32_t cap, const int32_t* dims, int32_t* bsum) {
-    __shared__ int32_t red[kNT / 32 + 1];
-    const int64_t n = (int64_t)(dims ? min(dims[1], cap) : cap) + 1;
-    int64_t lo, hi;
-    segment_of(n, blockIdx.x, gridDim.x, lo, hi);
-    int32_t s = 0;
-    for (int64_t i = lo + threadIdx.x; i < hi; i += kNT) s += in[i];
-    s = block_sum<kNT>(s, red);
-    if (threadIdx.x == 0) bsum[blockIdx.x] = s;
-}
+constexpr int kTTile = 1024;  // entries per scan tile (4 per thread)
 
-__global__ void __launch_bounds__(kNT) k_scan_write(const int32_t* in, int32_t cap, const int32_t* dims,
-                                                    const int32_t* bsum, int32_t* out) {
+// Exclusive scan of tcnt[0, n_src] into tptr[0, n_src] (tptr[n_src] = E).
+__global__ void __launch_bounds__(kNT) k_tscan(TSet t) {
     __shared__ int32_t red[kNT / 32 + 1];
-    __shared__ int32_t carry;
-    const int64_t n = (int64_t)(dims ? min(dims[1], cap) : cap) + 1;
-    int32_t pre = 0;
-    for (int b = threadIdx.x; b < (int)blockIdx.x; b += kNT) pre += bsum[b];
-    pre = block_sum<kNT>(pre, red);
-    if (threadIdx.x == 0) carry = pre;
-    __syncthreads();
-    int64_t lo, hi;
-    segment_of(n, blockIdx.x, gridDim.x, lo, hi);
-    for (int64_t t0 = lo; t0 < hi; t0 += kNT) {
-        const int64_t i = t0 + threadIdx.x;
-        const int32_t v = i < hi ? in[i] : 0;
-        int32_t tot;
-        const int32_t ex = block_excl_scan<kNT>(v, red, tot);
-        if (i < hi) out[i] = carry + ex;
+    __shared__ int32_t s_tile, s_excl;
+    const int b = blockIdx.y;
+    const int64_t n = (int64_t)set_n_src(t, b) + 1;
+    const int64_t n_tiles = (n + kTTile - 1) / kTTile;
+    if ((int64_t)blockIdx.x >= n_tiles) return;
+    for (int iter = 0;; ++iter) {
+        if (iter > 0 && (int64_t)gridDim.x >= n_tiles) break;
+        if (threadIdx.x == 0) s_tile = (int32_t)atomicAdd(t.ctr + 2 * b, 1u);
         __syncthreads();
-        if (threadIdx.x == 0) carry += tot;
+        const int64_t tile = s_tile;
+        if (tile >= n_tiles) break;
+        const int64_t i0 = tile * kTTile + (int64_t)threadIdx.x * 4;
+        int32_t v[4], mine = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            v[q] = i0 + q < n ? t.tcnt[b][i0 + q] : 0;
+            mine += v[q];
+        }
+        int32_t total;
+        const int32_t ex = block_excl_scan<kNT>(mine, red, total);
+        if (threadIdx.x < 32) {
+            bool late = false;
+            const int32_t x = chain_lookback(t.status[b], (int)tile, 0, total, &late);
+            if (threadIdx.x == 0) {
+                s_excl = x;
+                if (late) dev_err(ERR_TIMEOUT);
+            }
+        }
+        __syncthreads();
+        int32_t run = s_excl + ex;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (i0 + q < n) t.tptr[b][i0 + q] = run;
+            run += v[q];
+        }
         __syncthreads();
     }
 }
 
-// Places every edge in its src segment (order inside a segment is fixed by
-// the sort that follows) and records the edge's dst row.
-__global__ void k_tscatter(const int32_t* __restrict__ indptr, const int32_t* __restrict__ idx, int32_t n_dst_cap,
-                           int32_t n_src_cap, const int32_t* dims, const int32_t* __restrict__ tptr, int32_t* tcnt,
-                           int32_t* tkey, int32_t* dst_of) {
-    const int32_t n_dst = dims ? min(dims[0], n_dst_cap) : n_dst_cap;
-    const int32_t n_src = dims ? min(dims[1], n_src_cap) : n_src_cap;
+// Places every edge in its src segment and records the edge's dst row.
+__global__ void k_tscatter(TSet t) {
+    const int b = blockIdx.y;
+    const int32_t n_dst = set_n_dst(t, b), n_src = set_n_src(t, b);
+    const int32_t* indptr = t.indptr[b];
+    const int32_t* idx = t.idx[b];
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
     for (int64_t v = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32; v < n_dst; v += warps) {
         const int32_t lo = indptr[v], hi = indptr[v + 1];
         for (int32_t e = lo + (int32_t)lane_id(); e < hi; e += 32) {
             const int32_t u = idx[e];
-            dst_of[e] = (int32_t)v;
+            t.dst_of[b][e] = (int32_t)v;
             if (u < 0 || u >= n_src) continue;
-            const int32_t p = tptr[u] + atomicSub(tcnt + u, 1) - 1;
-            tkey[p] = e;
+            const int32_t p = t.tptr[b][u] + atomicSub(t.tcnt[b] + u, 1) - 1;
+            t.tkey[b][p] = e;
         }
     }
 }
@@ -292,13 +326,15 @@ __device__ __forceinline__ void emit_transposed(const int32_t* indptr, const int
 }
 
 // Sorts each src segment by edge index.  Segments up to kWarpSortCap are
-// ranked by one warp; longer ones go to a list for k_tsort_long.
-__global__ void __launch_bounds__(kNT) k_tsort(const int32_t* __restrict__ indptr, int32_t n_src_cap, const int32_t* dims,
-                                               const int32_t* __restrict__ tptr, const int32_t* __restrict__ tkey,
-                                               const int32_t* __restrict__ dst_of, int32_t* tdst, float* tw,
-                                               int32_t* long_list, int32_t* long_count) {
+// ranked by one warp; longer ones go to the block's list for k_tsort_long.
+__global__ void __launch_bounds__(kNT) k_tsort(TSet t) {
     __shared__ int32_t sk[kNT / 32][kWarpSortCap];
-    const int32_t n_src = dims ? min(dims[1], n_src_cap) : n_src_cap;
+    const int b = blockIdx.y;
+    const int32_t n_src = set_n_src(t, b);
+    const int32_t* tptr = t.tptr[b];
+    const int32_t* tkey = t.tkey[b];
+    const int32_t* dst_of = t.dst_of[b];
+    const int32_t* indptr = t.indptr[b];
     const int wib = threadIdx.x >> 5;
     const unsigned lane = lane_id();
     const int64_t warps = (int64_t)gridDim.x * (kNT / 32);
@@ -308,21 +344,21 @@ __global__ void __launch_bounds__(kNT) k_tsort(const int32_t* __restrict__ indpt
         if (len <= 32) {
             const int32_t key = (int)lane < len ? tkey[lo + lane] : 0x7FFFFFFF;
             int rank = 0;
-            for (int t = 0; t < len; ++t) rank += __shfl_sync(0xffffffffu, key, t) < key;
-            if ((int)lane < len) emit_transposed(indptr, dst_of, key, lo + rank, tdst, tw);
+            for (int q = 0; q < len; ++q) rank += __shfl_sync(0xffffffffu, key, q) < key;
+            if ((int)lane < len) emit_transposed(indptr, dst_of, key, lo + rank, t.tdst[b], t.tw[b]);
         } else if (len <= kWarpSortCap) {
-            int32_t* s = sk[wib];
-            for (int t = lane; t < len; t += 32) s[t] = tkey[lo + t];
+            int32_t* sw = sk[wib];
+            for (int q = lane; q < len; q += 32) sw[q] = tkey[lo + q];
             __syncwarp();
             for (int i = lane; i < len; i += 32) {
-                const int32_t key = s[i];
+                const int32_t key = sw[i];
                 int rank = 0;
-                for (int t = 0; t < len; ++t) rank += s[t] < key;
-                emit_transposed(indptr, dst_of, key, lo + rank, tdst, tw);
+                for (int q = 0; q < len; ++q) rank += sw[q] < key;
+                emit_transposed(indptr, dst_of, key, lo + rank, t.tdst[b], t.tw[b]);
             }
             __syncwarp();
         } else if (lane == 0) {
-            long_list[atomicAdd(long_count, 1)] = (int32_t)u;
+            t.long_list[b][atomicAdd(t.ctr + 2 * b + 1, 1u)] = (int32_t)u;
         }
     }
 }
@@ -337,21 +373,21 @@ __device__ void block_bitonic_sort(int32_t* keys, int32_t len) {
     for (int32_t k = 2; k <= P; k <<= 1) {
         for (int32_t i = threadIdx.x; i < P / 2; i += blockDim.x) {
             const int32_t half = k >> 1;
-            const int32_t a = (i / half) * k + (i % half);
-            const int32_t b = (i / half) * k + (k - 1 - (i % half));
-            if (b < len) {
-                const int32_t x = keys[a], y = keys[b];
-                if (y < x) { keys[a] = y; keys[b] = x; }
+            const int32_t lo = (i / half) * k + (i % half);
+            const int32_t hi = (i / half) * k + (k - 1 - (i % half));
+            if (hi < len) {
+                const int32_t x = keys[lo], y = keys[hi];
+                if (y < x) { keys[lo] = y; keys[hi] = x; }
             }
         }
         __syncthreads();
         for (int32_t j = k >> 2; j > 0; j >>= 1) {
             for (int32_t i = threadIdx.x; i < P / 2; i += blockDim.x) {
-                const int32_t a = (i / j) * (2 * j) + (i % j);
-                const int32_t b = a + j;
-                if (b < len) {
-                    const int32_t x = keys[a], y = keys[b];
-                    if (y < x) { keys[a] = y; keys[b] = x; }
+                const int32_t lo = (i / j) * (2 * j) + (i % j);
+                const int32_t hi = lo + j;
+                if (hi < len) {
+                    const int32_t x = keys[lo], y = keys[hi];
+                    if (y < x) { keys[lo] = y; keys[hi] = x; }
                 }
             }
             __syncthreads();
@@ -359,24 +395,24 @@ __device__ void block_bitonic_sort(int32_t* keys, int32_t len) {
     }
 }
 
-__global__ void __launch_bounds__(kNT) k_tsort_long(const int32_t* __restrict__ indptr, const int32_t* __restrict__ tptr,
-                                                    int32_t* tkey, const int32_t* __restrict__ dst_of, int32_t* tdst,
-                                                    float* tw, const int32_t* long_list, const int32_t* long_count) {
+__global__ void __launch_bounds__(kNT) k_tsort_long(TSet t) {
     __shared__ int32_t sk[kBlockSortCap];
-    const int32_t n = *long_count;
+    const int b = blockIdx.y;
+    const int32_t n = (int32_t)t.ctr[2 * b + 1];
     for (int32_t i = blockIdx.x; i < n; i += gridDim.x) {
-        const int32_t u = long_list[i];
-        const int32_t lo = tptr[u], len = tptr[u + 1] - lo;
+        const int32_t u = t.long_list[b][i];
+        const int32_t lo = t.tptr[b][u], len = t.tptr[b][u + 1] - lo;
         int32_t* keys;
         if (len <= kBlockSortCap) {
-            for (int32_t t = threadIdx.x; t < len; t += blockDim.x) sk[t] = tkey[lo + t];
+            for (int32_t q = threadIdx.x; q < len; q += blockDim.x) sk[q] = t.tkey[b][lo + q];
             keys = sk;
         } else {
-            keys = tkey + lo;  // long segment: sort in place in global memory
+            keys = t.tkey[b] + lo;  // long segment: sort in place in global memory
         }
         __syncthreads();
         block_bitonic_sort(keys, len);
-        for (int32_t t = threadIdx.x; t < len; t += blockDim.x) emit_transposed(indptr, dst_of, keys[t], lo + t, tdst, tw);
+        for (int32_t q = threadIdx.x; q < len; q += blockDim.x)
+            emit_transposed(t.indptr[b], t.dst_of[b], keys[q], lo + q, t.tdst[b], t.tw[b]);
         __syncthreads();
     }
 }
@@ -393,11 +429,11 @@ template <int DT, bool WGT>
 sg_status launch_vec(int lpr, int vpl, int blocks, cudaStream_t s, const int32_t* ptr, const int32_t* col, const float* w,
                      int32_t nr, const int32_t* dr, int32_t nc, const int32_t* dc, const void* x, int32_t rv, void* y) {
 #define SG_SPMM(L, V) k_spmm<L, V, DT, WGT><<<blocks, kNT, 0, s>>>(ptr, col, w, nr, dr, nc, dc, (const uint4*)x, rv, y)
-    if (lpr == 4) SG_SPMM(4, 1);
-    else if (lpr == 8) SG_SPMM(8, 1);
-    else if (lpr == 16) SG_SPMM(16, 1);
-    else if (vpl == 1) SG_SPMM(32, 1);
-    else if (vpl == 2) SG_SPMM(32, 2);
+    if (lpr == 4 && vpl == 1) SG_SPMM(4, 1);
+    else if (lpr == 4 && vpl == 2) SG_SPMM(4, 2);
+    else if (lpr == 4) SG_SPMM(4, 4);
+    else if (lpr == 8) SG_SPMM(8, 4);
+    else if (lpr == 16) SG_SPMM(16, 4);
     else if (vpl == 4) SG_SPMM(32, 4);
     else SG_SPMM(32, 8);
 #undef SG_SPMM
@@ -424,11 +460,23 @@ sg_status run_spmm(const int32_t* ptr, const int32_t* col, const float* w, int32
         SG_CHECK_LAUNCH("k_spmm_scalar");
         return SG_OK;
     }
-    int lpr = 32, vpl = 1;
-    if (row_vecs <= 4) lpr = 4;
-    else if (row_vecs <= 8) lpr = 8;
-    else if (row_vecs <= 16) lpr = 16;
-    else vpl = row_vecs <= 32 ? 1 : (row_vecs <= 64 ? 2 : (row_vecs <= 128 ? 4 : 8));
+    // a row goes to a group of LPR lanes holding VPL vectors each: small
+    // groups put several rows of one warp in flight (rows of sampled blocks
+    // are short, so latency, not bandwidth, limits a lone row)
+    int lpr, vpl;
+    if (row_vecs <= 16) {
+        lpr = 4;
+        vpl = row_vecs <= 4 ? 1 : (row_vecs <= 8 ? 2 : 4);
+    } else if (row_vecs <= 32) {
+        lpr = 8;
+        vpl = 4;
+    } else if (row_vecs <= 64) {
+        lpr = 16;
+        vpl = 4;
+    } else {
+        lpr = 32;
+        vpl = row_vecs <= 128 ? 4 : 8;
+    }
     int64_t blocks = cdiv((int64_t)n_rows_cap * lpr, kNT);
     if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
     if (blocks < 1) blocks = 1;
@@ -441,27 +489,87 @@ sg_status run_spmm(const int32_t* ptr, const int32_t* col, const float* w, int32
                : launch_vec<DT_BF16_F32, false>(lpr, vpl, (int)blocks, s, ptr, col, w, n_rows_cap, d_rows, n_cols_cap, d_cols, x, (int32_t)row_vecs, y);
 }
 
-struct BwdLayout {
-    size_t o_tcnt, o_tptr, o_tkey, o_dst, o_tdst, o_tw, o_bsum, o_long, total;
-};
-
 size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-BwdLayout bwd_layout(int32_t n_dst_cap, int32_t n_src_cap, int64_t n_edge_cap) {
-    (void)n_dst_cap;
-    BwdLayout L;
-    const size_t ns = (size_t)(n_src_cap > 0 ? n_src_cap : 0) + 2, ne = (size_t)(n_edge_cap > 0 ? n_edge_cap : 1);
+// Workspace of a transpose set: zeroed region first (counts, scan chains,
+// counters), then scratch.  Outputs (tptr, tdst, tw) may live in the
+// workspace (sg_aggregate_bwd) or in caller arrays (sg_transpose_blocks).
+struct TLayout {
+    size_t o_tcnt[SG_MAX_HOPS], o_status[SG_MAX_HOPS], o_ctr, zero_end;
+    size_t o_tkey[SG_MAX_HOPS], o_dst[SG_MAX_HOPS], o_long[SG_MAX_HOPS];
+    size_t o_tptr[SG_MAX_HOPS], o_tdst[SG_MAX_HOPS], o_tw[SG_MAX_HOPS], total;
+};
+
+TLayout t_layout(int nb, const int64_t* n_src_cap, const int64_t* n_edge_cap, bool outputs_inside) {
+    TLayout L;
     size_t o = 0;
-    L.o_tcnt = o; o = a256(o + (ns + 1) * 4);  // + the long-segment counter
-    L.o_tptr = o; o = a256(o + ns * 4);
-    L.o_tkey = o; o = a256(o + ne * 4);
-    L.o_dst = o;  o = a256(o + ne * 4);
-    L.o_tdst = o; o = a256(o + ne * 4);
-    L.o_tw = o;   o = a256(o + ne * 4);
-    L.o_bsum = o; o = a256(o + (size_t)kMaxSeg * 4);
-    L.o_long = o; o = a256(o + ns * 4);
+    for (int b = 0; b < nb; ++b) {
+        const size_t ns = (size_t)(n_src_cap[b] > 0 ? n_src_cap[b] : 0) + 1;
+        L.o_tcnt[b] = o;
+        o = a256(o + ns * 4);
+        L.o_status[b] = o;
+        o = a256(o + (ns / kTTile + 2) * 8);
+    }
+    L.o_ctr = o;
+    o = a256(o + 2 * SG_MAX_HOPS * 4);
+    L.zero_end = o;
+    for (int b = 0; b < nb; ++b) {
+        const size_t ns = (size_t)(n_src_cap[b] > 0 ? n_src_cap[b] : 0) + 1;
+        const size_t ne = (size_t)(n_edge_cap[b] > 0 ? n_edge_cap[b] : 1);
+        L.o_tkey[b] = o;
+        o = a256(o + ne * 4);
+        L.o_dst[b] = o;
+        o = a256(o + ne * 4);
+        L.o_long[b] = o;
+        o = a256(o + ns * 4);
+        if (outputs_inside) {
+            L.o_tptr[b] = o;
+            o = a256(o + (ns + 1) * 4);
+            L.o_tdst[b] = o;
+            o = a256(o + ne * 4);
+            L.o_tw[b] = o;
+            o = a256(o + ne * 4);
+        }
+    }
     L.total = o;
     return L;
+}
+
+// Launches the five transpose kernels for the set.
+sg_status run_transpose(TSet& t, const int64_t* n_dst_cap, const int64_t* n_src_cap, const int64_t* n_edge_cap,
+                        char* ws, const TLayout& L, cudaStream_t s) {
+    const int sms = num_sms();
+    const int nb = t.nb;
+    t.ctr = (uint32_t*)(ws + L.o_ctr);
+    int64_t max_e = 1, max_src = 1, max_dst = 1;
+    for (int b = 0; b < nb; ++b) {
+        t.tcnt[b] = (int32_t*)(ws + L.o_tcnt[b]);
+        t.status[b] = (unsigned long long*)(ws + L.o_status[b]);
+        t.tkey[b] = (int32_t*)(ws + L.o_tkey[b]);
+        t.dst_of[b] = (int32_t*)(ws + L.o_dst[b]);
+        t.long_list[b] = (int32_t*)(ws + L.o_long[b]);
+        if (n_edge_cap[b] > max_e) max_e = n_edge_cap[b];
+        if (n_src_cap[b] > max_src) max_src = n_src_cap[b];
+        if (n_dst_cap[b] > max_dst) max_dst = n_dst_cap[b];
+    }
+    SG_CUDA(cudaMemsetAsync(ws, 0, L.zero_end, s));
+    auto grid = [&](int64_t work, int64_t per_block) {
+        int64_t g = cdiv(work, per_block);
+        if (g > (int64_t)sms * 8) g = (int64_t)sms * 8;
+        if (g < 1) g = 1;
+        return dim3((unsigned)g, (unsigned)nb, 1);
+    };
+    k_tcount<<<grid(max_e, 256 * 4), 256, 0, s>>>(t);
+    SG_CHECK_LAUNCH("k_tcount");
+    k_tscan<<<grid(max_src + 1, kTTile), kNT, 0, s>>>(t);
+    SG_CHECK_LAUNCH("k_tscan");
+    k_tscatter<<<grid(max_dst, 8), 256, 0, s>>>(t);
+    SG_CHECK_LAUNCH("k_tscatter");
+    k_tsort<<<grid(max_src, kNT / 32), kNT, 0, s>>>(t);
+    SG_CHECK_LAUNCH("k_tsort");
+    k_tsort_long<<<dim3((unsigned)sms, (unsigned)nb, 1), kNT, 0, s>>>(t);
+    SG_CHECK_LAUNCH("k_tsort_long");
+    return SG_OK;
 }
 
 }  // namespace
@@ -477,7 +585,9 @@ extern "C" sg_status sg_aggregate_fwd(const int32_t* d_indptr, const int32_t* d_
 }
 
 extern "C" size_t sg_aggregate_bwd_workspace(int32_t n_dst_cap, int32_t n_src_cap, int64_t n_edge_cap) {
-    return bwd_layout(n_dst_cap, n_src_cap, n_edge_cap).total;
+    (void)n_dst_cap;
+    const int64_t ns = n_src_cap, ne = n_edge_cap;
+    return t_layout(1, &ns, &ne, true).total;
 }
 
 extern "C" sg_status sg_aggregate_bwd(const int32_t* d_indptr, const int32_t* d_idx, int32_t n_dst_cap, int32_t n_src_cap,
@@ -490,48 +600,79 @@ extern "C" sg_status sg_aggregate_bwd(const int32_t* d_indptr, const int32_t* d_
     if (!d_indptr || !d_gsrc || !d_workspace || (n_dst_cap > 0 && (!d_gdst || !d_idx)))
         return fail(SG_ERR_INVALID_ARG, "sg_aggregate_bwd: NULL array");
     if (dt_code(dtype_in, dtype_out) < 0) return fail(SG_ERR_UNSUPPORTED, "sg_aggregate_bwd: dtype pair not supported");
-    const BwdLayout L = bwd_layout(n_dst_cap, n_src_cap, n_edge_cap);
+    const int64_t nd = n_dst_cap, ns = n_src_cap, ne = n_edge_cap;
+    const TLayout L = t_layout(1, &ns, &ne, true);
     if (workspace_bytes < L.total) return fail(SG_ERR_INVALID_ARG, "sg_aggregate_bwd: workspace needs %zu bytes", L.total);
     if (((uintptr_t)d_workspace) % 256) return fail(SG_ERR_INVALID_ARG, "sg_aggregate_bwd: workspace must be 256-byte aligned");
     cudaStream_t s = (cudaStream_t)stream;
     char* ws = (char*)d_workspace;
-    int32_t* tcnt = (int32_t*)(ws + L.o_tcnt);
-    int32_t* long_count = tcnt + (n_src_cap + 2);
-    int32_t* tptr = (int32_t*)(ws + L.o_tptr);
-    int32_t* tkey = (int32_t*)(ws + L.o_tkey);
-    int32_t* dst_of = (int32_t*)(ws + L.o_dst);
-    int32_t* tdst = (int32_t*)(ws + L.o_tdst);
-    float* tw = (float*)(ws + L.o_tw);
-    int32_t* bsum = (int32_t*)(ws + L.o_bsum);
-    int32_t* long_list = (int32_t*)(ws + L.o_long);
-    const int sms = num_sms();
-    SG_CUDA(cudaMemsetAsync(tcnt, 0, ((size_t)n_src_cap + 3) * 4, s));
-    if (n_dst_cap > 0) {
-        int64_t eb = cdiv(n_edge_cap > 0 ? n_edge_cap : 1, 256);
-        if (eb > (int64_t)sms * 8) eb = (int64_t)sms * 8;
-        k_tcount<<<(unsigned)eb, 256, 0, s>>>(d_indptr, d_idx, n_dst_cap, n_src_cap, d_dims, tcnt);
-        SG_CHECK_LAUNCH("k_tcount");
+    TSet t;
+    memset(&t, 0, sizeof(t));
+    t.nb = 1;
+    t.indptr[0] = d_indptr;
+    t.idx[0] = d_idx;
+    t.n_dst_cap[0] = n_dst_cap;
+    t.n_src_cap[0] = n_src_cap;
+    t.dims[0] = d_dims;
+    t.tptr[0] = (int32_t*)(ws + L.o_tptr[0]);
+    t.tdst[0] = (int32_t*)(ws + L.o_tdst[0]);
+    t.tw[0] = (float*)(ws + L.o_tw[0]);
+    sg_status st = run_transpose(t, &nd, &ns, &ne, ws, L, s);
+    if (st != SG_OK) return st;
+    return run_spmm(t.tptr[0], t.tdst[0], t.tw[0], n_src_cap, d_dims ? d_dims + 1 : nullptr, n_dst_cap, d_dims, d_gdst,
+                    dtype_in, dim, d_gsrc, dtype_out, s);
+}
+
+extern "C" size_t sg_transpose_workspace(const int64_t* max_nodes, const int64_t* max_edges, int32_t n_hops) {
+    if (!max_nodes || !max_edges || n_hops < 1 || n_hops > SG_MAX_HOPS) return 0;
+    int64_t ns[SG_MAX_HOPS], ne[SG_MAX_HOPS];
+    for (int h = 0; h < n_hops; ++h) {
+        ns[h] = max_nodes[h + 1];
+        ne[h] = max_edges[h];
     }
-    int64_t gs = cdiv((int64_t)n_src_cap + 1, 2048);
-    if (gs > kMaxSeg) gs = kMaxSeg;
-    if (gs < 1) gs = 1;
-    k_scan_sums<<<(unsigned)gs, kNT, 0, s>>>(tcnt, n_src_cap, d_dims, bsum);
-    SG_CHECK_LAUNCH("k_scan_sums");
-    k_scan_write<<<(unsigned)gs, kNT, 0, s>>>(tcnt, n_src_cap, d_dims, bsum, tptr);
-    SG_CHECK_LAUNCH("k_scan_write");
-    if (n_dst_cap > 0) {
-        int64_t wb = cdiv(n_dst_cap, 8);
-        if (wb > (int64_t)sms * 8) wb = (int64_t)sms * 8;
-        k_tscatter<<<(unsigned)wb, 256, 0, s>>>(d_indptr, d_idx, n_dst_cap, n_src_cap, d_dims, tptr, tcnt, tkey, dst_of);
-        SG_CHECK_LAUNCH("k_tscatter");
+    return t_layout(n_hops, ns, ne, false).total;
+}
+
+extern "C" sg_status sg_transpose_blocks(const sg_blocks* blocks, const int64_t* max_nodes, const int64_t* max_edges,
+                                         int32_t n_hops, const sg_transposed* out, void* d_workspace,
+                                         size_t workspace_bytes, sg_stream_t stream) {
+    if (!blocks || !blocks->counts || !max_nodes || !max_edges || !out || n_hops < 1 || n_hops > SG_MAX_HOPS)
+        return fail(SG_ERR_INVALID_ARG, "sg_transpose_blocks: bad arguments");
+    int64_t nd[SG_MAX_HOPS], ns[SG_MAX_HOPS], ne[SG_MAX_HOPS];
+    TSet t;
+    memset(&t, 0, sizeof(t));
+    t.nb = n_hops;
+    for (int h = 0; h < n_hops; ++h) {
+        nd[h] = max_nodes[h];
+        ns[h] = max_nodes[h + 1];
+        ne[h] = max_edges[h];
+        if (nd[h] < 0 || ns[h] < 0 || ne[h] < 0 || ns[h] > 2147483646LL || ne[h] > 2147483647LL || nd[h] > 2147483646LL)
+            return fail(SG_ERR_INVALID_ARG, "sg_transpose_blocks: sizes of hop %d out of range", h + 1);
+        if (!blocks->indptr[h] || !blocks->idx[h] || !out->tptr[h] || !out->tdst[h] || !out->tw[h])
+            return fail(SG_ERR_INVALID_ARG, "sg_transpose_blocks: arrays of hop %d missing", h + 1);
+        t.indptr[h] = blocks->indptr[h];
+        t.idx[h] = blocks->idx[h];
+        t.n_dst_cap[h] = (int32_t)nd[h];
+        t.n_src_cap[h] = (int32_t)ns[h];
+        t.dims[h] = blocks->counts + h;  // {sum_k |V_{h-1}^k|, sum_k |V_h^k|}
+        t.tptr[h] = out->tptr[h];
+        t.tdst[h] = out->tdst[h];
+        t.tw[h] = out->tw[h];
     }
-    int64_t sb = cdiv(n_src_cap, kNT / 32);
-    if (sb > (int64_t)sms * 8) sb = (int64_t)sms * 8;
-    if (sb < 1) sb = 1;
-    k_tsort<<<(unsigned)sb, kNT, 0, s>>>(d_indptr, n_src_cap, d_dims, tptr, tkey, dst_of, tdst, tw, long_list, long_count);
-    SG_CHECK_LAUNCH("k_tsort");
-    k_tsort_long<<<(unsigned)sms, kNT, 0, s>>>(d_indptr, tptr, tkey, dst_of, tdst, tw, long_list, long_count);
-    SG_CHECK_LAUNCH("k_tsort_long");
-    return run_spmm(tptr, tdst, tw, n_src_cap, d_dims ? d_dims + 1 : nullptr, n_dst_cap, d_dims, d_gdst, dtype_in, dim,
-                    d_gsrc, dtype_out, s);
+    const TLayout L = t_layout(n_hops, ns, ne, false);
+    if (!d_workspace || workspace_bytes < L.total)
+        return fail(SG_ERR_INVALID_ARG, "sg_transpose_blocks: workspace needs %zu bytes", L.total);
+    if (((uintptr_t)d_workspace) % 256) return fail(SG_ERR_INVALID_ARG, "sg_transpose_blocks: workspace must be 256-byte aligned");
+    return run_transpose(t, nd, ns, ne, (char*)d_workspace, L, (cudaStream_t)stream);
+}
+
+extern "C" sg_status sg_aggregate_bwd_t(const int32_t* d_tptr, const int32_t* d_tdst, const float* d_tw, int32_t n_src_cap,
+                                        int32_t n_dst_cap, const int32_t* d_dims, const void* d_gdst, int32_t dtype_in,
+                                        int32_t dim, void* d_gsrc, int32_t dtype_out, sg_stream_t stream) {
+    if (n_src_cap < 0 || n_dst_cap < 0 || dim <= 0) return fail(SG_ERR_INVALID_ARG, "sg_aggregate_bwd_t: bad sizes");
+    if (n_src_cap == 0) return SG_OK;
+    if (!d_tptr || !d_gsrc || (n_dst_cap > 0 && (!d_tdst || !d_tw || !d_gdst)))
+        return fail(SG_ERR_INVALID_ARG, "sg_aggregate_bwd_t: NULL array");
+    return run_spmm(d_tptr, d_tdst, d_tw, n_src_cap, d_dims ? d_dims + 1 : nullptr, n_dst_cap, d_dims, d_gdst, dtype_in, dim,
+                    d_gsrc, dtype_out, (cudaStream_t)stream);
 }

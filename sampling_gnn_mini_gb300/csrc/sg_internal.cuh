@@ -116,6 +116,64 @@ __device__ __forceinline__ T block_sum(T x, T* sh) {
     return t;
 }
 
+// ------------------------------------------------- single-pass scan chains
+// Tile status words: (state << 32) | value, state 1 aggregate, 2 inclusive
+// prefix, anything else (a zeroed or all-ones word) empty.  A block publishes its tile's aggregate, then walks back
+// over its predecessors until one has an inclusive prefix (decoupled
+// look-back).  Tiles are handed out in increasing order by an atomic counter,
+// so every predecessor belongs to a block that is already running; each wait
+// is still bounded (kLookbackSpins polls), and *timed_out reports a wait that
+// gave up.
+constexpr int kLookbackSpins = 1 << 22;
+
+__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Exclusive prefix of tile t in the chain whose first tile is t0.  Called by
+// all 32 lanes of one warp: the warp reads 32 predecessors at once, adds the
+// aggregates up to the closest inclusive prefix, and moves the window back by
+// 32 only while none is inclusive.
+__device__ __forceinline__ int32_t chain_lookback(unsigned long long* status, int t, int t0, int32_t agg,
+                                                  bool* timed_out) {
+    const int lane = (int)lane_id();
+    if (t == t0) {
+        if (lane == 0) st_release(status + t, (2ull << 32) | (uint32_t)agg);
+        return 0;
+    }
+    if (lane == 0) st_release(status + t, (1ull << 32) | (uint32_t)agg);
+    int32_t excl = 0;
+    for (int top = t - 1;; top -= 32) {
+        const int p = top - lane;
+        unsigned long long s = 2ull << 32;  // before the chain: an inclusive zero
+        if (p >= t0) {
+            int spins = 0;
+            while (true) {
+                s = ld_acquire(status + p);
+                if ((s >> 32) == 1 || (s >> 32) == 2 || ++spins >= kLookbackSpins) break;
+                __nanosleep(32);
+            }
+            if ((s >> 32) != 1 && (s >> 32) != 2) {
+                *timed_out = true;
+                s = 2ull << 32;
+            }
+        }
+        const unsigned incl = __ballot_sync(0xffffffffu, (s >> 32) == 2);
+        const int first = incl ? __ffs(incl) - 1 : 31;
+        excl += warp_sum(lane <= first ? (int32_t)(uint32_t)s : 0);
+        if (incl) break;
+    }
+    if (lane == 0) st_release(status + t, (2ull << 32) | (uint32_t)(excl + agg));
+    *timed_out = __any_sync(0xffffffffu, *timed_out);
+    return excl;
+}
+
 // Contiguous segment [lo, hi) of n items owned by block b of g.
 __device__ __forceinline__ void segment_of(int64_t n, int b, int g, int64_t& lo, int64_t& hi) {
     const int64_t len = (n + g - 1) / g;

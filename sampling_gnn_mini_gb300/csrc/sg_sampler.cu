@@ -18,18 +18,20 @@
 //    keeps the minimum edge position per node (atomicMin) and one flag + scan
 //    pass turns that into the deterministic first-occurrence numbering.
 //
-// Per hop h four kernels run (five for a super-batch):
-//   k_rows     [the map of hop h-1's edges, fused] and one pass over the dst
-//              rows V_{h-1}: c_v = min(deg, f), the block row pointer by a
-//              single-pass exclusive scan (decoupled look-back), per-row
-//              metadata, and the rows' degree bins (work order, largest first)
-//   k_sample   rows by bin: a warp per large row, an 8-lane group per small
-//              row; full rows are copied, random rows hashed with Philox;
-//              keys under a threshold are candidates and the f smallest are
-//              picked exactly
+// One memset clears the tables and scan state; then per hop h three kernels
+// run (four for a super-batch):
+//   k_rows     one pass over the dst rows V_{h-1}: c_v = min(deg, f), the
+//              block row pointer by a single-pass exclusive scan (decoupled
+//              look-back), per-row metadata and the rows' degree bins (work
+//              order, largest first).  For hop 1 it also places the seeds;
+//              for later hops it also maps the previous hop's edges.
+//   k_sample   rows by bin: a block per row longer than 4096, a warp per
+//              other long row, an 8-lane group per short row; full rows are
+//              copied, random rows hashed with Philox; keys under a threshold
+//              are candidates and the f smallest are picked exactly; every
+//              emitted neighbour goes into its mini-batch's table with value =
+//              its edge position (atomicMin keeps the first occurrence)
 //   k_copy     (super-batch only) rows whose node another row samples copy it
-//   k_insert   every sampled neighbour goes into its mini-batch's table with
-//              value = its edge position (atomicMin keeps the first)
 //   k_relabel  first-occurrence flags, ranked by a single-pass scan per
 //              mini-batch: new local IDs into the table and into V_h
 // and k_finish maps the last hop's edges (and lays a super-batch out).
@@ -50,9 +52,8 @@ constexpr int kNT = 256;             // threads of every sampler kernel (8 warps
 constexpr int kTile = 1024;          // rows / edges per scan tile (4 per thread)
 constexpr int kWarpCap = 256;        // candidate slots of a warp
 constexpr int kGroupCap = 128;       // candidate slots of an 8-lane group
-constexpr int kGroupLambdaMax = 64;  // groups take random rows only when f + 2 sqrt(f) + 4 <= this
+constexpr int kGroupLambdaMax = 0;   // groups take random rows only when f + 2 sqrt(f) + 4 <= this (never: a warp is faster)
 constexpr uint32_t kEmpty = 0xFFFFFFFFu;
-constexpr int kSpinLimit = 1 << 22;  // bound of a look-back wait (then the error word is set)
 
 struct SubPtr {
     int32_t v[SG_MAX_SUB + 1];
@@ -113,59 +114,6 @@ __device__ void load_prefix_sub_n(const int32_t* counts, CountsLayout L, int K, 
         pre[K] = acc;
     }
     __syncthreads();
-}
-
-// ------------------------------------------------- single-pass scan chains
-// Tile status words: (state << 32) | value, state 0 empty, 1 aggregate,
-// 2 inclusive prefix.  A block publishes its tile's aggregate, then walks back
-// over its predecessors until one has an inclusive prefix (decoupled
-// look-back).  Tiles are handed out in increasing order by an atomic counter,
-// so every predecessor belongs to a block that is already running; each wait
-// is still bounded and, if the bound is hit, reports ERR_TIMEOUT.
-__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long* p) {
-    unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_release(unsigned long long* p, unsigned long long v) {
-    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-// Exclusive prefix of tile t in the chain whose first tile is t0.  Called by
-// all 32 lanes of one warp: the warp reads 32 predecessors at once, adds the
-// aggregates up to the closest inclusive prefix, and moves the window back by
-// 32 only while none is inclusive.
-__device__ int32_t chain_lookback(unsigned long long* status, int t, int t0, int32_t agg) {
-    const int lane = (int)lane_id();
-    if (t == t0) {
-        if (lane == 0) st_release(status + t, (2ull << 32) | (uint32_t)agg);
-        return 0;
-    }
-    if (lane == 0) st_release(status + t, (1ull << 32) | (uint32_t)agg);
-    int32_t excl = 0;
-    for (int top = t - 1;; top -= 32) {
-        const int p = top - lane;
-        unsigned long long s = 2ull << 32;  // before the chain: an inclusive zero
-        if (p >= t0) {
-            int spins = 0;
-            while (true) {
-                s = ld_acquire(status + p);
-                if ((s >> 32) != 0 || ++spins >= kSpinLimit) break;
-                __nanosleep(32);
-            }
-            if ((s >> 32) == 0) {
-                dev_err(ERR_TIMEOUT);
-                s = 2ull << 32;
-            }
-        }
-        const unsigned incl = __ballot_sync(0xffffffffu, (s >> 32) == 2);
-        const int first = incl ? __ffs(incl) - 1 : 31;
-        excl += warp_sum(lane <= first ? (int32_t)(uint32_t)s : 0);
-        if (incl) break;
-    }
-    if (lane == 0) st_release(status + t, (2ull << 32) | (uint32_t)(excl + agg));
-    return excl;
 }
 
 // ------------------------------------------------------------------ seeds
@@ -256,13 +204,24 @@ __device__ void map_prev_edges(const HopArgs& a, int blk, int nblk, int32_t* ep,
     }
 }
 
+// In seed mode (hop 1) the rows are the seeds themselves, in the given order
+// (V_0 of every mini-batch, back to back): each is also placed, with local
+// ID = its index inside its mini-batch, in that mini-batch's table and V_0.
 template <typename Off>
-__global__ void __launch_bounds__(kNT) k_rows(HopArgs a) {
+__global__ void __launch_bounds__(kNT) k_rows(HopArgs a, int seed_mode, const int32_t* __restrict__ seeds,
+                                              SubPtr bptr) {
     __shared__ int32_t pre[SG_MAX_SUB + 1];
     __shared__ int32_t ep[SG_MAX_SUB + 1];
     __shared__ int32_t red[kNT / 32 + 1];
     __shared__ int32_t s_tile, s_excl, s_bcnt[4], s_bbase[4];
-    load_prefix_sub_n(a.counts, a.L, a.K, a.h - 1, pre);  // V_{h-1} per mini-batch
+    if (seed_mode) {
+        for (int k = threadIdx.x; k <= a.K; k += kNT) pre[k] = bptr.v[k];
+        __syncthreads();
+        if (blockIdx.x == 0)
+            for (int k = threadIdx.x; k < a.K; k += kNT) a.counts[a.L.sub_n(k, 0)] = pre[k + 1] - pre[k];
+    } else {
+        load_prefix_sub_n(a.counts, a.L, a.K, a.h - 1, pre);  // V_{h-1} per mini-batch
+    }
     const int64_t T = pre[a.K];
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         a.counts[a.L.tot_n(a.h - 1)] = (int32_t)T;
@@ -280,8 +239,14 @@ __global__ void __launch_bounds__(kNT) k_rows(HopArgs a) {
     const int f = a.fanout;
     const bool group_ok = a.lambda_num <= (uint32_t)kGroupLambdaMax;
     const int64_t n_tiles = (T + kTile - 1) / kTile;
-    while (true) {
-        if (threadIdx.x == 0) s_tile = (int32_t)atomicAdd(a.ctr + 0, 1u);
+    // blocks past the tile count leave at once; the others take tiles in
+    // order (one each unless the grid is smaller than the tile count)
+    const int64_t row_block = (int64_t)blockIdx.x - a.map_blocks;
+    const int64_t row_grid = (int64_t)gridDim.x - a.map_blocks;
+    if (row_block >= n_tiles) return;
+    for (int iter = 0;; ++iter) {
+        if (iter > 0 && row_grid >= n_tiles) break;
+        if (threadIdx.x == 0) s_tile = (int32_t)(atomicAdd(a.ctr + 0, 1u) + 1u);
         __syncthreads();
         const int64_t tile = s_tile;
         if (tile >= n_tiles) break;
@@ -296,7 +261,19 @@ __global__ void __launch_bounds__(kNT) k_rows(HopArgs a) {
             b[q] = -1;
             if (r < T) {
                 const int k = find_sub(pre, a.K, r);
-                const int32_t v = a.ustr[(int64_t)k * a.capU + (r - pre[k])];
+                int32_t v;
+                if (seed_mode) {
+                    v = seeds[r];
+                    const int32_t l = (int32_t)(r - pre[k]);
+                    a.ustr[(int64_t)k * a.capU + l] = v;
+                    if (v >= 0 && (int64_t)v < a.n_nodes) {
+                        bool present = false;
+                        table_insert(a.table + ((int64_t)k << a.logT), a.logT, v, (uint32_t)l, &present);
+                        if (present) dev_err(ERR_ARG);  // a repeated seed in one mini-batch
+                    }
+                } else {
+                    v = a.ustr[(int64_t)k * a.capU + (r - pre[k])];
+                }
                 int64_t start = 0, deg = 0;
                 if (v >= 0 && (int64_t)v < a.n_nodes) {
                     start = (int64_t)indptr[v];
@@ -317,8 +294,10 @@ __global__ void __launch_bounds__(kNT) k_rows(HopArgs a) {
         int32_t tile_total;
         const int32_t ex = block_excl_scan<kNT>(mysum, red, tile_total);
         if (threadIdx.x < 32) {
-            const int32_t x = chain_lookback(a.row_status, (int)tile, 0, tile_total);
+            bool late = false;
+            const int32_t x = chain_lookback(a.row_status, (int)tile, 0, tile_total, &late);
             if (threadIdx.x == 0) s_excl = x;
+            if (late && threadIdx.x == 0) dev_err(ERR_TIMEOUT);
         }
         // bin sizes of the tile, then one global atomic per bin
         if (threadIdx.x < 4) s_bcnt[threadIdx.x] = 0;
@@ -327,7 +306,8 @@ __global__ void __launch_bounds__(kNT) k_rows(HopArgs a) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) brank[q] = b[q] >= 0 ? atomicAdd(&s_bcnt[b[q]], 1) : 0;
         __syncthreads();
-        if (threadIdx.x < 4) s_bbase[threadIdx.x] = s_bcnt[threadIdx.x] ? (int32_t)atomicAdd(a.ctr + 2 + threadIdx.x, (uint32_t)s_bcnt[threadIdx.x]) : 0;
+        if (threadIdx.x < 4)
+            s_bbase[threadIdx.x] = s_bcnt[threadIdx.x] ? (int32_t)(atomicAdd(a.ctr + 2 + threadIdx.x, (uint32_t)s_bcnt[threadIdx.x]) + 1u) : 0;
         __syncthreads();
         int32_t off = s_excl + ex;
 #pragma unroll
@@ -357,7 +337,13 @@ __global__ void __launch_bounds__(kNT) k_rows(HopArgs a) {
 }
 
 // ------------------------------------------------------------------ sample
-__device__ __forceinline__ void emit_edge(const HopArgs& a, int64_t e, int32_t u) { a.enbr[e] = u; }
+// Edge e of mini-batch table `tab` gets node u: recorded, and inserted with
+// value = position (the table keeps each node's smallest).
+__device__ __forceinline__ void emit_edge(const HopArgs& a, uint2* tab, int64_t e, int32_t u) {
+    a.enbr[e] = u;
+    const int s = table_insert(tab, a.logT, u, (uint32_t)(a.pos_base + e), nullptr);
+    a.eslot[e] = s < 0 ? -1 : (int32_t)((int64_t)(tab - a.table) + s);
+}
 
 __device__ __forceinline__ unsigned long long min_u64_xor(unsigned long long x, unsigned mask, int width) {
     for (int d = width >> 1; d > 0; d >>= 1) {
@@ -371,7 +357,7 @@ __device__ __forceinline__ unsigned long long min_u64_xor(unsigned long long x, 
 // used only when the threshold filter cannot hold or find f keys.  A group is
 // W lanes (8 or 32) named by `mask`; cj has room for f entries.
 template <int W>
-__device__ void sample_exact(const HopArgs& a, uint32_t k0, uint32_t k1, int32_t v, int64_t start,
+__device__ void sample_exact(const HopArgs& a, uint2* tab, uint32_t k0, uint32_t k1, int32_t v, int64_t start,
                              int64_t deg, int64_t out0, int32_t* cj, unsigned mask, int gl) {
     const int f = a.fanout;
     unsigned long long prev = 0;
@@ -401,7 +387,7 @@ __device__ void sample_exact(const HopArgs& a, uint32_t k0, uint32_t k1, int32_t
         const int32_t x = cj[i];
         int rank = 0;
         for (int t = 0; t < f; ++t) rank += cj[t] < x;
-        emit_edge(a, out0 + rank, a.indices[start + x]);
+        emit_edge(a, tab, out0 + rank, a.indices[start + x]);
     }
     __syncwarp(mask);
 }
@@ -412,7 +398,7 @@ __device__ void sample_exact(const HopArgs& a, uint32_t k0, uint32_t k1, int32_t
 // f smallest in position order.  Falls back to sample_exact when the filter
 // overflows the buffer or, after two widenings, still holds fewer than f keys.
 template <int W, int CAP>
-__device__ void sample_random_row(const HopArgs& a, uint32_t k0, uint32_t k1, int32_t v, int64_t start,
+__device__ void sample_random_row(const HopArgs& a, uint2* tab, uint32_t k0, uint32_t k1, int32_t v, int64_t start,
                                   int64_t deg, int64_t out0, uint32_t* cr, int32_t* cj, unsigned mask, int gl) {
     const int f = a.fanout;
     const int shift = (int)(lane_id() & ~(unsigned)(W - 1));  // first lane of the group
@@ -479,13 +465,13 @@ __device__ void sample_random_row(const HopArgs& a, uint32_t k0, uint32_t k1, in
                 sel = rank < f;
             }
             const unsigned m = __ballot_sync(mask, sel) >> shift;
-            if (sel) emit_edge(a, out0 + sel_before + __popc(m & ltg), a.indices[start + cj[ci]]);
+            if (sel) emit_edge(a, tab, out0 + sel_before + __popc(m & ltg), a.indices[start + cj[ci]]);
             sel_before += __popc(m);
         }
         __syncwarp(mask);
         return;
     }
-    sample_exact<W>(a, k0, k1, v, start, deg, out0, cj, mask, gl);
+    sample_exact<W>(a, tab, k0, k1, v, start, deg, out0, cj, mask, gl);
 }
 
 // Row r of the frontier, by a group of W lanes.
@@ -499,19 +485,20 @@ __device__ void sample_row(const HopArgs& a, int32_t r, const int32_t* pre, uint
     if (a.utab && (a.rslot[r] < 0 || (int32_t)a.utab[a.rslot[r]].y != r)) return;  // another row samples this node
     const int64_t start = (int64_t)(uint32_t)m.x | ((int64_t)m.y << 32);
     const int64_t out0 = a.bindptr[r];
+    uint2* tab = a.table + ((int64_t)(a.K == 1 ? 0 : find_sub(pre, a.K, r)) << a.logT);
     if (deg <= a.fanout) {  // full node: every neighbour, in row order
-        for (int64_t t = gl; t < deg; t += W) emit_edge(a, out0 + t, a.indices[start + t]);
+        for (int64_t t = gl; t < deg; t += W) emit_edge(a, tab, out0 + t, a.indices[start + t]);
         return;
     }
-    sample_random_row<W, CAP>(a, k0, k1, v, start, deg, out0, cr, cj, mask, gl);
+    sample_random_row<W, CAP>(a, tab, k0, k1, v, start, deg, out0, cr, cj, mask, gl);
 }
 
 // A random row longer than 4096 by the whole block: each thread hashes one
 // counter block (4 positions) per step, candidates gather in shared memory
 // (order across warps is arbitrary, so the pick ranks by (key, position) and
 // the output is ordered by position afterwards).
-__device__ void sample_big_row(const HopArgs& a, int32_t r, uint32_t k0, uint32_t k1, uint32_t* cr, int32_t* cj,
-                               int32_t* s_n, int32_t* s_over) {
+__device__ void sample_big_row(const HopArgs& a, int32_t r, const int32_t* pre, uint32_t k0, uint32_t k1, uint32_t* cr,
+                               int32_t* cj, int32_t* s_n, int32_t* s_over) {
     constexpr int CAPB = 2048;  // candidates; cr[CAPB..2*CAPB) holds the pick flags
     const int4 m = a.rmeta[r];
     const int32_t v = m.w;
@@ -520,6 +507,7 @@ __device__ void sample_big_row(const HopArgs& a, int32_t r, uint32_t k0, uint32_
     if (a.utab && (a.rslot[r] < 0 || (int32_t)a.utab[a.rslot[r]].y != r)) return;
     const int64_t start = (int64_t)(uint32_t)m.x | ((int64_t)m.y << 32);
     const int64_t out0 = a.bindptr[r];
+    uint2* tab = a.table + ((int64_t)(a.K == 1 ? 0 : find_sub(pre, a.K, r)) << a.logT);
     const int f = a.fanout;
     const unsigned lane = lane_id();
     const unsigned long long tau64 = ((unsigned long long)a.lambda_num << 32) / (unsigned long long)deg;
@@ -583,12 +571,12 @@ __device__ void sample_big_row(const HopArgs& a, int32_t r, uint32_t k0, uint32_
             const int32_t ji = cj[i];
             int pos = 0;
             for (int t = 0; t < n; ++t) pos += picked[t] && cj[t] < ji;
-            emit_edge(a, out0 + pos, a.indices[start + ji]);
+            emit_edge(a, tab, out0 + pos, a.indices[start + ji]);
         }
         __syncthreads();
         return;
     }
-    if (threadIdx.x < 32) sample_exact<32>(a, k0, k1, v, start, deg, out0, cj, 0xffffffffu, (int)lane);
+    if (threadIdx.x < 32) sample_exact<32>(a, tab, k0, k1, v, start, deg, out0, cj, 0xffffffffu, (int)lane);
     __syncthreads();
 }
 
@@ -604,10 +592,12 @@ __global__ void __launch_bounds__(kNT) k_sample(HopArgs a) {
         k0 = (uint32_t)(sd & 0xFFFFFFFFull);
         k1 = (uint32_t)(sd >> 32);
     }
-    const int64_t n0 = a.ctr[2], n1 = a.ctr[3], n2 = a.ctr[4], n3 = a.ctr[5];
+    // the counters start at all-ones (the memset), so a count is the word + 1
+    const int64_t n0 = (uint32_t)(a.ctr[2] + 1u), n1 = (uint32_t)(a.ctr[3] + 1u), n2 = (uint32_t)(a.ctr[4] + 1u),
+                  n3 = (uint32_t)(a.ctr[5] + 1u);
     // rows of bin 3 first, a block each
     for (int64_t i = blockIdx.x; i < n3; i += gridDim.x)
-        sample_big_row(a, a.bins[3 * a.bin_stride + i], k0, k1, &cand_r[0][0], &cand_j[0][0], &s_n, &s_over);
+        sample_big_row(a, a.bins[3 * a.bin_stride + i], pre, k0, k1, &cand_r[0][0], &cand_j[0][0], &s_n, &s_over);
     // then work units: one per row of bin 2 (a warp each), one per four rows
     // of bins 1 and 0 (an 8-lane group each)
     const int64_t u32 = n2;
@@ -647,7 +637,8 @@ __global__ void __launch_bounds__(kNT) k_sample(HopArgs a) {
 
 // --------------------------------------------------------------------- copy
 // Super-batch: a row whose node was sampled by an earlier row (its owner)
-// copies the owner's neighbours into its own edge range.
+// copies the owner's neighbours into its own edge range and inserts them into
+// its own mini-batch's table at its own positions.
 __global__ void __launch_bounds__(kNT) k_copy(HopArgs a) {
     __shared__ int32_t pre[SG_MAX_SUB + 1];
     load_prefix_sub_n(a.counts, a.L, a.K, a.h - 1, pre);
@@ -660,23 +651,8 @@ __global__ void __launch_bounds__(kNT) k_copy(HopArgs a) {
         const int32_t owner = (int32_t)a.utab[s].y;
         if (owner == (int32_t)r || owner < 0 || (int64_t)owner >= T) continue;
         const int64_t o = a.bindptr[r], c = a.bindptr[r + 1] - o, so = a.bindptr[owner];
-        for (int64_t t = lane; t < c; t += 32) emit_edge(a, o + t, a.enbr[so + t]);
-    }
-}
-
-// ------------------------------------------------------------------ insert
-// Every edge's node goes into its mini-batch's table; the value kept is the
-// smallest edge position, i.e. the node's first occurrence in this hop.
-__global__ void __launch_bounds__(kNT) k_insert(HopArgs a) {
-    __shared__ int32_t ep[SG_MAX_SUB + 1];
-    for (int k = threadIdx.x; k <= a.K; k += kNT) ep[k] = a.epre[k];
-    __syncthreads();
-    const int64_t E = ep[a.K];
-    for (int64_t e = blockIdx.x * (int64_t)kNT + threadIdx.x; e < E; e += (int64_t)gridDim.x * kNT) {
-        const int32_t u = a.enbr[e];
-        const int k = a.K == 1 ? 0 : find_sub(ep, a.K, e);
-        const int s = table_insert(a.table + ((int64_t)k << a.logT), a.logT, u, (uint32_t)(a.pos_base + e), nullptr);
-        a.eslot[e] = s < 0 ? -1 : (int32_t)(((int64_t)k << a.logT) + s);
+        uint2* tab = a.table + ((int64_t)find_sub(pre, a.K, r) << a.logT);
+        for (int64_t t = lane; t < c; t += 32) emit_edge(a, tab, o + t, a.enbr[so + t]);
     }
 }
 
@@ -705,8 +681,10 @@ __global__ void __launch_bounds__(kNT) k_relabel(HopArgs a) {
         }
     }
     const int n_tiles = tpre[K];
-    while (true) {
-        if (threadIdx.x == 0) s_tile = (int32_t)atomicAdd(a.ctr + 1, 1u);
+    if ((int)blockIdx.x >= n_tiles) return;  // see k_rows
+    for (int iter = 0;; ++iter) {
+        if (iter > 0 && (int)gridDim.x >= n_tiles) break;
+        if (threadIdx.x == 0) s_tile = (int32_t)(atomicAdd(a.ctr + 1, 1u) + 1u);
         __syncthreads();
         const int t = s_tile;
         if (t >= n_tiles) break;
@@ -728,8 +706,10 @@ __global__ void __launch_bounds__(kNT) k_relabel(HopArgs a) {
         int32_t tile_total;
         const int32_t ex = block_excl_scan<kNT>(mine, red, tile_total);
         if (threadIdx.x < 32) {
-            const int32_t x = chain_lookback(a.edge_status, t, tpre[k], tile_total);
+            bool late = false;
+            const int32_t x = chain_lookback(a.edge_status, t, tpre[k], tile_total, &late);
             if (threadIdx.x == 0) s_excl = x;
+            if (late && threadIdx.x == 0) dev_err(ERR_TIMEOUT);
         }
         __syncthreads();
         const int32_t n_prev = a.counts[a.L.sub_n(k, a.h - 1)];
@@ -808,7 +788,7 @@ struct Plan {
     int logT;          // table slots per mini-batch = 2^logT
     int logU[SG_MAX_HOPS];
     int64_t nb_max, eb_max;
-    // workspace offsets; [o_table, o_zero) is set to 0xFF and [o_zero, o_rest) to 0 per call
+    // workspace offsets; [o_table, o_rest) is set to all-ones bytes per call
     size_t o_table, o_utab[SG_MAX_HOPS], o_zero, o_rstat[SG_MAX_HOPS], o_estat[SG_MAX_HOPS], o_ctr, o_rest;
     size_t o_ustr, o_rmeta, o_rslot, o_bins, o_enbr[2], o_eslot[2], o_epre, total;
 };
@@ -971,13 +951,10 @@ extern "C" sg_status sg_sampler_run(const sg_graph* g, const int32_t* d_seeds, i
     a.rslot = K > 1 ? (int32_t*)(ws + p.o_rslot) : nullptr;
     int32_t* epre_all = (int32_t*)(ws + p.o_epre);
 
-    SG_CUDA(cudaMemsetAsync(ws + p.o_table, 0xFF, p.o_zero - p.o_table, s));
-    SG_CUDA(cudaMemsetAsync(ws + p.o_zero, 0, p.o_rest - p.o_zero, s));
+    // tables, scan states and counters all start as all-ones bytes
+    SG_CUDA(cudaMemsetAsync(ws + p.o_table, 0xFF, p.o_rest - p.o_table, s));
     SubPtr bp;
     for (int k = 0; k <= K; ++k) bp.v[k] = p.bptr[k];
-    k_seed_init<<<n_seeds > 0 ? (int)cdiv(n_seeds, 256) : 1, 256, 0, s>>>(d_seeds, n_seeds, bp, K, g->n_nodes, a.table,
-                                                                          p.logT, a.ustr, p.capU, out->counts, L);
-    SG_CHECK_LAUNCH("k_seed_init");
     const int64_t cap_blocks = (int64_t)sms * 8;
     for (int h = 1; h <= H; ++h) {
         const int cur = (h - 1) & 1, prv = h & 1;
@@ -1000,8 +977,11 @@ extern "C" sg_status sg_sampler_run(const sg_graph* g, const int32_t* d_seeds, i
         const int64_t nb = p.nb_tot[h - 1], eb = p.eb_tot[h - 1];
         a.map_blocks = h > 1 ? (int)clamp_blocks(cdiv(p.eb_tot[h - 2], kNT * 8), cap_blocks) : 0;
         const int64_t row_blocks = clamp_blocks(cdiv(nb, kTile), cap_blocks);
-        if (g->offset_bits == 32) k_rows<int32_t><<<(unsigned)(a.map_blocks + row_blocks), kNT, 0, s>>>(a);
-        else k_rows<int64_t><<<(unsigned)(a.map_blocks + row_blocks), kNT, 0, s>>>(a);
+        const int seed_mode = h == 1;
+        if (g->offset_bits == 32)
+            k_rows<int32_t><<<(unsigned)(a.map_blocks + row_blocks), kNT, 0, s>>>(a, seed_mode, d_seeds, bp);
+        else
+            k_rows<int64_t><<<(unsigned)(a.map_blocks + row_blocks), kNT, 0, s>>>(a, seed_mode, d_seeds, bp);
         SG_CHECK_LAUNCH("k_rows");
         k_sample<<<(unsigned)clamp_blocks(cdiv(nb, kNT / 32), cap_blocks), kNT, 0, s>>>(a);
         SG_CHECK_LAUNCH("k_sample");
@@ -1009,8 +989,6 @@ extern "C" sg_status sg_sampler_run(const sg_graph* g, const int32_t* d_seeds, i
             k_copy<<<(unsigned)clamp_blocks(cdiv(nb, kNT / 32), cap_blocks), kNT, 0, s>>>(a);
             SG_CHECK_LAUNCH("k_copy");
         }
-        k_insert<<<(unsigned)clamp_blocks(cdiv(eb, kNT * 2), cap_blocks), kNT, 0, s>>>(a);
-        SG_CHECK_LAUNCH("k_insert");
         k_relabel<<<(unsigned)clamp_blocks(cdiv(eb, kTile) + K, cap_blocks), kNT, 0, s>>>(a);
         SG_CHECK_LAUNCH("k_relabel");
     }
@@ -1080,10 +1058,10 @@ sg_status relabel_launch(const RelabelPlan& p, char* ws, const int32_t* d_ids, i
     a.edge_status = (unsigned long long*)(ws + p.o_estat);
     a.h = 1;
     a.fanout = 1;
-    // the scratch may hold a previous call's contents: the table and the scan
-    // state are cleared before use, everything else is written before it is read
-    SG_CUDA(cudaMemsetAsync(ws + p.o_table, 0xFF, p.o_zero - p.o_table, s));
-    SG_CUDA(cudaMemsetAsync(ws + p.o_zero, 0, p.o_rest - p.o_zero, s));
+    // the scratch may hold a previous call's contents: the table, the scan
+    // state and the counter are reset (all-ones bytes) before use; everything
+    // else is written before it is read
+    SG_CUDA(cudaMemsetAsync(ws + p.o_table, 0xFF, p.o_rest - p.o_table, s));
     SubPtr bp;
     bp.v[0] = 0;
     bp.v[1] = (int32_t)n_prefix;

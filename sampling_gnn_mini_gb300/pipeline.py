@@ -5,8 +5,10 @@ seeds, aggregation inward from the input nodes):
   1. sg_sampler_run   V_0 .. V_H and the H blocks (sampling + relabel)
   2. sg_gather        X = features of V_H through the HBM cache
   3. sg_aggregate_fwd H_{h-1} = mean over block h of H_h, h = H .. 1 (H_H = X)
-  4. sg_aggregate_bwd G_h = transpose of block h applied to G_{h-1}, h = 1 .. H,
-                      with G_0 = H_0 (the gradient of 0.5 * ||H_0||^2)
+  4. sg_aggregate_bwd_t  G_h = transpose of block h applied to G_{h-1}, h = 1 .. H,
+                      with G_0 = H_0 (the gradient of 0.5 * ||H_0||^2); the
+                      transposed blocks (sg_transpose_blocks) are built on a
+                      second stream while 2 and 3 run
 Every size that depends on the sample stays on the device (the calls read
 the counts the sampler wrote), so a step has no host synchronisation and can
 be captured in a CUDA graph and replayed with new seeds (written into the
@@ -45,9 +47,10 @@ class MiniBatchPipeline:
         if backward:
             self.g_feat = [self.h_feat[0]] + [torch.empty(max(1, nb[h]), d, dtype=dt, device=device)
                                               for h in range(1, self.H + 1)]
-            ws = max(sg.sg_aggregate_bwd_workspace(nb[h - 1], nb[h], self.bounds.max_edges[h - 1])
-                     for h in range(1, self.H + 1))
-            self.bwd_ws = sg.aligned_workspace(ws, device)
+            self.tbuf = sg.TransposedBuffers(self.bounds, device)
+            self.side = torch.cuda.Stream(device=device)
+            self.ev_sampled = torch.cuda.Event()
+            self.ev_transposed = torch.cuda.Event()
 
     @property
     def counts(self) -> torch.Tensor:
@@ -79,20 +82,32 @@ class MiniBatchPipeline:
             sg.sg_aggregate_fwd(self.buf.indptr[h - 1], self.buf.idx[h - 1], nb[h - 1], nb[h], self.buf.dims(h),
                                 self.h_feat[h], self.h_feat[h - 1], stream=stream)
 
+    def transpose(self, stream=None) -> None:
+        sg.sg_transpose_blocks(self.buf, self.tbuf, stream=stream)
+
     def backward_pass(self, stream=None) -> None:
         nb = self.bounds.max_nodes
+        t = self.tbuf
         for h in range(1, self.H + 1):
-            sg.sg_aggregate_bwd(self.buf.indptr[h - 1], self.buf.idx[h - 1], nb[h - 1], nb[h],
-                                self.bounds.max_edges[h - 1], self.buf.dims(h), self.g_feat[h - 1], self.g_feat[h],
-                                self.bwd_ws, stream=stream)
+            sg.sg_aggregate_bwd_t(t.tptr[h - 1], t.tdst[h - 1], t.tw[h - 1], nb[h], nb[h - 1], self.buf.dims(h),
+                                  self.g_feat[h - 1], self.g_feat[h], stream=stream)
 
     def step(self, stream=None) -> None:
-        """Sample, gather, forward and (if enabled) backward of one batch."""
-        self.sample(stream)
-        self.gather(stream)
-        self.forward(stream)
+        """Sample, gather, forward and (if enabled) backward of one batch.
+        The transposed blocks are built on a second stream that forks after
+        sampling and joins before the backward pass."""
+        main = torch.cuda.current_stream() if stream is None else stream
+        self.sample(main)
         if self.backward:
-            self.backward_pass(stream)
+            self.ev_sampled.record(main)
+            self.side.wait_event(self.ev_sampled)
+            self.transpose(self.side)
+            self.ev_transposed.record(self.side)
+        self.gather(main)
+        self.forward(main)
+        if self.backward:
+            main.wait_event(self.ev_transposed)
+            self.backward_pass(main)
 
     def host_counts(self):
         c = self.buf.counts.cpu().tolist()

@@ -383,3 +383,25 @@ def test_pipeline_cuda_graph_replay_with_new_batches():
         torch.cuda.synchronize()
         sg.sg_stream_check()
         _check_pipeline_against_oracle(pipe, w, g, feat, seeds, w.sampler_seed(b))
+
+
+def test_transpose_blocks_match_stable_sort():
+    # the transposed blocks list each src row's edges in edge order, with the
+    # dst row and 1 / c_dst; compare with numpy's stable argsort
+    w, g = _tiny_graph()
+    G = sg.sg_graph_load(g.indptr.astype(np.int32), g.indices)
+    seeds = synth.batch_seeds(g.n, 1.0, 5, 256)
+    gpu = GpuSample(G, seeds, [10, 5, 3], 31)
+    tb = sg.TransposedBuffers(gpu.bounds)
+    sg.sg_transpose_blocks(gpu.buf, tb)
+    sg.sg_stream_check()
+    for h in range(3):
+        bp, idx = gpu.indptr[h], gpu.idx[h]
+        n_src = gpu.tot_nodes[h + 1]
+        order = np.argsort(idx, kind="stable")
+        dst = np.repeat(np.arange(len(bp) - 1), np.diff(bp))
+        want_ptr = np.concatenate([[0], np.cumsum(np.bincount(idx, minlength=n_src))]).astype(np.int32)
+        assert np.array_equal(tb.tptr[h][: n_src + 1].cpu().numpy(), want_ptr)
+        assert np.array_equal(tb.tdst[h][: len(idx)].cpu().numpy(), dst[order])
+        c = np.diff(bp)[dst[order]].astype(np.float32)
+        assert np.array_equal(tb.tw[h][: len(idx)].cpu().numpy(), (1.0 / c).astype(np.float32))
