@@ -131,9 +131,9 @@ class Workload:
 
 def kernels_per_step(H: int, n_sub: int) -> int:
     """Kernels one step launches: sampler 3 per hop (+1 per hop for a
-    super-batch) + 1, transposes 5, gather 1, forward 1 per hop, backward 1
+    super-batch) + 2, transposes 5, gather 1, forward 1 per hop, backward 1
     per hop."""
-    return (1 + 3 * H + (H if n_sub > 1 else 0)) + 5 + 1 + H + H
+    return (2 + 3 * H + (H if n_sub > 1 else 0)) + 5 + 1 + H + H
 
 
 def run_ours(args, rank, world, local):

@@ -107,7 +107,8 @@ typedef struct sg_sample_bounds {
     int64_t max_nodes[SG_MAX_HOPS + 1];  /* bound on sum_k |V_h^k|, h = 0..H */
     int64_t max_edges[SG_MAX_HOPS];      /* bound on sum_k E_h^k, index h-1 */
     int64_t counts_len;                  /* int32 entries of sg_blocks.counts */
-    size_t workspace_bytes;              /* device workspace sampler_run needs */
+    size_t workspace_bytes;              /* device workspace sampler_run needs (see
+                                            sg_sampler_workspace_init) */
 } sg_sample_bounds;
 
 /*   h_batch_ptr  host, n_sub+1 non-decreasing offsets into the seed array
@@ -146,6 +147,12 @@ typedef struct sg_blocks {
     int32_t* idx[SG_MAX_HOPS];
 } sg_blocks;
 
+/* Prepares a sampler workspace (sizes as in sg_sampler_bounds): clears its
+ * persistent part once.  Asynchronous on `stream`. */
+sg_status sg_sampler_workspace_init(const sg_graph* g, int32_t n_seeds, const int32_t* h_batch_ptr, int32_t n_sub,
+                                    const int32_t* h_fanouts, int32_t n_hops, void* d_workspace,
+                                    size_t workspace_bytes, sg_stream_t stream);
+
 /* Multi-hop sampling plus relabel (GARDEN page Section II-B and Fig. 1;
  * Section IV-C; Section IV-D; FastGL explainer "Fused-Map").
  * Hop h = 1..H samples every node v of V_{h-1}: with deg = the length of
@@ -165,8 +172,14 @@ typedef struct sg_blocks {
  *   seed / d_seed  the hash seed; when d_seed (device, one uint64) is not
  *                NULL it overrides `seed` and is read when the kernels run, so
  *                a captured CUDA graph can be replayed with a new seed.
- *   d_workspace  device scratch of at least bounds.workspace_bytes, 256-byte
- *                aligned; contents need no initialisation and are not kept.
+ *   d_workspace  device workspace of at least bounds.workspace_bytes, 256-byte
+ *                aligned, prepared once by sg_sampler_workspace_init for this
+ *                graph and these sizes.  Part of it persists: a direct map
+ *                with one 32-bit entry per node and mini-batch (the first
+ *                position of each sampled node, then its local ID) that every
+ *                run leaves cleared for the next.  Hand the same workspace to
+ *                no other call in between, and do not run two calls on it at
+ *                once.
  * Asynchronous on `stream`; no host synchronisation inside. */
 sg_status sg_sampler_run(const sg_graph* g, const int32_t* d_seeds, int32_t n_seeds, const int32_t* h_batch_ptr,
                          int32_t n_sub, const int32_t* h_fanouts, int32_t n_hops, uint64_t seed,

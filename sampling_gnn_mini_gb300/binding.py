@@ -41,7 +41,7 @@ EXPORTS = ["sg_version", "sg_last_error", "sg_stream_check", "sg_graph_load", "s
            "sg_sampler_bounds", "sg_sampler_run", "sg_relabel_workspace", "sg_relabel", "sg_cache_build",
            "sg_cache_destroy", "sg_cache_info", "sg_gather", "sg_aggregate_fwd", "sg_aggregate_bwd_workspace",
            "sg_aggregate_bwd", "sg_read_probe", "sg_hash_probe", "sg_relabel_noalloc", "sg_transpose_workspace",
-           "sg_transpose_blocks", "sg_aggregate_bwd_t"]
+           "sg_transpose_blocks", "sg_aggregate_bwd_t", "sg_sampler_workspace_init"]
 
 
 class SgError(RuntimeError):
@@ -116,6 +116,7 @@ def load(build_if_missing: bool = True):
             "sg_transpose_blocks": (i32, [ctypes.POINTER(_Blocks), vp, vp, i32, ctypes.POINTER(_Transposed), vp, sz,
                                           vp]),
             "sg_aggregate_bwd_t": (i32, [vp, vp, vp, i32, i32, vp, vp, i32, i32, vp, i32, vp]),
+            "sg_sampler_workspace_init": (i32, [vp, i32, vp, i32, vp, i32, vp, sz, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -231,9 +232,11 @@ def _aligned_bytes(nbytes: int, device, align: int = 256) -> torch.Tensor:
 
 
 class SampleBuffers:
-    """Caller-owned device arrays for sg_sampler_run, sized by the bounds."""
+    """Caller-owned device arrays for sg_sampler_run, sized by the bounds.
+    With the graph and sampling shape given, the workspace is also prepared
+    (sg_sampler_workspace_init); otherwise call init_workspace() before use."""
 
-    def __init__(self, bounds: Bounds, device="cuda"):
+    def __init__(self, bounds: Bounds, device="cuda", graph=None, n_seeds=None, fanouts=None, batch_ptr=None):
         self.bounds = bounds
         H = len(bounds.max_edges)
         self.n_hops = H
@@ -248,6 +251,15 @@ class SampleBuffers:
         for h in range(H):
             self._blocks.indptr[h] = self.indptr[h].data_ptr()
             self._blocks.idx[h] = self.idx[h].data_ptr()
+        if graph is not None:
+            self.init_workspace(graph, n_seeds, fanouts, batch_ptr)
+
+    def init_workspace(self, graph, n_seeds, fanouts, batch_ptr=None, stream=None) -> None:
+        fo = np.ascontiguousarray(fanouts, dtype=np.int32)
+        bp = None if batch_ptr is None else np.ascontiguousarray(batch_ptr, dtype=np.int32)
+        _check(load().sg_sampler_workspace_init(graph.handle, int(n_seeds), None if bp is None else bp.ctypes.data,
+                                                1 if bp is None else len(bp) - 1, fo.ctypes.data, len(fo),
+                                                self.workspace.data_ptr(), self.workspace.numel(), _stream(stream)))
 
     def dims(self, h: int) -> torch.Tensor:
         """Device int32[2] = {|V_{h-1}|, |V_h|} totals for the hop-h block."""

@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(kNT) k_spmm(const int32_t* __restrict__ ptr, c
                                               const int32_t* __restrict__ d_cols, const uint4* __restrict__ x,
                                               int32_t row_vecs, void* __restrict__ y) {
     constexpr int EPV = Elems<DT>::n;
-    constexpr int UE = VPL >= 4 ? 1 : (VPL == 2 ? 2 : 4);  // edges in flight per lane
+    constexpr int UE = VPL >= 8 ? 1 : (VPL == 4 ? 2 : 4);  // edges in flight per lane
     const int64_t n_rows = d_rows ? (int64_t)min(*d_rows, n_rows_cap) : n_rows_cap;
     const int32_t n_cols = d_cols ? min(*d_cols, n_cols_cap) : n_cols_cap;
     const unsigned lane = lane_id();
@@ -114,8 +114,19 @@ __global__ void __launch_bounds__(kNT) k_spmm(const int32_t* __restrict__ ptr, c
     // shuffles name only them, so groups of one warp proceed independently
     const unsigned gmask = LPR == 32 ? 0xffffffffu : (((1u << LPR) - 1u) << (lane - gl));
     const int64_t groups = (int64_t)gridDim.x * (kNT / LPR);
-    for (int64_t r = (blockIdx.x * (int64_t)kNT + threadIdx.x) / LPR; r < n_rows; r += groups) {
-        const int32_t lo = ptr[r], hi = ptr[r + 1];
+    int64_t r = (blockIdx.x * (int64_t)kNT + threadIdx.x) / LPR;
+    // the next row's bounds are loaded while the current row is summed
+    int32_t nlo = 0, nhi = 0;
+    if (r < n_rows) {
+        nlo = ptr[r];
+        nhi = ptr[r + 1];
+    }
+    for (; r < n_rows; r += groups) {
+        const int32_t lo = nlo, hi = nhi;
+        if (r + groups < n_rows) {
+            nlo = ptr[r + groups];
+            nhi = ptr[r + groups + 1];
+        }
         float acc[VPL][EPV];
 #pragma unroll
         for (int p = 0; p < VPL; ++p)

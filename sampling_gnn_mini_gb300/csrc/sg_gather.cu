@@ -7,8 +7,8 @@
 // (row, vector) so that consecutive threads copy consecutive 16-byte pieces
 // of the output: output stores are fully coalesced and each source row is
 // read as a contiguous run, from the cache or from the host table.  Every
-// thread keeps UNROLL independent loads in flight before it stores, which the
-// ~1-2 us latency of host-link reads needs.
+// thread keeps kUnroll (8) independent 16-byte loads in flight before it
+// stores, which the latency of host-link reads needs.
 #include "sg_internal.cuh"
 #include "sg_objects.cuh"
 
@@ -19,7 +19,7 @@ using namespace sgi;
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 4;
+constexpr int kUnroll = 8;
 
 __global__ void __launch_bounds__(kThreads) k_gather(const int32_t* __restrict__ ids, const int32_t* __restrict__ d_n,
                                                      int64_t n_cap, const int32_t* __restrict__ slot_of, int64_t n_nodes,

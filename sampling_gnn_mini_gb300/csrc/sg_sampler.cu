@@ -52,7 +52,7 @@ constexpr int kNT = 256;             // threads of every sampler kernel (8 warps
 constexpr int kTile = 1024;          // rows / edges per scan tile (4 per thread)
 constexpr int kWarpCap = 256;        // candidate slots of a warp
 constexpr int kGroupCap = 128;       // candidate slots of an 8-lane group
-constexpr int kGroupLambdaMax = 0;   // groups take random rows only when f + 2 sqrt(f) + 4 <= this (never: a warp is faster)
+constexpr int kGroupLambdaMax = 64;  // short random rows go to lockstep groups when f + 2 sqrt(f) + 4 <= this
 constexpr uint32_t kEmpty = 0xFFFFFFFFu;
 
 struct SubPtr {
@@ -165,7 +165,9 @@ struct HopArgs {
     int32_t* bindptr;
     int32_t* epre;           // [K+1] edge offset of each mini-batch in this hop
     int32_t* enbr;
-    int32_t* eslot;
+    int32_t* eslot;          // standalone relabel: table slot of each id
+    uint32_t* pos_of;        // sampler: direct map, [K][n_nodes] first position / local ID
+    const int32_t* prev_enbr;
     // super-batch owner rows
     uint2* utab;
     int logU;
@@ -194,11 +196,13 @@ __device__ void map_prev_edges(const HopArgs& a, int blk, int nblk, int32_t* ep,
     __syncthreads();
     const int64_t E = ep[K];
     for (int64_t e = (int64_t)blk * kNT + threadIdx.x; e < E; e += (int64_t)nblk * kNT) {
-        const int32_t s = a.prev_eslot[e];
+        const int k = K == 1 ? 0 : find_sub(ep, K, e);
         int32_t out = -1;
-        if (s >= 0) {
-            const int k = K == 1 ? 0 : find_sub(ep, K, e);
-            out = spre[k] + (int32_t)a.table[s].y;
+        if (a.pos_of) {
+            out = spre[k] + (int32_t)a.pos_of[(int64_t)k * a.n_nodes + a.prev_enbr[e]];
+        } else {
+            const int32_t s = a.prev_eslot[e];
+            if (s >= 0) out = spre[k] + (int32_t)a.table[s].y;
         }
         a.prev_bidx[e] = out;
     }
@@ -267,9 +271,8 @@ __global__ void __launch_bounds__(kNT) k_rows(HopArgs a, int seed_mode, const in
                     const int32_t l = (int32_t)(r - pre[k]);
                     a.ustr[(int64_t)k * a.capU + l] = v;
                     if (v >= 0 && (int64_t)v < a.n_nodes) {
-                        bool present = false;
-                        table_insert(a.table + ((int64_t)k << a.logT), a.logT, v, (uint32_t)l, &present);
-                        if (present) dev_err(ERR_ARG);  // a repeated seed in one mini-batch
+                        const uint32_t old = atomicMin(a.pos_of + (int64_t)k * a.n_nodes + v, (uint32_t)l);
+                        if (old != kEmpty) dev_err(ERR_ARG);  // a repeated seed in one mini-batch
                     }
                 } else {
                     v = a.ustr[(int64_t)k * a.capU + (r - pre[k])];
@@ -337,12 +340,19 @@ __global__ void __launch_bounds__(kNT) k_rows(HopArgs a, int seed_mode, const in
 }
 
 // ------------------------------------------------------------------ sample
-// Edge e of mini-batch table `tab` gets node u: recorded, and inserted with
-// value = position (the table keeps each node's smallest).
-__device__ __forceinline__ void emit_edge(const HopArgs& a, uint2* tab, int64_t e, int32_t u) {
+// Key threshold keeping about lam of deg positions as candidates; any value
+// gives the same sample (the filter only decides how many keys are ranked).
+__device__ __forceinline__ uint32_t threshold_for(uint32_t lam, int64_t deg) {
+    const float t = (float)lam * 4294967296.0f / (float)deg;
+    return t >= 4294967040.0f ? 0xFFFFFFFFu : (uint32_t)t;
+}
+
+// Edge e of a mini-batch gets node u: recorded, and the node's entry in the
+// mini-batch's direct map `pos` keeps the smallest position (no reply is
+// waited for).
+__device__ __forceinline__ void emit_edge(const HopArgs& a, uint32_t* pos, int64_t e, int32_t u) {
     a.enbr[e] = u;
-    const int s = table_insert(tab, a.logT, u, (uint32_t)(a.pos_base + e), nullptr);
-    a.eslot[e] = s < 0 ? -1 : (int32_t)((int64_t)(tab - a.table) + s);
+    atomicMin(pos + u, (uint32_t)(a.pos_base + e));
 }
 
 __device__ __forceinline__ unsigned long long min_u64_xor(unsigned long long x, unsigned mask, int width) {
@@ -357,7 +367,7 @@ __device__ __forceinline__ unsigned long long min_u64_xor(unsigned long long x, 
 // used only when the threshold filter cannot hold or find f keys.  A group is
 // W lanes (8 or 32) named by `mask`; cj has room for f entries.
 template <int W>
-__device__ void sample_exact(const HopArgs& a, uint2* tab, uint32_t k0, uint32_t k1, int32_t v, int64_t start,
+__device__ void sample_exact(const HopArgs& a, uint32_t* tab, uint32_t k0, uint32_t k1, int32_t v, int64_t start,
                              int64_t deg, int64_t out0, int32_t* cj, unsigned mask, int gl) {
     const int f = a.fanout;
     unsigned long long prev = 0;
@@ -398,32 +408,36 @@ __device__ void sample_exact(const HopArgs& a, uint2* tab, uint32_t k0, uint32_t
 // f smallest in position order.  Falls back to sample_exact when the filter
 // overflows the buffer or, after two widenings, still holds fewer than f keys.
 template <int W, int CAP>
-__device__ void sample_random_row(const HopArgs& a, uint2* tab, uint32_t k0, uint32_t k1, int32_t v, int64_t start,
+__device__ void sample_random_row(const HopArgs& a, uint32_t* tab, uint32_t k0, uint32_t k1, int32_t v, int64_t start,
                                   int64_t deg, int64_t out0, uint32_t* cr, int32_t* cj, unsigned mask, int gl) {
     const int f = a.fanout;
     const int shift = (int)(lane_id() & ~(unsigned)(W - 1));  // first lane of the group
     const unsigned ltg = (1u << gl) - 1u;
-    const unsigned long long tau64 = ((unsigned long long)a.lambda_num << 32) / (unsigned long long)deg;
-    uint32_t tau = tau64 > 0xFFFFFFFFull ? 0xFFFFFFFFu : (uint32_t)tau64;
+    uint32_t tau = threshold_for(a.lambda_num, deg);
     for (int attempt = 0; attempt < 3; ++attempt) {
         int n = 0;
         bool overflow = false;
-        // each step covers 8W positions: counter blocks q (first half) and
-        // q + W (second half) of every lane; appending is skipped unless some
-        // key of the step passes the threshold
-        for (int64_t base = 0; base < deg && !overflow; base += 8 * W) {
-            const int64_t qa = (base >> 2) + gl, qb = qa + W;
-            uint4 wa = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty), wb = wa;
-            if (4 * qa < deg) wa = philox4x32_10(make_uint4((uint32_t)qa, (uint32_t)v, (uint32_t)a.h, 0u), k0, k1);
-            if (4 * qb < deg) wb = philox4x32_10(make_uint4((uint32_t)qb, (uint32_t)v, (uint32_t)a.h, 0u), k0, k1);
-            const uint32_t lo = min(min(wa.x, wa.y), min(wa.z, wa.w)), hi = min(min(wb.x, wb.y), min(wb.z, wb.w));
+        // each step covers 4*U*W positions: counter blocks q + u*W (u < U) of
+        // every lane, hashed as U independent chains; appending is skipped
+        // unless some key of the step passes the threshold
+        constexpr int U = 2;
+        for (int64_t base = 0; base < deg && !overflow; base += 4 * U * W) {
+            uint4 wq[U];
+            uint32_t mn = 0xFFFFFFFFu;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t q = (base >> 2) + u * W + gl;
+                wq[u] = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty);
+                if (4 * q < deg) wq[u] = philox4x32_10(make_uint4((uint32_t)q, (uint32_t)v, (uint32_t)a.h, 0u), k0, k1);
+                mn = min(mn, min(min(wq[u].x, wq[u].y), min(wq[u].z, wq[u].w)));
+            }
             // lanes past the row end hold kEmpty keys; a real key equal to
             // kEmpty passes only when tau = kEmpty, and then the row is short
-            if (!__any_sync(mask, lo <= tau || hi <= tau)) continue;
+            if (!__any_sync(mask, mn <= tau)) continue;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const uint4 w = half ? wb : wa;
-                const int64_t j0 = 4 * (half ? qb : qa);
+            for (int u = 0; u < U; ++u) {
+                const uint4 w = wq[u];
+                const int64_t j0 = 4 * ((base >> 2) + u * W + gl);
                 const bool p0 = j0 + 0 < deg && w.x <= tau;
                 const bool p1 = j0 + 1 < deg && w.y <= tau;
                 const bool p2 = j0 + 2 < deg && w.z <= tau;
@@ -458,6 +472,7 @@ __device__ void sample_random_row(const HopArgs& a, uint2* tab, uint32_t k0, uin
             if (ci < n) {
                 const uint32_t ri = cr[ci];
                 int rank = 0;
+#pragma unroll 4
                 for (int t = 0; t < n; ++t) {
                     const uint32_t rt = cr[t];
                     rank += (rt < ri) || (rt == ri && t < ci);
@@ -485,7 +500,7 @@ __device__ void sample_row(const HopArgs& a, int32_t r, const int32_t* pre, uint
     if (a.utab && (a.rslot[r] < 0 || (int32_t)a.utab[a.rslot[r]].y != r)) return;  // another row samples this node
     const int64_t start = (int64_t)(uint32_t)m.x | ((int64_t)m.y << 32);
     const int64_t out0 = a.bindptr[r];
-    uint2* tab = a.table + ((int64_t)(a.K == 1 ? 0 : find_sub(pre, a.K, r)) << a.logT);
+    uint32_t* tab = a.pos_of + (int64_t)(a.K == 1 ? 0 : find_sub(pre, a.K, r)) * a.n_nodes;
     if (deg <= a.fanout) {  // full node: every neighbour, in row order
         for (int64_t t = gl; t < deg; t += W) emit_edge(a, tab, out0 + t, a.indices[start + t]);
         return;
@@ -507,21 +522,26 @@ __device__ void sample_big_row(const HopArgs& a, int32_t r, const int32_t* pre, 
     if (a.utab && (a.rslot[r] < 0 || (int32_t)a.utab[a.rslot[r]].y != r)) return;
     const int64_t start = (int64_t)(uint32_t)m.x | ((int64_t)m.y << 32);
     const int64_t out0 = a.bindptr[r];
-    uint2* tab = a.table + ((int64_t)(a.K == 1 ? 0 : find_sub(pre, a.K, r)) << a.logT);
+    uint32_t* tab = a.pos_of + (int64_t)(a.K == 1 ? 0 : find_sub(pre, a.K, r)) * a.n_nodes;
     const int f = a.fanout;
     const unsigned lane = lane_id();
-    const unsigned long long tau64 = ((unsigned long long)a.lambda_num << 32) / (unsigned long long)deg;
-    uint32_t tau = tau64 > 0xFFFFFFFFull ? 0xFFFFFFFFu : (uint32_t)tau64;
+    uint32_t tau = threshold_for(a.lambda_num, deg);
     for (int attempt = 0; attempt < 3; ++attempt) {
         if (threadIdx.x == 0) {
             *s_n = 0;
             *s_over = 0;
         }
         __syncthreads();
-        for (int64_t base = 0; base < deg; base += 4 * kNT) {
-            const int64_t q = (base >> 2) + threadIdx.x;
-            uint4 w = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty);
-            if (4 * q < deg) w = philox4x32_10(make_uint4((uint32_t)q, (uint32_t)v, (uint32_t)a.h, 0u), k0, k1);
+        for (int64_t base = 0; base < deg; base += 8 * kNT) {
+          const int64_t qa = (base >> 2) + threadIdx.x, qb = qa + kNT;
+          uint4 wab[2];
+          wab[0] = wab[1] = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty);
+          if (4 * qa < deg) wab[0] = philox4x32_10(make_uint4((uint32_t)qa, (uint32_t)v, (uint32_t)a.h, 0u), k0, k1);
+          if (4 * qb < deg) wab[1] = philox4x32_10(make_uint4((uint32_t)qb, (uint32_t)v, (uint32_t)a.h, 0u), k0, k1);
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const uint4 w = wab[half];
+            const int64_t q = half ? qb : qa;
             const uint32_t mn = min(min(w.x, w.y), min(w.z, w.w));
             if (!__any_sync(0xffffffffu, mn <= tau)) continue;
             const int64_t j0 = 4 * q;
@@ -547,6 +567,7 @@ __device__ void sample_big_row(const HopArgs& a, int32_t r, const int32_t* pre, 
             if (p1) { cr[p] = w.y; cj[p] = (int32_t)(j0 + 1); ++p; }
             if (p2) { cr[p] = w.z; cj[p] = (int32_t)(j0 + 2); ++p; }
             if (p3) { cr[p] = w.w; cj[p] = (int32_t)(j0 + 3); ++p; }
+          }
         }
         __syncthreads();
         const int n = *s_n;
@@ -578,6 +599,95 @@ __device__ void sample_big_row(const HopArgs& a, int32_t r, const int32_t* pre, 
     }
     if (threadIdx.x < 32) sample_exact<32>(a, tab, k0, k1, v, start, deg, out0, cj, 0xffffffffu, (int)lane);
     __syncthreads();
+}
+
+// Four short random rows at once, one per 8-lane group of the warp, in
+// lockstep: every loop runs to the warp-wide maximum trip count with per-group
+// predicates, and ballots name the whole warp, so the groups never diverge.
+// A group whose filter overflows or keeps fewer than f keys finishes alone on
+// the per-group path (rare).
+__device__ void sample_rows_x4(const HopArgs& a, int32_t r, bool valid, const int32_t* pre, uint32_t k0, uint32_t k1,
+                               uint32_t* cr, int32_t* cj) {
+    constexpr int G = 8, CAP = kGroupCap;
+    const unsigned lane = lane_id();
+    const int g = (int)(lane >> 3), gl = (int)(lane & 7), shift = 8 * g;
+    const unsigned gmask = 0xFFu << shift, ltg = (1u << gl) - 1u;
+    const int f = a.fanout;
+    int32_t v = 0;
+    int64_t deg = 0, start = 0, out0 = 0;
+    uint32_t* tab = a.pos_of;
+    if (valid) {
+        const int4 m = a.rmeta[r];
+        v = m.w;
+        deg = m.z;
+        valid = v >= 0 && (int64_t)v < a.n_nodes && deg > f;
+        if (valid && a.utab && (a.rslot[r] < 0 || (int32_t)a.utab[a.rslot[r]].y != r)) valid = false;
+        start = (int64_t)(uint32_t)m.x | ((int64_t)m.y << 32);
+        out0 = a.bindptr[r];
+        tab = a.pos_of + (int64_t)(a.K == 1 ? 0 : find_sub(pre, a.K, r)) * a.n_nodes;
+    }
+    const uint32_t tau = valid ? threshold_for(a.lambda_num, deg) : 0u;
+    const int steps = valid ? (int)((deg + 8 * G - 1) / (8 * G)) : 0;
+    const int max_steps = __reduce_max_sync(0xffffffffu, (unsigned)steps);
+    int n = 0;
+    bool over = false;
+    for (int step = 0; step < max_steps; ++step) {
+        const bool act = step < steps && !over;
+        const int64_t qa = (int64_t)step * 2 * G + gl, qb = qa + G;
+        uint4 wa = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty), wb = wa;
+        if (act && 4 * qa < deg) wa = philox4x32_10(make_uint4((uint32_t)qa, (uint32_t)v, (uint32_t)a.h, 0u), k0, k1);
+        if (act && 4 * qb < deg) wb = philox4x32_10(make_uint4((uint32_t)qb, (uint32_t)v, (uint32_t)a.h, 0u), k0, k1);
+        const uint32_t lo = min(min(wa.x, wa.y), min(wa.z, wa.w)), hi = min(min(wb.x, wb.y), min(wb.z, wb.w));
+        if (!__any_sync(0xffffffffu, act && (lo <= tau || hi <= tau))) continue;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const uint4 w = half ? wb : wa;
+            const int64_t j0 = 4 * (half ? qb : qa);
+            const bool p0 = act && j0 + 0 < deg && w.x <= tau;
+            const bool p1 = act && j0 + 1 < deg && w.y <= tau;
+            const bool p2 = act && j0 + 2 < deg && w.z <= tau;
+            const bool p3 = act && j0 + 3 < deg && w.w <= tau;
+            const unsigned m0 = (__ballot_sync(0xffffffffu, p0) & gmask) >> shift;
+            const unsigned m1 = (__ballot_sync(0xffffffffu, p1) & gmask) >> shift;
+            const unsigned m2 = (__ballot_sync(0xffffffffu, p2) & gmask) >> shift;
+            const unsigned m3 = (__ballot_sync(0xffffffffu, p3) & gmask) >> shift;
+            const int before = __popc(m0 & ltg) + __popc(m1 & ltg) + __popc(m2 & ltg) + __popc(m3 & ltg);
+            const int tot = __popc(m0) + __popc(m1) + __popc(m2) + __popc(m3);
+            if (act && n + tot > CAP) over = true;
+            if (act && !over) {
+                int p = n + before;  // candidates stay in ascending position order
+                if (p0) { cr[p] = w.x; cj[p] = (int32_t)(j0 + 0); ++p; }
+                if (p1) { cr[p] = w.y; cj[p] = (int32_t)(j0 + 1); ++p; }
+                if (p2) { cr[p] = w.z; cj[p] = (int32_t)(j0 + 2); ++p; }
+                if (p3) { cr[p] = w.w; cj[p] = (int32_t)(j0 + 3); ++p; }
+                n += tot;
+            }
+        }
+    }
+    __syncwarp();
+    const bool ok = valid && !over && n >= f;
+    // exact pick among the candidates, all groups together
+    const int n_max = __reduce_max_sync(0xffffffffu, ok ? (unsigned)n : 0u);
+    int sel_before = 0;
+    for (int c0 = 0; c0 < n_max; c0 += G) {
+        const int ci = c0 + gl;
+        const bool in = ok && ci < n;
+        const uint32_t ri = in ? cr[ci] : 0u;
+        int rank = 0;
+#pragma unroll 4
+        for (int t = 0; t < n_max; ++t) {
+            const uint32_t rt = cr[t < CAP ? t : 0];
+            rank += (t < n) && ((rt < ri) || (rt == ri && t < ci));
+        }
+        const bool sel = in && rank < f;
+        const unsigned m = (__ballot_sync(0xffffffffu, sel) & gmask) >> shift;
+        if (sel) emit_edge(a, tab, out0 + sel_before + __popc(m & ltg), a.indices[start + cj[ci]]);
+        sel_before += __popc(m);
+    }
+    __syncwarp();
+    // groups that need a retry or the exact pick finish on their own
+    if (valid && !ok) sample_random_row<G, CAP>(a, tab, k0, k1, v, start, deg, out0, cr, cj, gmask, gl);
+    __syncwarp();
 }
 
 __global__ void __launch_bounds__(kNT) k_sample(HopArgs a) {
@@ -626,7 +736,10 @@ __global__ void __launch_bounds__(kNT) k_sample(HopArgs a) {
                 bin = 0;
                 n = n0;
             }
-            if (i < n) {
+            if (bin == 1) {
+                const int32_t r = i < n ? a.bins[bin * a.bin_stride + i] : 0;
+                sample_rows_x4(a, r, i < n, pre, k0, k1, cr + g * kGroupCap, cj + g * kGroupCap);
+            } else if (i < n) {
                 const int32_t r = a.bins[bin * a.bin_stride + i];
                 sample_row<8, kGroupCap>(a, r, pre, k0, k1, cr + g * kGroupCap, cj + g * kGroupCap, gmask, gl);
             }
@@ -651,7 +764,7 @@ __global__ void __launch_bounds__(kNT) k_copy(HopArgs a) {
         const int32_t owner = (int32_t)a.utab[s].y;
         if (owner == (int32_t)r || owner < 0 || (int64_t)owner >= T) continue;
         const int64_t o = a.bindptr[r], c = a.bindptr[r + 1] - o, so = a.bindptr[owner];
-        uint2* tab = a.table + ((int64_t)find_sub(pre, a.K, r) << a.logT);
+        uint32_t* tab = a.pos_of + (int64_t)find_sub(pre, a.K, r) * a.n_nodes;
         for (int64_t t = lane; t < c; t += 32) emit_edge(a, tab, o + t, a.enbr[so + t]);
     }
 }
@@ -698,8 +811,12 @@ __global__ void __launch_bounds__(kNT) k_relabel(HopArgs a) {
             const int64_t e = e0 + q;
             fl[q] = false;
             if (e < e_end) {
-                const int32_t s = a.eslot[e];
-                fl[q] = s >= 0 && a.table[s].y == (uint32_t)(a.pos_base + e);
+                if (a.pos_of) {
+                    fl[q] = a.pos_of[(int64_t)k * a.n_nodes + a.enbr[e]] == (uint32_t)(a.pos_base + e);
+                } else {
+                    const int32_t s = a.eslot[e];
+                    fl[q] = s >= 0 && a.table[s].y == (uint32_t)(a.pos_base + e);
+                }
             }
             mine += fl[q];
         }
@@ -722,8 +839,10 @@ __global__ void __launch_bounds__(kNT) k_relabel(HopArgs a) {
                 if (lid >= a.capU) {
                     dev_err(ERR_CAPACITY);
                 } else {
-                    a.table[a.eslot[e]].y = (uint32_t)lid;
-                    a.ustr[(int64_t)k * a.capU + lid] = a.enbr[e];
+                    const int32_t u = a.enbr[e];
+                    if (a.pos_of) a.pos_of[(int64_t)k * a.n_nodes + u] = (uint32_t)lid;
+                    else a.table[a.eslot[e]].y = (uint32_t)lid;
+                    a.ustr[(int64_t)k * a.capU + lid] = u;
                 }
                 ++rank;
             }
@@ -749,6 +868,23 @@ __global__ void __launch_bounds__(kNT) k_finish(HopArgs a, int32_t* unique_out) 
             unique_out[i] = a.ustr[(int64_t)k * a.capU + (i - pre[k])];
         }
     }
+}
+
+// ----------------------------------------------------------------- cleanup
+// Leaves the workspace ready for the next call: every node of V_H gets its
+// direct-map entry back to empty, and the scan states and counters of all
+// hops are reset (all-ones).
+__global__ void __launch_bounds__(kNT) k_cleanup(HopArgs a, uint32_t* reset, int64_t reset_words) {
+    __shared__ int32_t pre[SG_MAX_SUB + 1];
+    load_prefix_sub_n(a.counts, a.L, a.K, a.h, pre);
+    const int64_t n = pre[a.K];
+    const int64_t stride = (int64_t)gridDim.x * kNT;
+    for (int64_t i = blockIdx.x * (int64_t)kNT + threadIdx.x; i < n; i += stride) {
+        const int k = a.K == 1 ? 0 : find_sub(pre, a.K, i);
+        const int32_t u = a.ustr[(int64_t)k * a.capU + (i - pre[k])];
+        if (u >= 0 && (int64_t)u < a.n_nodes) a.pos_of[(int64_t)k * a.n_nodes + u] = kEmpty;
+    }
+    for (int64_t i = blockIdx.x * (int64_t)kNT + threadIdx.x; i < reset_words; i += stride) reset[i] = kEmpty;
 }
 
 // ------------------------------------------------------ standalone relabel
@@ -785,12 +921,15 @@ struct Plan {
     int32_t fan[SG_MAX_HOPS];
     int64_t nb_tot[SG_MAX_HOPS + 1], eb_tot[SG_MAX_HOPS];
     int64_t capU;      // per mini-batch bound on |V_H^k|
-    int logT;          // table slots per mini-batch = 2^logT
     int logU[SG_MAX_HOPS];
     int64_t nb_max, eb_max;
-    // workspace offsets; [o_table, o_rest) is set to all-ones bytes per call
-    size_t o_table, o_utab[SG_MAX_HOPS], o_zero, o_rstat[SG_MAX_HOPS], o_estat[SG_MAX_HOPS], o_ctr, o_rest;
-    size_t o_ustr, o_rmeta, o_rslot, o_bins, o_enbr[2], o_eslot[2], o_epre, total;
+    // workspace: [o_pos, o_rest) persists between calls (all-ones when idle:
+    // set by sg_sampler_workspace_init, restored by every run's cleanup);
+    // [o_utab[0], o_scratch) is set to all-ones per call (super-batch only);
+    // the rest is scratch
+    size_t o_pos, o_zero, o_rstat[SG_MAX_HOPS], o_estat[SG_MAX_HOPS], o_ctr, o_rest;
+    size_t o_utab[SG_MAX_HOPS], o_scratch;
+    size_t o_ustr, o_rmeta, o_rslot, o_bins, o_enbr[2], o_epre, total;
 };
 
 sg_status make_plan(const sg_graph* g, int32_t n_seeds, const int32_t* h_bptr, int32_t n_sub, const int32_t* h_fan,
@@ -840,18 +979,12 @@ sg_status make_plan(const sg_graph* g, int32_t n_seeds, const int32_t* h_bptr, i
         if (p->nb_tot[h] > p->nb_max) p->nb_max = p->nb_tot[h];
         if (p->eb_tot[h] > p->eb_max) p->eb_max = p->eb_tot[h];
     }
-    // table values hold local IDs (< capU) and edge positions capU + e
+    // map values hold local IDs (< capU) and edge positions capU + e
     if (p->capU + p->eb_max >= 2147483647LL || p->nb_tot[n_hops] >= 2147483647LL)
         return fail(SG_ERR_UNSUPPORTED, "sampler: a mini-batch this large needs 64-bit local IDs");
-    p->logT = pow2_log(2 * p->capU);
     size_t o = 0;
-    p->o_table = o;
-    o = align256(o + (size_t)K * ((size_t)1 << p->logT) * sizeof(uint2));
-    for (int h = 0; h < n_hops; ++h) {
-        p->logU[h] = K > 1 ? pow2_log(2 * p->nb_tot[h]) : 0;
-        p->o_utab[h] = o;
-        if (K > 1) o = align256(o + ((size_t)1 << p->logU[h]) * sizeof(uint2));
-    }
+    p->o_pos = o;
+    o = align256(o + (size_t)K * (size_t)N * 4);
     p->o_zero = o;
     for (int h = 0; h < n_hops; ++h) {
         p->o_rstat[h] = o;
@@ -862,6 +995,12 @@ sg_status make_plan(const sg_graph* g, int32_t n_seeds, const int32_t* h_bptr, i
     p->o_ctr = o;
     o = align256(o + (size_t)n_hops * 8 * 4);
     p->o_rest = o;
+    for (int h = 0; h < n_hops; ++h) {
+        p->logU[h] = K > 1 ? pow2_log(2 * p->nb_tot[h]) : 0;
+        p->o_utab[h] = o;
+        if (K > 1) o = align256(o + ((size_t)1 << p->logU[h]) * sizeof(uint2));
+    }
+    p->o_scratch = o;
     p->o_ustr = o;
     o = align256(o + (K > 1 ? (size_t)K * (size_t)p->capU * 4 : 0));
     p->o_rmeta = o;
@@ -872,8 +1011,6 @@ sg_status make_plan(const sg_graph* g, int32_t n_seeds, const int32_t* h_bptr, i
     o = align256(o + 4 * (size_t)p->nb_max * 4);
     for (int i = 0; i < 2; ++i) {  // edge arrays alternate between hops (k_rows maps the previous hop's)
         p->o_enbr[i] = o;
-        o = align256(o + (size_t)p->eb_max * 4);
-        p->o_eslot[i] = o;
         o = align256(o + (size_t)p->eb_max * 4);
     }
     p->o_epre = o;
@@ -910,6 +1047,19 @@ extern "C" sg_status sg_sampler_bounds(const sg_graph* g, int32_t n_seeds, const
     return SG_OK;
 }
 
+extern "C" sg_status sg_sampler_workspace_init(const sg_graph* g, int32_t n_seeds, const int32_t* h_batch_ptr,
+                                               int32_t n_sub, const int32_t* h_fanouts, int32_t n_hops,
+                                               void* d_workspace, size_t workspace_bytes, sg_stream_t stream) {
+    Plan p;
+    sg_status st = make_plan(g, n_seeds, h_batch_ptr, n_sub, h_fanouts, n_hops, &p);
+    if (st != SG_OK) return st;
+    if (!d_workspace || workspace_bytes < p.total)
+        return fail(SG_ERR_INVALID_ARG, "sg_sampler_workspace_init: workspace needs %zu bytes", p.total);
+    if (((uintptr_t)d_workspace) % 256) return fail(SG_ERR_INVALID_ARG, "sg_sampler_workspace_init: workspace must be 256-byte aligned");
+    SG_CUDA(cudaMemsetAsync((char*)d_workspace + p.o_pos, 0xFF, p.o_rest - p.o_pos, (cudaStream_t)stream));
+    return SG_OK;
+}
+
 extern "C" sg_status sg_sampler_run(const sg_graph* g, const int32_t* d_seeds, int32_t n_seeds, const int32_t* h_batch_ptr,
                                     int32_t n_sub, const int32_t* h_fanouts, int32_t n_hops, uint64_t seed,
                                     const uint64_t* d_seed, void* d_workspace, size_t workspace_bytes,
@@ -935,7 +1085,6 @@ extern "C" sg_status sg_sampler_run(const sg_graph* g, const int32_t* d_seeds, i
     a.indices = g->indices;
     a.n_nodes = g->n_nodes;
     a.K = K;
-    a.logT = p.logT;
     a.capU = p.capU;
     a.key0 = (uint32_t)(seed & 0xFFFFFFFFull);
     a.key1 = (uint32_t)(seed >> 32);
@@ -944,15 +1093,17 @@ extern "C" sg_status sg_sampler_run(const sg_graph* g, const int32_t* d_seeds, i
     a.L = L;
     a.counts = out->counts;
     a.ustr = K > 1 ? (int32_t*)(ws + p.o_ustr) : out->unique;
-    a.table = (uint2*)(ws + p.o_table);
+    a.pos_of = (uint32_t*)(ws + p.o_pos);
     a.rmeta = (int4*)(ws + p.o_rmeta);
     a.bins = (int32_t*)(ws + p.o_bins);
     a.bin_stride = p.nb_max;
     a.rslot = K > 1 ? (int32_t*)(ws + p.o_rslot) : nullptr;
     int32_t* epre_all = (int32_t*)(ws + p.o_epre);
 
-    // tables, scan states and counters all start as all-ones bytes
-    SG_CUDA(cudaMemsetAsync(ws + p.o_table, 0xFF, p.o_rest - p.o_table, s));
+    // the direct map, scan states and counters arrive all-ones (left so by
+    // sg_sampler_workspace_init or the previous run); the owner tables of a
+    // super-batch are cleared here
+    if (K > 1) SG_CUDA(cudaMemsetAsync(ws + p.o_utab[0], 0xFF, p.o_scratch - p.o_utab[0], s));
     SubPtr bp;
     for (int k = 0; k <= K; ++k) bp.v[k] = p.bptr[k];
     const int64_t cap_blocks = (int64_t)sms * 8;
@@ -964,7 +1115,6 @@ extern "C" sg_status sg_sampler_run(const sg_graph* g, const int32_t* d_seeds, i
         a.bindptr = out->indptr[h - 1];
         a.epre = epre_all + (size_t)h * (SG_MAX_SUB + 1);
         a.enbr = (int32_t*)(ws + p.o_enbr[cur]);
-        a.eslot = (int32_t*)(ws + p.o_eslot[cur]);
         a.ctr = (uint32_t*)(ws + p.o_ctr) + (size_t)(h - 1) * 8;
         a.row_status = (unsigned long long*)(ws + p.o_rstat[h - 1]);
         a.edge_status = (unsigned long long*)(ws + p.o_estat[h - 1]);
@@ -973,7 +1123,7 @@ extern "C" sg_status sg_sampler_run(const sg_graph* g, const int32_t* d_seeds, i
         // the previous hop's edges are mapped inside this hop's row pass
         a.prev_bidx = h > 1 ? out->idx[h - 2] : nullptr;
         a.prev_epre = h > 1 ? epre_all + (size_t)(h - 1) * (SG_MAX_SUB + 1) : nullptr;
-        a.prev_eslot = h > 1 ? (const int32_t*)(ws + p.o_eslot[prv]) : nullptr;
+        a.prev_enbr = h > 1 ? (const int32_t*)(ws + p.o_enbr[prv]) : nullptr;
         const int64_t nb = p.nb_tot[h - 1], eb = p.eb_tot[h - 1];
         a.map_blocks = h > 1 ? (int)clamp_blocks(cdiv(p.eb_tot[h - 2], kNT * 8), cap_blocks) : 0;
         const int64_t row_blocks = clamp_blocks(cdiv(nb, kTile), cap_blocks);
@@ -995,11 +1145,15 @@ extern "C" sg_status sg_sampler_run(const sg_graph* g, const int32_t* d_seeds, i
     // the last hop's edges, the last total and the super-batch layout
     a.prev_bidx = out->idx[H - 1];
     a.prev_epre = epre_all + (size_t)H * (SG_MAX_SUB + 1);
-    a.prev_eslot = (const int32_t*)(ws + p.o_eslot[(H - 1) & 1]);
+    a.prev_enbr = (const int32_t*)(ws + p.o_enbr[(H - 1) & 1]);
     a.h = H;
     const int64_t fin = p.eb_tot[H - 1] > p.nb_tot[H] ? p.eb_tot[H - 1] : p.nb_tot[H];
     k_finish<<<(unsigned)clamp_blocks(cdiv(fin, kNT * 4), cap_blocks), kNT, 0, s>>>(a, K > 1 ? out->unique : nullptr);
     SG_CHECK_LAUNCH("k_finish");
+    const int64_t reset_words = (int64_t)(p.o_rest - p.o_zero) / 4;
+    k_cleanup<<<(unsigned)clamp_blocks(cdiv(p.nb_tot[H] > reset_words ? p.nb_tot[H] : reset_words, kNT * 4), cap_blocks),
+                kNT, 0, s>>>(a, (uint32_t*)(ws + p.o_zero), reset_words);
+    SG_CHECK_LAUNCH("k_cleanup");
     return SG_OK;
 }
 

@@ -34,7 +34,7 @@ class MiniBatchPipeline:
         self.batch_ptr = None if batch_ptr is None else [int(x) for x in batch_ptr]
         self.backward = backward
         self.bounds = sg.sg_sampler_bounds(graph, n_seeds, self.fanouts, self.batch_ptr)
-        self.buf = sg.SampleBuffers(self.bounds, device)
+        self.buf = sg.SampleBuffers(self.bounds, device, graph, n_seeds, self.fanouts, self.batch_ptr)
         dt = torch.float32 if cache.dtype == sg.SG_F32 else torch.bfloat16
         self.dtype = dt
         d = cache.dim

@@ -54,7 +54,7 @@ class GpuSample:
     def __init__(self, graph: sg.Graph, seeds, fanouts, seed, batch_ptr=None):
         seeds = np.ascontiguousarray(seeds, dtype=np.int32)
         self.bounds = sg.sg_sampler_bounds(graph, len(seeds), fanouts, batch_ptr)
-        self.buf = sg.SampleBuffers(self.bounds)
+        self.buf = sg.SampleBuffers(self.bounds, graph=graph, n_seeds=len(seeds), fanouts=fanouts, batch_ptr=batch_ptr)
         sg.sg_sampler_run(graph, dev_i32(seeds) if len(seeds) else torch.zeros(1, dtype=torch.int32, device="cuda")[:0],
                           fanouts, seed, self.buf, batch_ptr)
         sg.sg_stream_check()

@@ -299,7 +299,7 @@ def test_sampler_reports_bad_seeds():
     w, g = _tiny_graph()
     G = sg.sg_graph_load(g.indptr.astype(np.int32), g.indices)
     b = sg.sg_sampler_bounds(G, 3, [5])
-    buf = sg.SampleBuffers(b)
+    buf = sg.SampleBuffers(b, graph=G, n_seeds=3, fanouts=[5])
     sg.sg_sampler_run(G, dev_i32([1, 2, 1]), [5], 0, buf)
     with pytest.raises(sg.SgError) as e:
         sg.sg_stream_check()
@@ -405,3 +405,25 @@ def test_transpose_blocks_match_stable_sort():
         assert np.array_equal(tb.tdst[h][: len(idx)].cpu().numpy(), dst[order])
         c = np.diff(bp)[dst[order]].astype(np.float32)
         assert np.array_equal(tb.tw[h][: len(idx)].cpu().numpy(), (1.0 / c).astype(np.float32))
+
+
+def test_sampler_workspace_reused_across_runs_and_errors():
+    # the persistent part of the workspace is left clean by every run, also
+    # after a run that reported a repeated seed
+    w, g = _tiny_graph()
+    G = sg.sg_graph_load(g.indptr.astype(np.int32), g.indices)
+    b = sg.sg_sampler_bounds(G, 128, [10, 5])
+    buf = sg.SampleBuffers(b, graph=G, n_seeds=128, fanouts=[10, 5])
+    for it, bi in enumerate([0, 1, 0, 2]):
+        seeds = synth.batch_seeds(g.n, 1.0, bi, 128)
+        if it == 2:
+            bad = seeds.copy()
+            bad[7] = bad[3]
+            sg.sg_sampler_run(G, dev_i32(bad), [10, 5], 99, buf)
+            with pytest.raises(sg.SgError):
+                sg.sg_stream_check()
+        sg.sg_sampler_run(G, dev_i32(seeds), [10, 5], 99, buf)
+        sg.sg_stream_check()
+        ref = oracle.sampler_run(g.indptr, g.indices, seeds, [10, 5], 99)
+        assert np.array_equal(buf.unique.cpu().numpy()[: ref.hop_off[-1]], ref.unique)
+        assert np.array_equal(buf.idx[1].cpu().numpy()[: len(ref.idx[1])], ref.idx[1])
