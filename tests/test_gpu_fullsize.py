@@ -1,0 +1,192 @@
+"""Parity at the full sizes of the Skew, Billion-edge and Wide workloads, in
+the launch configuration the benchmark uses (MiniBatchPipeline: sample,
+transpose, gather, forward, backward).
+
+The oracle recomputes what it can one by one: whole mini-batches of the
+sampler (two sub-batches of a super-batch), sampled rows of the gather, and
+sampled dst rows of every aggregation hop (each on the GPU's own input rows).
+"""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from helpers import as_f64, assert_close, dev_i32, torch_to_np
+from sampling_gnn_mini_gb300 import binding as sg
+from sampling_gnn_mini_gb300.pipeline import MiniBatchPipeline
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+TOL = {"f32": 1e-5, "bf16": 1e-2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    sg.load()
+    yield
+    torch.cuda.synchronize()
+
+
+class PinnedTable:
+    """The whole feature table in page-locked host memory (as the benchmark
+    holds it), with a numpy view for the checks (bf16 as uint16 bits)."""
+
+    def __init__(self, n, dim, dtype, seed):
+        self.t = torch.empty((n, dim), dtype=torch.float32 if dtype == "f32" else torch.bfloat16, pin_memory=True)
+        synth.features_into(self.t.data_ptr(), 0, n, dim, dtype, seed)
+        self.arr = self.t.numpy() if dtype == "f32" else self.t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _take(t, rows):
+    """Rows of a tensor, as numpy (bf16 as uint16 bits)."""
+    return torch_to_np(t[torch.from_numpy(np.asarray(rows, dtype=np.int64)).to(t.device)])
+
+
+def _sub_blocks(pipe, k):
+    """Mini-batch k of a super-batch from the pipeline's concatenated layout."""
+    c = pipe.buf.counts.cpu().numpy()
+    H, K = pipe.H, len(pipe.batch_ptr) - 1 if pipe.batch_ptr else 1
+    per = np.array([[c[(2 * H + 1) * (1 + kk) + h] for h in range(H + 1)] for kk in range(K)], np.int64)
+    off = np.concatenate([np.zeros((1, H + 1), np.int64), np.cumsum(per, axis=0)])
+    u0 = off[k, H]
+    unique = pipe.buf.unique[u0: u0 + per[k, H]].cpu().numpy()
+    blocks = []
+    for h in range(1, H + 1):
+        r0, r1 = off[k, h - 1], off[k, h - 1] + per[k, h - 1]
+        ip = pipe.buf.indptr[h - 1][r0: r1 + 1].cpu().numpy().astype(np.int64)
+        idx = pipe.buf.idx[h - 1][ip[0]: ip[-1]].cpu().numpy().astype(np.int64) - off[k, h]
+        blocks.append((ip - ip[0], idx.astype(np.int32)))
+    return per[k].tolist(), unique, blocks
+
+
+def _check_sampling(pipe, g, seeds_k, k, fanouts, seed):
+    ref = oracle.sampler_run(g.indptr, g.indices, seeds_k, fanouts, seed)
+    n, unique, blocks = _sub_blocks(pipe, k)
+    assert n == list(ref.hop_off)
+    assert np.array_equal(unique, ref.unique)
+    for h in range(len(fanouts)):
+        assert np.array_equal(blocks[h][0], ref.indptr[h]), "indptr, hop %d" % (h + 1)
+        assert np.array_equal(blocks[h][1], ref.idx[h]), "idx, hop %d" % (h + 1)
+
+
+def _check_gather(pipe, feat, rng, n_check=3000):
+    H = pipe.H
+    n = int(pipe.buf.counts[H].item())
+    rows = rng.choice(n, size=min(n, n_check), replace=False)
+    ids = _take(pipe.buf.unique, rows)
+    got = _take(pipe.x, rows)
+    assert np.array_equal(got, feat[ids])
+
+
+def _check_aggregation(pipe, rng, dtype, n_check=600):
+    H = pipe.H
+    c = pipe.buf.counts.cpu().numpy()
+    for h in range(1, H + 1):
+        n_dst, n_src = int(c[h - 1]), int(c[h])
+        ip = pipe.buf.indptr[h - 1][: n_dst + 1].cpu().numpy().astype(np.int64)
+        idx = pipe.buf.idx[h - 1][: ip[-1]].cpu().numpy()
+        # forward: sampled dst rows, on the GPU's own H_h
+        rows = rng.choice(n_dst, size=min(n_dst, n_check), replace=False)
+        sub_ip = np.concatenate([[0], np.cumsum(ip[rows + 1] - ip[rows])])
+        sub_idx = np.concatenate([idx[ip[r]:ip[r + 1]] for r in rows]) if len(rows) else np.zeros(0, np.int32)
+        uniq, loc = np.unique(sub_idx, return_inverse=True)
+        hin = _take(pipe.h_feat[h], uniq)
+        want, am = oracle.aggregate_fwd(sub_ip, loc.astype(np.int32), hin)
+        got = as_f64(_take(pipe.h_feat[h - 1], rows))
+        assert_close(got, want, am, TOL[dtype], "forward hop %d" % h)
+        # backward: sampled src rows u, summing over the dst rows that name u
+        srcs = rng.choice(n_src, size=min(n_src, n_check), replace=False)
+        order = np.argsort(idx, kind="stable")
+        tptr = np.concatenate([[0], np.cumsum(np.bincount(idx, minlength=n_src))])
+        dst_of = np.repeat(np.arange(n_dst), np.diff(ip))
+        cnt = np.diff(ip)
+        gdst_all_rows = np.unique(np.concatenate([dst_of[order[tptr[u]:tptr[u + 1]]] for u in srcs]))
+        gd = _take(pipe.g_feat[h - 1], gdst_all_rows)
+        pos = {int(v): i for i, v in enumerate(gdst_all_rows)}
+        # a small transposed problem: one "dst" row per sampled src
+        b_ip, b_idx, b_w = [0], [], []
+        for u in srcs:
+            for e in order[tptr[u]:tptr[u + 1]]:
+                b_idx.append(pos[int(dst_of[e])])
+                b_w.append(1.0 / cnt[dst_of[e]])
+            b_ip.append(len(b_idx))
+        gdf = as_f64(gd)
+        want = np.zeros((len(srcs), gd.shape[1]))
+        am = np.zeros_like(want)
+        for i in range(len(srcs)):
+            for p in range(b_ip[i], b_ip[i + 1]):
+                want[i] += gdf[b_idx[p]] * b_w[p]
+                am[i] += np.abs(gdf[b_idx[p]]) * b_w[p]
+        got = as_f64(_take(pipe.g_feat[h], srcs))
+        assert_close(got, want, am, TOL[dtype], "backward hop %d" % h)
+
+
+# ----------------------------------------------------------------- Skew
+SKEW = [("skew_g1.8_b512", (0, 7)), ("skew_g2.0_b512", (0, 7)), ("skew_g2.3_b512", (0, 7)),
+        ("skew_g2.6_b512", (0, 7)), ("skew_g2.0_b4096", (0, 3))]
+
+
+@pytest.mark.parametrize("name,check_subs", SKEW)
+def test_skew_super_batch_full_size(name, check_subs):
+    w = synth.workload(name)
+    g = synth.chung_lu(w.n_nodes, w.mean_deg, w.gamma, w.wmax, w.rng_seed)
+    G = sg.sg_graph_load(g.indptr.astype(np.int32), g.indices)
+    feat = synth.features(w.n_nodes, w.dim, w.dtype, w.rng_seed)
+    d_feat = torch.from_numpy(feat).cuda()
+    cache = sg.sg_cache_build(None, d_feat, sg.SG_F32, w.n_nodes, w.dim, None, w.n_nodes)  # 100% in HBM
+    del d_feat
+    bs = synth.BatchStream(w)
+    seed_lists = [bs.seeds(k) for k in range(w.n_sub)]
+    bptr = np.concatenate([[0], np.cumsum([len(s) for s in seed_lists])]).tolist()
+    pipe = MiniBatchPipeline(G, cache, w.fanouts, bptr[-1], batch_ptr=bptr)
+    seed = w.sampler_seed(0)
+    pipe.set_batch(dev_i32(np.concatenate(seed_lists)), seed)
+    pipe.step()
+    sg.sg_stream_check()
+    for k in check_subs:
+        _check_sampling(pipe, g, seed_lists[k], k, w.fanouts, seed)
+    rng = np.random.default_rng(1)
+    _check_gather(pipe, feat, rng)
+    _check_aggregation(pipe, rng, w.dtype)
+    del pipe, cache, G, feat
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+# ------------------------------------------------- Billion-edge and Wide
+@pytest.mark.parametrize("name", ["billion", "wide"])
+def test_host_feature_workloads_full_size(name):
+    w = synth.workload(name)
+    g = synth.chung_lu(w.n_nodes, w.mean_deg, w.gamma, w.wmax, w.rng_seed)
+    indptr = g.indptr if w.offset_bits == 64 else g.indptr.astype(np.int32)
+    G = sg.sg_graph_load(indptr, g.indices, w.offset_bits)
+    assert G.offset_bits == w.offset_bits
+    table = PinnedTable(w.n_nodes, w.dim, w.dtype, w.rng_seed)
+    try:
+        deg = np.diff(g.indptr)
+        ranked = np.argpartition(-deg, w.cache_rows - 1)[: w.cache_rows].astype(np.int32)  # the hubs: speed only
+        cache = sg.sg_cache_build(table.t, None, sg.SG_F32 if w.dtype == "f32" else sg.SG_BF16, w.n_nodes, w.dim,
+                                  ranked, w.cache_rows)
+        pipe = MiniBatchPipeline(G, cache, w.fanouts, w.batch)
+        bs = synth.BatchStream(w)
+        seeds = bs.seeds(0)
+        pipe.set_batch(dev_i32(seeds), w.sampler_seed(0))
+        pipe.step()
+        sg.sg_stream_check()
+        hits, misses = pipe.stats.cpu().tolist()
+        assert misses > 0 and hits > 0  # both the HBM cache and the host table were read
+        _check_sampling(pipe, g, seeds, 0, w.fanouts, w.sampler_seed(0))
+        rng = np.random.default_rng(2)
+        _check_gather(pipe, table.arr, rng)
+        _check_aggregation(pipe, rng, w.dtype)
+        del pipe, cache
+    finally:
+        torch.cuda.synchronize()
+    del table, G, g
+    gc.collect()
+    torch.cuda.empty_cache()
