@@ -18,23 +18,27 @@
 //    keeps the minimum edge position per node (atomicMin) and one flag + scan
 //    pass turns that into the deterministic first-occurrence numbering.
 //
-// One memset clears the tables and scan state; then per hop h three kernels
-// run (four for a super-batch):
+// The workspace holds, per mini-batch, a direct map from node ID to the
+// smallest edge position that names it (then to its local ID); it and the
+// scan states arrive all-ones and every run leaves them so (k_cleanup).  Per
+// hop h three kernels run (four for a super-batch):
 //   k_rows     one pass over the dst rows V_{h-1}: c_v = min(deg, f), the
 //              block row pointer by a single-pass exclusive scan (decoupled
 //              look-back), per-row metadata and the rows' degree bins (work
 //              order, largest first).  For hop 1 it also places the seeds;
 //              for later hops it also maps the previous hop's edges.
-//   k_sample   rows by bin: a block per row longer than 4096, a warp per
-//              other long row, an 8-lane group per short row; full rows are
-//              copied, random rows hashed with Philox; keys under a threshold
-//              are candidates and the f smallest are picked exactly; every
-//              emitted neighbour goes into its mini-batch's table with value =
-//              its edge position (atomicMin keeps the first occurrence)
+//   k_sample   rows by bin, handed out by counters: a block per row longer
+//              than 4096, a warp per other long row, an 8-lane group per
+//              short row; full rows are copied, random rows hashed with
+//              Philox; keys under a threshold are candidates (a shared-memory
+//              pool) and the f smallest are picked exactly; every emitted
+//              neighbour records its edge position in its mini-batch's map
+//              (atomicMin keeps the first occurrence)
 //   k_copy     (super-batch only) rows whose node another row samples copy it
 //   k_relabel  first-occurrence flags, ranked by a single-pass scan per
-//              mini-batch: new local IDs into the table and into V_h
-// and k_finish maps the last hop's edges (and lays a super-batch out).
+//              mini-batch: new local IDs into the map and into V_h
+// then k_finish maps the last hop's edges (and lays a super-batch out) and
+// k_cleanup restores the workspace.
 #include <string.h>
 
 #include <mutex>
@@ -50,9 +54,7 @@ namespace {
 
 constexpr int kNT = 256;             // threads of every sampler kernel (8 warps)
 constexpr int kTile = 1024;          // rows / edges per scan tile (4 per thread)
-constexpr int kWarpCap = 256;        // candidate slots of a warp
-constexpr int kGroupCap = 128;       // candidate slots of an 8-lane group
-constexpr int kGroupLambdaMax = 64;  // short random rows go to lockstep groups when f + 2 sqrt(f) + 4 <= this
+constexpr int kGroupLambdaMax = 64;  // short random rows go to 8-lane groups when f + 2 sqrt(f) + 4 <= this
 constexpr uint32_t kEmpty = 0xFFFFFFFFu;
 
 struct SubPtr {
@@ -402,97 +404,149 @@ __device__ void sample_exact(const HopArgs& a, uint32_t* tab, uint32_t k0, uint3
     __syncwarp(mask);
 }
 
-// One random row by a group of W lanes (W = 8 or 32) named by `mask`:
-// hash every position (4 per lane per step), keep keys <= tau in position
-// order (candidate buffer of CAP), rank them by (key, position) and emit the
-// f smallest in position order.  Falls back to sample_exact when the filter
-// overflows the buffer or, after two widenings, still holds fewer than f keys.
-template <int W, int CAP>
-__device__ void sample_random_row(const HopArgs& a, uint32_t* tab, uint32_t k0, uint32_t k1, int32_t v, int64_t start,
-                                  int64_t deg, int64_t out0, uint32_t* cr, int32_t* cj, unsigned mask, int gl) {
+// Candidates: a pool holds the key (Philox word) and the row position of
+// every candidate in two arrays, keys[] and pos[], filled in arbitrary order.
+constexpr int kWarpPool = 512;                      // candidates of a warp
+constexpr int kGroupPool = kWarpPool / 4;           // of an 8-lane group
+constexpr int kBlockPool = kWarpPool * (kNT / 32);  // of a block (rows longer than 4096)
+constexpr int kWarpSel = 256;                       // picked positions of a warp (f <= 256)
+constexpr int kGroupSel = kWarpSel / 4;             // of an 8-lane group (f + 2 sqrt(f) + 4 <= 64)
+
+struct Pool {
+    uint32_t* keys;  // room for cap entries, 16-byte aligned, cap a multiple of 4
+    uint32_t* pos;
+    uint32_t* sel;   // room for f entries
+    int* n;          // fill count (shared)
+    int cap;
+};
+
+// Adds one candidate; past cap the entry is dropped, and the caller sees the
+// overflow as *n > cap.
+__device__ __forceinline__ void push_cand(const Pool& p, uint32_t key, uint32_t j) {
+    const int s = atomicAdd(p.n, 1);
+    if (s < p.cap) {
+        p.keys[s] = key;
+        p.pos[s] = j;
+    }
+}
+
+// The positions of counter block q (4q .. 4q+3, those below deg) whose key is
+// at most tau.  4q < deg holds.
+__device__ __forceinline__ void filter_block(const uint4& w, uint32_t q, uint32_t deg, uint32_t tau, const Pool& p) {
+    const uint32_t j0 = 4u * q, rem = deg - j0;
+    if (w.x <= tau) push_cand(p, w.x, j0);
+    if (w.y <= tau && rem > 1u) push_cand(p, w.y, j0 + 1u);
+    if (w.z <= tau && rem > 2u) push_cand(p, w.z, j0 + 2u);
+    if (w.w <= tau && rem > 3u) push_cand(p, w.w, j0 + 3u);
+}
+
+// Hashes every position of row v by `nthr` threads (this one is number t):
+// each step takes counter blocks t and t + nthr of the next 2 * nthr, as two
+// independent Philox chains.
+__device__ __forceinline__ void hash_row(const HopArgs& a, uint32_t k0, uint32_t k1, int32_t v, uint32_t deg,
+                                         uint32_t tau, const Pool& p, uint32_t t, uint32_t nthr) {
+    const uint32_t qn = (deg + 3u) >> 2;
+    for (uint32_t qb = 0; qb < qn; qb += 2u * nthr) {
+        const uint32_t qa = qb + t, qc = qa + nthr;
+        const uint4 wa = philox4x32_10(make_uint4(qa, (uint32_t)v, (uint32_t)a.h, 0u), k0, k1);
+        const uint4 wc = philox4x32_10(make_uint4(qc, (uint32_t)v, (uint32_t)a.h, 0u), k0, k1);
+        if (qa < qn) filter_block(wa, qa, deg, tau, p);
+        if (qc < qn) filter_block(wc, qc, deg, tau, p);
+    }
+}
+
+__device__ __forceinline__ uint32_t widen(uint32_t tau) { return tau > 0x3FFFFFFFu ? 0xFFFFFFFFu : (tau << 2) | 3u; }
+
+// A group of threads that picks together: W lanes of a warp named by a mask,
+// or the whole block.
+struct LaneGroup {
+    unsigned mask;
+    __device__ void sync() const { __syncwarp(mask); }
+    __device__ bool any(bool x) const { return __any_sync(mask, x); }
+};
+struct BlockGroup {
+    __device__ void sync() const { __syncthreads(); }
+    __device__ bool any(bool x) const { return __syncthreads_or(x) != 0; }
+};
+
+// The f smallest of the n pool candidates (f <= n <= cap) by (key, position),
+// emitted in position order.  A candidate's rank is the number of keys below
+// its own (16-byte loads of four keys at a time); a candidate of rank r < f
+// puts its position in sel[r].  Two equal keys below the f-th get the same
+// rank, so some slot is claimed twice; then the ranks are taken again with the
+// position as tie-break.  The output slot of sel[r] is the number of picks at
+// smaller positions.  The group is `nthr` threads (this one is number t).
+template <typename Grp>
+__device__ __forceinline__ void pick_emit(const HopArgs& a, uint32_t* tab, const Pool& p, int n, int64_t start,
+                                          int64_t out0, int t, int nthr, const Grp& grp) {
     const int f = a.fanout;
-    const int shift = (int)(lane_id() & ~(unsigned)(W - 1));  // first lane of the group
-    const unsigned ltg = (1u << gl) - 1u;
+    const int n4 = (n + 3) & ~3;
+    for (int i = n + t; i < n4; i += nthr) p.keys[i] = 0xFFFFFFFFu;  // never below a real key
+    for (int i = t; i < f; i += nthr) p.sel[i] = 0xFFFFFFFFu;        // no position is this large
+    grp.sync();
+    const uint4* k4 = reinterpret_cast<const uint4*>(p.keys);
+    bool tie = false;
+    for (int i = t; i < n; i += nthr) {
+        const uint32_t x = p.keys[i];
+        int rank = 0;
+#pragma unroll 2
+        for (int s = 0; s < (n4 >> 2); ++s) {
+            const uint4 k = k4[s];
+            rank += (k.x < x) + (k.y < x) + (k.z < x) + (k.w < x);
+        }
+        if (rank < f && atomicExch(&p.sel[rank], p.pos[i]) != 0xFFFFFFFFu) tie = true;
+    }
+    grp.sync();
+    if (grp.any(tie)) {  // equal keys: rank by (key, position)
+        for (int i = t; i < n; i += nthr) {
+            const uint32_t x = p.keys[i], j = p.pos[i];
+            int rank = 0;
+            for (int s = 0; s < n; ++s) rank += (p.keys[s] < x) || (p.keys[s] == x && p.pos[s] < j);
+            if (rank < f) p.sel[rank] = j;
+        }
+        grp.sync();
+    }
+    for (int r = t; r < f; r += nthr) {
+        const uint32_t j = p.sel[r];
+        int slot = 0;
+        for (int q = 0; q < f; ++q) slot += p.sel[q] < j;
+        emit_edge(a, tab, out0 + slot, a.indices[start + j]);
+    }
+    grp.sync();
+}
+
+// One random row by a group of W lanes (W = 8 or 32) named by `mask`: keys at
+// most tau become candidates (about lambda of them), and the f smallest are
+// emitted.  With fewer than f candidates tau widens (twice at most); when the
+// pool overflows or two widenings do not suffice, the exact path runs.
+template <int W>
+__device__ void sample_random_row(const HopArgs& a, uint32_t* tab, uint32_t k0, uint32_t k1, int32_t v, int64_t start,
+                                  uint32_t deg, int64_t out0, const Pool& p, unsigned mask, int gl) {
+    const int f = a.fanout;
+    const LaneGroup grp{mask};
     uint32_t tau = threshold_for(a.lambda_num, deg);
     for (int attempt = 0; attempt < 3; ++attempt) {
-        int n = 0;
-        bool overflow = false;
-        // each step covers 4*U*W positions: counter blocks q + u*W (u < U) of
-        // every lane, hashed as U independent chains; appending is skipped
-        // unless some key of the step passes the threshold
-        constexpr int U = 2;
-        for (int64_t base = 0; base < deg && !overflow; base += 4 * U * W) {
-            uint4 wq[U];
-            uint32_t mn = 0xFFFFFFFFu;
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t q = (base >> 2) + u * W + gl;
-                wq[u] = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty);
-                if (4 * q < deg) wq[u] = philox4x32_10(make_uint4((uint32_t)q, (uint32_t)v, (uint32_t)a.h, 0u), k0, k1);
-                mn = min(mn, min(min(wq[u].x, wq[u].y), min(wq[u].z, wq[u].w)));
-            }
-            // lanes past the row end hold kEmpty keys; a real key equal to
-            // kEmpty passes only when tau = kEmpty, and then the row is short
-            if (!__any_sync(mask, mn <= tau)) continue;
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const uint4 w = wq[u];
-                const int64_t j0 = 4 * ((base >> 2) + u * W + gl);
-                const bool p0 = j0 + 0 < deg && w.x <= tau;
-                const bool p1 = j0 + 1 < deg && w.y <= tau;
-                const bool p2 = j0 + 2 < deg && w.z <= tau;
-                const bool p3 = j0 + 3 < deg && w.w <= tau;
-                const unsigned m0 = __ballot_sync(mask, p0) >> shift, m1 = __ballot_sync(mask, p1) >> shift;
-                const unsigned m2 = __ballot_sync(mask, p2) >> shift, m3 = __ballot_sync(mask, p3) >> shift;
-                const int before = __popc(m0 & ltg) + __popc(m1 & ltg) + __popc(m2 & ltg) + __popc(m3 & ltg);
-                const int tot = __popc(m0) + __popc(m1) + __popc(m2) + __popc(m3);
-                if (n + tot > CAP) {
-                    overflow = true;
-                    break;
-                }
-                int p = n + before;  // candidates stay in ascending position order
-                if (p0) { cr[p] = w.x; cj[p] = (int32_t)(j0 + 0); ++p; }
-                if (p1) { cr[p] = w.y; cj[p] = (int32_t)(j0 + 1); ++p; }
-                if (p2) { cr[p] = w.z; cj[p] = (int32_t)(j0 + 2); ++p; }
-                if (p3) { cr[p] = w.w; cj[p] = (int32_t)(j0 + 3); ++p; }
-                n += tot;
-            }
-        }
+        if (gl == 0) *p.n = 0;
         __syncwarp(mask);
-        if (overflow) break;
-        if (n < f) {  // too few under the threshold: widen it and retry
-            tau = tau > 0x3FFFFFFFu ? 0xFFFFFFFFu : (tau << 2) | 3u;
-            __syncwarp(mask);
+        hash_row(a, k0, k1, v, deg, tau, p, (uint32_t)gl, W);
+        __syncwarp(mask);
+        const int n = *p.n;
+        __syncwarp(mask);
+        if (n > p.cap) break;
+        if (n < f) {
+            tau = widen(tau);
             continue;
         }
-        int sel_before = 0;
-        for (int c0 = 0; c0 < n; c0 += W) {
-            const int ci = c0 + gl;
-            bool sel = false;
-            if (ci < n) {
-                const uint32_t ri = cr[ci];
-                int rank = 0;
-#pragma unroll 4
-                for (int t = 0; t < n; ++t) {
-                    const uint32_t rt = cr[t];
-                    rank += (rt < ri) || (rt == ri && t < ci);
-                }
-                sel = rank < f;
-            }
-            const unsigned m = __ballot_sync(mask, sel) >> shift;
-            if (sel) emit_edge(a, tab, out0 + sel_before + __popc(m & ltg), a.indices[start + cj[ci]]);
-            sel_before += __popc(m);
-        }
-        __syncwarp(mask);
+        pick_emit(a, tab, p, n, start, out0, gl, W, grp);
         return;
     }
-    sample_exact<W>(a, tab, k0, k1, v, start, deg, out0, cj, mask, gl);
+    sample_exact<W>(a, tab, k0, k1, v, start, deg, out0, (int32_t*)p.sel, mask, gl);
 }
 
 // Row r of the frontier, by a group of W lanes.
-template <int W, int CAP>
-__device__ void sample_row(const HopArgs& a, int32_t r, const int32_t* pre, uint32_t k0, uint32_t k1, uint32_t* cr,
-                           int32_t* cj, unsigned mask, int gl) {
+template <int W>
+__device__ void sample_row(const HopArgs& a, int32_t r, const int32_t* pre, uint32_t k0, uint32_t k1, const Pool& p,
+                           unsigned mask, int gl) {
     const int4 m = a.rmeta[r];
     const int32_t v = m.w;
     const int64_t deg = m.z;
@@ -505,16 +559,87 @@ __device__ void sample_row(const HopArgs& a, int32_t r, const int32_t* pre, uint
         for (int64_t t = gl; t < deg; t += W) emit_edge(a, tab, out0 + t, a.indices[start + t]);
         return;
     }
-    sample_random_row<W, CAP>(a, tab, k0, k1, v, start, deg, out0, cr, cj, mask, gl);
+    sample_random_row<W>(a, tab, k0, k1, v, start, (uint32_t)deg, out0, p, mask, gl);
 }
 
-// A random row longer than 4096 by the whole block: each thread hashes one
-// counter block (4 positions) per step, candidates gather in shared memory
-// (order across warps is arbitrary, so the pick ranks by (key, position) and
-// the output is ordered by position afterwards).
-__device__ void sample_big_row(const HopArgs& a, int32_t r, const int32_t* pre, uint32_t k0, uint32_t k1, uint32_t* cr,
-                               int32_t* cj, int32_t* s_n, int32_t* s_over) {
-    constexpr int CAPB = 2048;  // candidates; cr[CAPB..2*CAPB) holds the pick flags
+// Four short random rows at once, one per 8-lane group of the warp (the steps
+// of sample_random_row).  Every loop runs to the warp-wide maximum trip count
+// with per-group predicates, so the groups stay converged: diverged groups
+// would take turns.  A group whose pool overflows, keeps fewer than f keys or
+// holds equal keys finishes alone (rare).
+__device__ void sample_rows_x4(const HopArgs& a, int32_t r, bool valid, const int32_t* pre, uint32_t k0, uint32_t k1,
+                               const Pool& p, unsigned gmask, int gl) {
+    const int f = a.fanout;
+    int32_t v = 0;
+    uint32_t deg = 0;
+    int64_t start = 0, out0 = 0;
+    uint32_t* tab = a.pos_of;
+    if (valid) {
+        const int4 m = a.rmeta[r];
+        v = m.w;
+        deg = (uint32_t)m.z;
+        valid = v >= 0 && (int64_t)v < a.n_nodes && (int64_t)deg > f;
+        if (valid && a.utab && (a.rslot[r] < 0 || (int32_t)a.utab[a.rslot[r]].y != r)) valid = false;
+        start = (int64_t)(uint32_t)m.x | ((int64_t)m.y << 32);
+        out0 = a.bindptr[r];
+        tab = a.pos_of + (int64_t)(a.K == 1 ? 0 : find_sub(pre, a.K, r)) * a.n_nodes;
+    }
+    const uint32_t tau = valid ? threshold_for(a.lambda_num, deg) : 0u;
+    const uint32_t qn = valid ? (deg + 3u) >> 2 : 0u;
+    const uint32_t max_steps = __reduce_max_sync(0xffffffffu, (qn + 15u) >> 4);
+    if (gl == 0) *p.n = 0;
+    __syncwarp();
+    for (uint32_t st = 0; st < max_steps; ++st) {
+        const uint32_t qa = st * 16u + (uint32_t)gl, qc = qa + 8u;
+        const uint4 wa = philox4x32_10(make_uint4(qa, (uint32_t)v, (uint32_t)a.h, 0u), k0, k1);
+        const uint4 wc = philox4x32_10(make_uint4(qc, (uint32_t)v, (uint32_t)a.h, 0u), k0, k1);
+        if (qa < qn) filter_block(wa, qa, deg, tau, p);
+        if (qc < qn) filter_block(wc, qc, deg, tau, p);
+    }
+    __syncwarp();
+    const int n = *p.n;
+    bool ok = valid && n >= f && n <= p.cap;
+    const int n_max = (int)__reduce_max_sync(0xffffffffu, ok ? (unsigned)n : 0u);
+    const int n4 = (n_max + 3) & ~3;  // the same padded length for every group
+    if (ok) {
+        for (int i = n + gl; i < n4; i += 8) p.keys[i] = 0xFFFFFFFFu;
+        for (int i = gl; i < f; i += 8) p.sel[i] = 0xFFFFFFFFu;
+    }
+    __syncwarp();
+    const uint4* k4 = reinterpret_cast<const uint4*>(p.keys);
+    bool tie = false;
+    for (int i0 = 0; i0 < n_max; i0 += 8) {
+        const int i = i0 + gl;
+        const bool in = ok && i < n;
+        const uint32_t x = in ? p.keys[i] : 0u;
+        int rank = 0;
+#pragma unroll 2
+        for (int s = 0; s < (n4 >> 2); ++s) {
+            const uint4 k = k4[s];
+            rank += (k.x < x) + (k.y < x) + (k.z < x) + (k.w < x);
+        }
+        if (in && rank < f && atomicExch(&p.sel[rank], p.pos[i]) != 0xFFFFFFFFu) tie = true;
+    }
+    __syncwarp();
+    if (ok && __any_sync(gmask, tie)) ok = false;  // equal keys: this group takes the general path
+    for (int r0 = 0; r0 < f; r0 += 8) {
+        const int rr = r0 + gl;
+        if (ok && rr < f) {
+            const uint32_t j = p.sel[rr];
+            int slot = 0;
+            for (int q = 0; q < f; ++q) slot += p.sel[q] < j;
+            emit_edge(a, tab, out0 + slot, a.indices[start + j]);
+        }
+    }
+    __syncwarp();
+    if (valid && !ok) sample_random_row<8>(a, tab, k0, k1, v, start, deg, out0, p, gmask, gl);
+    __syncwarp();
+}
+
+// A random row longer than 4096 by the whole block (the same steps as
+// sample_random_row, with 256 threads and the block's pool).
+__device__ void sample_big_row(const HopArgs& a, int32_t r, const int32_t* pre, uint32_t k0, uint32_t k1,
+                               const Pool& p) {
     const int4 m = a.rmeta[r];
     const int32_t v = m.w;
     const int64_t deg = m.z;
@@ -524,177 +649,38 @@ __device__ void sample_big_row(const HopArgs& a, int32_t r, const int32_t* pre, 
     const int64_t out0 = a.bindptr[r];
     uint32_t* tab = a.pos_of + (int64_t)(a.K == 1 ? 0 : find_sub(pre, a.K, r)) * a.n_nodes;
     const int f = a.fanout;
-    const unsigned lane = lane_id();
     uint32_t tau = threshold_for(a.lambda_num, deg);
+    const BlockGroup grp;
     for (int attempt = 0; attempt < 3; ++attempt) {
-        if (threadIdx.x == 0) {
-            *s_n = 0;
-            *s_over = 0;
-        }
+        if (threadIdx.x == 0) *p.n = 0;
         __syncthreads();
-        for (int64_t base = 0; base < deg; base += 8 * kNT) {
-          const int64_t qa = (base >> 2) + threadIdx.x, qb = qa + kNT;
-          uint4 wab[2];
-          wab[0] = wab[1] = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty);
-          if (4 * qa < deg) wab[0] = philox4x32_10(make_uint4((uint32_t)qa, (uint32_t)v, (uint32_t)a.h, 0u), k0, k1);
-          if (4 * qb < deg) wab[1] = philox4x32_10(make_uint4((uint32_t)qb, (uint32_t)v, (uint32_t)a.h, 0u), k0, k1);
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const uint4 w = wab[half];
-            const int64_t q = half ? qb : qa;
-            const uint32_t mn = min(min(w.x, w.y), min(w.z, w.w));
-            if (!__any_sync(0xffffffffu, mn <= tau)) continue;
-            const int64_t j0 = 4 * q;
-            const bool p0 = j0 + 0 < deg && w.x <= tau;
-            const bool p1 = j0 + 1 < deg && w.y <= tau;
-            const bool p2 = j0 + 2 < deg && w.z <= tau;
-            const bool p3 = j0 + 3 < deg && w.w <= tau;
-            const unsigned m0 = __ballot_sync(0xffffffffu, p0), m1 = __ballot_sync(0xffffffffu, p1);
-            const unsigned m2 = __ballot_sync(0xffffffffu, p2), m3 = __ballot_sync(0xffffffffu, p3);
-            const unsigned lt = lanemask_lt();
-            const int before = __popc(m0 & lt) + __popc(m1 & lt) + __popc(m2 & lt) + __popc(m3 & lt);
-            const int tot = __popc(m0) + __popc(m1) + __popc(m2) + __popc(m3);
-            if (tot == 0) continue;
-            int wbase = 0;
-            if (lane == 0) wbase = atomicAdd(s_n, tot);
-            wbase = __shfl_sync(0xffffffffu, wbase, 0);
-            if (wbase + tot > CAPB) {
-                if (lane == 0) *s_over = 1;
-                continue;
-            }
-            int p = wbase + before;
-            if (p0) { cr[p] = w.x; cj[p] = (int32_t)(j0 + 0); ++p; }
-            if (p1) { cr[p] = w.y; cj[p] = (int32_t)(j0 + 1); ++p; }
-            if (p2) { cr[p] = w.z; cj[p] = (int32_t)(j0 + 2); ++p; }
-            if (p3) { cr[p] = w.w; cj[p] = (int32_t)(j0 + 3); ++p; }
-          }
-        }
+        hash_row(a, k0, k1, v, (uint32_t)deg, tau, p, threadIdx.x, kNT);
         __syncthreads();
-        const int n = *s_n;
-        const bool over = *s_over != 0;
+        const int n = *p.n;
         __syncthreads();
-        if (over) break;
-        if (n < f) {  // too few under the threshold: widen it and retry
-            tau = tau > 0x3FFFFFFFu ? 0xFFFFFFFFu : (tau << 2) | 3u;
+        if (n > p.cap) break;
+        if (n < f) {
+            tau = widen(tau);
             continue;
         }
-        uint32_t* picked = cr + CAPB;
-        for (int i = threadIdx.x; i < n; i += kNT) {  // rank by (key, position)
-            const uint32_t ri = cr[i];
-            const int32_t ji = cj[i];
-            int rank = 0;
-            for (int t = 0; t < n; ++t) rank += cr[t] < ri || (cr[t] == ri && cj[t] < ji);
-            picked[i] = rank < f;
-        }
-        __syncthreads();
-        for (int i = threadIdx.x; i < n; i += kNT) {  // the picks, by position
-            if (!picked[i]) continue;
-            const int32_t ji = cj[i];
-            int pos = 0;
-            for (int t = 0; t < n; ++t) pos += picked[t] && cj[t] < ji;
-            emit_edge(a, tab, out0 + pos, a.indices[start + ji]);
-        }
-        __syncthreads();
+        pick_emit(a, tab, p, n, start, out0, (int)threadIdx.x, kNT, grp);
         return;
     }
-    if (threadIdx.x < 32) sample_exact<32>(a, tab, k0, k1, v, start, deg, out0, cj, 0xffffffffu, (int)lane);
+    if (threadIdx.x < 32) sample_exact<32>(a, tab, k0, k1, v, start, deg, out0, (int32_t*)p.sel, 0xffffffffu, (int)lane_id());
     __syncthreads();
 }
 
-// Four short random rows at once, one per 8-lane group of the warp, in
-// lockstep: every loop runs to the warp-wide maximum trip count with per-group
-// predicates, and ballots name the whole warp, so the groups never diverge.
-// A group whose filter overflows or keeps fewer than f keys finishes alone on
-// the per-group path (rare).
-__device__ void sample_rows_x4(const HopArgs& a, int32_t r, bool valid, const int32_t* pre, uint32_t k0, uint32_t k1,
-                               uint32_t* cr, int32_t* cj) {
-    constexpr int G = 8, CAP = kGroupCap;
-    const unsigned lane = lane_id();
-    const int g = (int)(lane >> 3), gl = (int)(lane & 7), shift = 8 * g;
-    const unsigned gmask = 0xFFu << shift, ltg = (1u << gl) - 1u;
-    const int f = a.fanout;
-    int32_t v = 0;
-    int64_t deg = 0, start = 0, out0 = 0;
-    uint32_t* tab = a.pos_of;
-    if (valid) {
-        const int4 m = a.rmeta[r];
-        v = m.w;
-        deg = m.z;
-        valid = v >= 0 && (int64_t)v < a.n_nodes && deg > f;
-        if (valid && a.utab && (a.rslot[r] < 0 || (int32_t)a.utab[a.rslot[r]].y != r)) valid = false;
-        start = (int64_t)(uint32_t)m.x | ((int64_t)m.y << 32);
-        out0 = a.bindptr[r];
-        tab = a.pos_of + (int64_t)(a.K == 1 ? 0 : find_sub(pre, a.K, r)) * a.n_nodes;
-    }
-    const uint32_t tau = valid ? threshold_for(a.lambda_num, deg) : 0u;
-    const int steps = valid ? (int)((deg + 8 * G - 1) / (8 * G)) : 0;
-    const int max_steps = __reduce_max_sync(0xffffffffu, (unsigned)steps);
-    int n = 0;
-    bool over = false;
-    for (int step = 0; step < max_steps; ++step) {
-        const bool act = step < steps && !over;
-        const int64_t qa = (int64_t)step * 2 * G + gl, qb = qa + G;
-        uint4 wa = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty), wb = wa;
-        if (act && 4 * qa < deg) wa = philox4x32_10(make_uint4((uint32_t)qa, (uint32_t)v, (uint32_t)a.h, 0u), k0, k1);
-        if (act && 4 * qb < deg) wb = philox4x32_10(make_uint4((uint32_t)qb, (uint32_t)v, (uint32_t)a.h, 0u), k0, k1);
-        const uint32_t lo = min(min(wa.x, wa.y), min(wa.z, wa.w)), hi = min(min(wb.x, wb.y), min(wb.z, wb.w));
-        if (!__any_sync(0xffffffffu, act && (lo <= tau || hi <= tau))) continue;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const uint4 w = half ? wb : wa;
-            const int64_t j0 = 4 * (half ? qb : qa);
-            const bool p0 = act && j0 + 0 < deg && w.x <= tau;
-            const bool p1 = act && j0 + 1 < deg && w.y <= tau;
-            const bool p2 = act && j0 + 2 < deg && w.z <= tau;
-            const bool p3 = act && j0 + 3 < deg && w.w <= tau;
-            const unsigned m0 = (__ballot_sync(0xffffffffu, p0) & gmask) >> shift;
-            const unsigned m1 = (__ballot_sync(0xffffffffu, p1) & gmask) >> shift;
-            const unsigned m2 = (__ballot_sync(0xffffffffu, p2) & gmask) >> shift;
-            const unsigned m3 = (__ballot_sync(0xffffffffu, p3) & gmask) >> shift;
-            const int before = __popc(m0 & ltg) + __popc(m1 & ltg) + __popc(m2 & ltg) + __popc(m3 & ltg);
-            const int tot = __popc(m0) + __popc(m1) + __popc(m2) + __popc(m3);
-            if (act && n + tot > CAP) over = true;
-            if (act && !over) {
-                int p = n + before;  // candidates stay in ascending position order
-                if (p0) { cr[p] = w.x; cj[p] = (int32_t)(j0 + 0); ++p; }
-                if (p1) { cr[p] = w.y; cj[p] = (int32_t)(j0 + 1); ++p; }
-                if (p2) { cr[p] = w.z; cj[p] = (int32_t)(j0 + 2); ++p; }
-                if (p3) { cr[p] = w.w; cj[p] = (int32_t)(j0 + 3); ++p; }
-                n += tot;
-            }
-        }
-    }
-    __syncwarp();
-    const bool ok = valid && !over && n >= f;
-    // exact pick among the candidates, all groups together
-    const int n_max = __reduce_max_sync(0xffffffffu, ok ? (unsigned)n : 0u);
-    int sel_before = 0;
-    for (int c0 = 0; c0 < n_max; c0 += G) {
-        const int ci = c0 + gl;
-        const bool in = ok && ci < n;
-        const uint32_t ri = in ? cr[ci] : 0u;
-        int rank = 0;
-#pragma unroll 4
-        for (int t = 0; t < n_max; ++t) {
-            const uint32_t rt = cr[t < CAP ? t : 0];
-            rank += (t < n) && ((rt < ri) || (rt == ri && t < ci));
-        }
-        const bool sel = in && rank < f;
-        const unsigned m = (__ballot_sync(0xffffffffu, sel) & gmask) >> shift;
-        if (sel) emit_edge(a, tab, out0 + sel_before + __popc(m & ltg), a.indices[start + cj[ci]]);
-        sel_before += __popc(m);
-    }
-    __syncwarp();
-    // groups that need a retry or the exact pick finish on their own
-    if (valid && !ok) sample_random_row<G, CAP>(a, tab, k0, k1, v, start, deg, out0, cr, cj, gmask, gl);
-    __syncwarp();
-}
-
+// Rows by bin, largest first, handed out by counters so that no SM is left
+// with a long tail: blocks take the rows of bin 3 one at a time, then warps
+// take units (a bin 2 row; four bin 1 rows, one per 8-lane group; or sixteen
+// full rows).  The grid is at most what fits on the GPU at once.
 __global__ void __launch_bounds__(kNT) k_sample(HopArgs a) {
     __shared__ int32_t pre[SG_MAX_SUB + 1];
-    __shared__ uint32_t cand_r[kNT / 32][2 * kWarpCap];
-    __shared__ int32_t cand_j[kNT / 32][2 * kWarpCap];
-    __shared__ int32_t s_n, s_over;
+    __shared__ __align__(16) uint32_t s_key[kBlockPool];
+    __shared__ uint32_t s_pos[kBlockPool];
+    __shared__ uint32_t s_sel[kWarpSel * (kNT / 32)];
+    __shared__ int s_n[kNT / 8];
+    __shared__ int s_item;
     load_prefix_sub_n(a.counts, a.L, a.K, a.h - 1, pre);
     uint32_t k0 = a.key0, k1 = a.key1;
     if (a.d_seed) {
@@ -702,49 +688,45 @@ __global__ void __launch_bounds__(kNT) k_sample(HopArgs a) {
         k0 = (uint32_t)(sd & 0xFFFFFFFFull);
         k1 = (uint32_t)(sd >> 32);
     }
-    // the counters start at all-ones (the memset), so a count is the word + 1
+    // the counters start at all-ones, so a count is the word + 1
     const int64_t n0 = (uint32_t)(a.ctr[2] + 1u), n1 = (uint32_t)(a.ctr[3] + 1u), n2 = (uint32_t)(a.ctr[4] + 1u),
                   n3 = (uint32_t)(a.ctr[5] + 1u);
-    // rows of bin 3 first, a block each
-    for (int64_t i = blockIdx.x; i < n3; i += gridDim.x)
-        sample_big_row(a, a.bins[3 * a.bin_stride + i], pre, k0, k1, &cand_r[0][0], &cand_j[0][0], &s_n, &s_over);
-    // then work units: one per row of bin 2 (a warp each), one per four rows
-    // of bins 1 and 0 (an 8-lane group each)
-    const int64_t u32 = n2;
-    const int64_t u8a = (n1 + 3) / 4, u8b = (n0 + 3) / 4;
-    const int64_t units = u32 + u8a + u8b;
+    const Pool bpool{s_key, s_pos, s_sel, &s_n[0], kBlockPool};
+    for (;;) {
+        if (threadIdx.x == 0) s_item = (int)(atomicAdd(a.ctr + 6, 1u) + 1u);
+        __syncthreads();
+        const int64_t i = s_item;
+        __syncthreads();
+        if (i >= n3) break;
+        sample_big_row(a, a.bins[3 * a.bin_stride + i], pre, k0, k1, bpool);
+    }
+    const int64_t u2 = n2, u1 = (n1 + 3) / 4, u0 = (n0 + 15) / 16;
+    const int64_t units = u2 + u1 + u0;
     const unsigned lane = lane_id();
     const int wib = threadIdx.x >> 5;
-    uint32_t* cr = cand_r[wib];
-    int32_t* cj = cand_j[wib];
-    const int64_t nwarps = (int64_t)gridDim.x * (kNT / 32);
-    for (int64_t u = blockIdx.x * (int64_t)(kNT / 32) + wib; u < units; u += nwarps) {
-        if (u < u32) {
-            const int32_t r = a.bins[2 * a.bin_stride + u];
-            sample_row<32, kWarpCap>(a, r, pre, k0, k1, cr, cj, 0xffffffffu, (int)lane);
+    const int g = (int)(lane >> 3), gl = (int)(lane & 7);
+    const unsigned gmask = 0xFFu << (8 * g);
+    const Pool wpool{s_key + wib * kWarpPool, s_pos + wib * kWarpPool, s_sel + wib * kWarpSel, &s_n[4 * wib], kWarpPool};
+    const Pool gpool{s_key + wib * kWarpPool + g * kGroupPool, s_pos + wib * kWarpPool + g * kGroupPool,
+                     s_sel + wib * kWarpSel + g * kGroupSel, &s_n[4 * wib + g], kGroupPool};
+    uint32_t nxt = 0;
+    if (lane == 0) nxt = atomicAdd(a.ctr + 7, 1u) + 1u;
+    int64_t u = __shfl_sync(0xffffffffu, nxt, 0);
+    while (u < units) {
+        if (lane == 0) nxt = atomicAdd(a.ctr + 7, 1u) + 1u;  // the next unit, fetched ahead
+        if (u < u2) {
+            sample_row<32>(a, a.bins[2 * a.bin_stride + u], pre, k0, k1, wpool, 0xffffffffu, (int)lane);
+        } else if (u < u2 + u1) {
+            const int64_t i = (u - u2) * 4 + g;
+            sample_rows_x4(a, i < n1 ? a.bins[a.bin_stride + i] : 0, i < n1, pre, k0, k1, gpool, gmask, gl);
         } else {
-            const int g = (int)(lane >> 3), gl = (int)(lane & 7);
-            const unsigned gmask = 0xFFu << (8 * g);
-            int64_t i, n;
-            int bin;
-            if (u < u32 + u8a) {
-                i = (u - u32) * 4 + g;
-                bin = 1;
-                n = n1;
-            } else {
-                i = (u - u32 - u8a) * 4 + g;
-                bin = 0;
-                n = n0;
-            }
-            if (bin == 1) {
-                const int32_t r = i < n ? a.bins[bin * a.bin_stride + i] : 0;
-                sample_rows_x4(a, r, i < n, pre, k0, k1, cr + g * kGroupCap, cj + g * kGroupCap);
-            } else if (i < n) {
-                const int32_t r = a.bins[bin * a.bin_stride + i];
-                sample_row<8, kGroupCap>(a, r, pre, k0, k1, cr + g * kGroupCap, cj + g * kGroupCap, gmask, gl);
+            for (int t = 0; t < 4; ++t) {
+                const int64_t i = (u - u2 - u1) * 16 + 4 * t + g;
+                if (i < n0) sample_row<8>(a, a.bins[i], pre, k0, k1, gpool, gmask, gl);
             }
         }
         __syncwarp();
+        u = __shfl_sync(0xffffffffu, nxt, 0);
     }
 }
 
@@ -958,6 +940,7 @@ sg_status make_plan(const sg_graph* g, int32_t n_seeds, const int32_t* h_bptr, i
         p->fan[h] = h_fan[h];
     }
     const int64_t N = g->n_nodes, maxdeg = g->max_degree;
+    if (maxdeg > 2147483647LL) return fail(SG_ERR_UNSUPPORTED, "sampler: rows longer than 2^31 - 1 entries");
     for (int h = 0; h <= n_hops; ++h) p->nb_tot[h] = 0;
     for (int h = 0; h < n_hops; ++h) p->eb_tot[h] = 0;
     p->capU = 1;
@@ -1024,6 +1007,18 @@ uint32_t lambda_for(int f) {
     // (fewer than f pass, about 1% of rows) cheap and the candidate set small
     double lam = f + 2.0 * __builtin_sqrt((double)f) + 4.0;
     return (uint32_t)lam;
+}
+
+// Blocks of k_sample that fit on the GPU at once (its grid hands out work by
+// counters, so more blocks would only wait).
+int64_t resident_sample_blocks(int sms) {
+    static int per_sm = 0;
+    if (per_sm == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_sample, kNT, 0) != cudaSuccess || n < 1) n = 1;
+        per_sm = n;
+    }
+    return (int64_t)per_sm * sms;
 }
 
 int64_t clamp_blocks(int64_t want, int64_t cap) {
@@ -1107,6 +1102,7 @@ extern "C" sg_status sg_sampler_run(const sg_graph* g, const int32_t* d_seeds, i
     SubPtr bp;
     for (int k = 0; k <= K; ++k) bp.v[k] = p.bptr[k];
     const int64_t cap_blocks = (int64_t)sms * 8;
+    const int64_t sample_blocks = resident_sample_blocks(sms);
     for (int h = 1; h <= H; ++h) {
         const int cur = (h - 1) & 1, prv = h & 1;
         a.h = h;
@@ -1133,7 +1129,7 @@ extern "C" sg_status sg_sampler_run(const sg_graph* g, const int32_t* d_seeds, i
         else
             k_rows<int64_t><<<(unsigned)(a.map_blocks + row_blocks), kNT, 0, s>>>(a, seed_mode, d_seeds, bp);
         SG_CHECK_LAUNCH("k_rows");
-        k_sample<<<(unsigned)clamp_blocks(cdiv(nb, kNT / 32), cap_blocks), kNT, 0, s>>>(a);
+        k_sample<<<(unsigned)clamp_blocks(cdiv(nb, kNT / 32), sample_blocks), kNT, 0, s>>>(a);
         SG_CHECK_LAUNCH("k_sample");
         if (K > 1) {
             k_copy<<<(unsigned)clamp_blocks(cdiv(nb, kNT / 32), cap_blocks), kNT, 0, s>>>(a);

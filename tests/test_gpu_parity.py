@@ -4,6 +4,8 @@ Bit-exact for sampled blocks, relabel maps and gathered rows; aggregation
 within the fp tolerance |gpu - oracle| <= tol * (mean |term| + 1e-30) per
 element, tol = 1e-5 for fp32 and 1e-2 for bf16 inputs (fp32 accumulation).
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -230,6 +232,25 @@ def test_sampler_hub_rows_and_fanout_limits(fanout):
     for seed in (0, 99, 2 ** 40 + 17):
         gpu = GpuSample(G, seeds, [fanout, 2], seed)
         assert_blocks_equal(gpu, oracle.sampler_run(indptr, indices, seeds, [fanout, 2], seed))
+
+
+def test_sampler_key_ties_take_the_lower_position():
+    # rows in which two positions share a Philox key, with the fanout set so
+    # that only one of the two is taken (tests/golden/key_ties.txt): the
+    # 8-lane group, warp and block paths must all keep the lower position
+    path = os.path.join(os.path.dirname(__file__), "golden", "key_ties.txt")
+    seed = int(open(path).read().split("Seed ")[1].split(",")[0], 16)
+    rows = [l.split() for l in open(path) if l.strip() and not l.startswith("#")]
+    for r in rows:
+        v, deg, f = int(r[0]), int(r[1]), int(r[2])
+        n = max(v + 1, deg + 1)
+        indptr = np.zeros(n + 1, np.int64)
+        indptr[v + 1:] = deg
+        indices = np.array([u if u < v else u + 1 for u in range(deg)], np.int32)  # no self-loop
+        G = sg.sg_graph_load(indptr, indices)
+        for fanouts in ([f], [f, 3]):
+            gpu = GpuSample(G, [v], fanouts, seed)
+            assert_blocks_equal(gpu, oracle.sampler_run(indptr, indices, [v], fanouts, seed))
 
 
 def test_sampler_empty_and_isolated():

@@ -327,3 +327,30 @@ def test_bf16_decode_exact():
     bits = np.array([0x3F80, 0xBF80, 0x4049, 0x0000, 0x8000, 0x7F80], np.uint16)
     assert oracle.bf16_to_f32(bits).tolist()[:5] == [1.0, -1.0, 3.140625, 0.0, -0.0]
     assert np.isinf(oracle.bf16_to_f32(bits)[5])
+
+
+# ------------------------------------------------------------- key ties
+def _key_ties():
+    rows = _read_rows("key_ties.txt")
+    with open(os.path.join(GOLDEN, "key_ties.txt")) as fh:
+        seed = int(fh.read().split("Seed ")[1].split(",")[0], 16)
+    return seed, [[int(r[0]), int(r[1]), int(r[2]), int(r[3]), int(r[4]), int(r[5], 16), int(r[6])] for r in rows]
+
+
+def test_key_tie_rows_pin_the_position_tie_break():
+    # Rows whose two positions share a Philox key (found by make_key_ties.py):
+    # the oracle's own key function gives them the same key, with `rank`
+    # smaller keys in the row, and the sample of fanout rank + 1 keeps the
+    # lower position only (reading: ties in the key go to the lower position).
+    seed, rows = _key_ties()
+    assert len(rows) >= 3
+    for v, deg, f, j_lo, j_hi, key, rank in rows:
+        assert j_lo < j_hi
+        keys = np.array([oracle.sample_key(seed, 1, v, j) for j in range(deg)], np.uint64)
+        assert keys[j_lo] == key and keys[j_hi] == key
+        assert int((keys < key).sum()) == rank and f == rank + 1
+        indptr = np.zeros(v + 2, np.int64)
+        indptr[v + 1] = deg
+        got = oracle.sample_positions(indptr, v, f, 1, seed)
+        want = np.sort(np.concatenate([np.nonzero(keys < key)[0], [j_lo]]))
+        assert np.array_equal(got, want)
