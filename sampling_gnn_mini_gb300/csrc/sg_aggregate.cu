@@ -27,6 +27,7 @@ namespace {
 constexpr int kNT = 256;
 constexpr int kWarpSortCap = 256;   // longest segment a warp sorts in shared memory
 constexpr int kBlockSortCap = 4096; // longest segment a block sorts in shared memory
+constexpr int kLongRow = 16;        // SpMM rows longer than this are summed by a whole warp
 
 enum { DT_F32 = 0, DT_BF16 = 1, DT_BF16_F32 = 2 };  // input -> output types
 
@@ -95,9 +96,85 @@ __device__ __forceinline__ void store_vec(void* y, int64_t r, int32_t row_vecs, 
     }
 }
 
+// Adds to acc the edges of chunks lo + (first + k * stride) * LPR, k = 0, 1,
+// ..., of row [lo, hi) (a chunk is LPR consecutive edges), for the group of
+// LPR lanes named by gmask (this lane is gl): each lane holds VPL 16-byte
+// vectors of the row (vector gl + p * LPR) and keeps UE edges in flight.
+template <int LPR, int VPL, int DT, bool WEIGHTED>
+__device__ __forceinline__ void accumulate_chunks(float (&acc)[VPL][Elems<DT>::n], int32_t lo, int32_t hi, int first,
+                                                  int stride, const int32_t* __restrict__ col,
+                                                  const float* __restrict__ w, int32_t n_cols,
+                                                  const uint4* __restrict__ x, int32_t row_vecs, unsigned gmask,
+                                                  int gl) {
+    constexpr int UE = VPL >= 8 ? 1 : (VPL == 4 ? 2 : 4);  // edges in flight per lane
+    for (int32_t c0 = lo + first * LPR; c0 < hi; c0 += stride * LPR) {
+        const int32_t my_e = c0 + gl;
+        int32_t my_col = -1;
+        float my_w = 1.f;
+        if (my_e < hi) {
+            my_col = __ldg(col + my_e);
+            if (WEIGHTED) my_w = __ldg(w + my_e);
+        }
+        const int cnt = min(LPR, hi - c0);
+        for (int t0 = 0; t0 < cnt; t0 += UE) {
+            uint4 buf[UE][VPL];
+            float wt[UE];
+            bool ok[UE];
+#pragma unroll
+            for (int u = 0; u < UE; ++u) {
+                const int t = t0 + u;
+                const int32_t cu = __shfl_sync(gmask, my_col, t < cnt ? t : 0, LPR);
+                wt[u] = WEIGHTED ? __shfl_sync(gmask, my_w, t < cnt ? t : 0, LPR) : 1.f;
+                ok[u] = t < cnt && cu >= 0 && cu < n_cols;
+                if (t < cnt && !ok[u] && gl == 0) dev_err(ERR_INDEX);
+                const uint4* xr = x + (int64_t)(ok[u] ? cu : 0) * row_vecs;
+#pragma unroll
+                for (int p = 0; p < VPL; ++p) {
+                    const int vi = gl + p * LPR;
+                    buf[u][p] = (ok[u] && vi < row_vecs) ? __ldg(xr + vi) : make_uint4(0, 0, 0, 0);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < UE; ++u) {
+                if (!ok[u]) continue;
+#pragma unroll
+                for (int p = 0; p < VPL; ++p) {
+                    if (WEIGHTED) fma_vec<DT>(acc[p], buf[u][p], wt[u]);
+                    else add_vec<DT>(acc[p], buf[u][p]);
+                }
+            }
+        }
+    }
+}
+
+// Scales and stores output row r from the group's accumulators.
+template <int LPR, int VPL, int DT, bool WEIGHTED>
+__device__ __forceinline__ void store_row(const float (&acc)[VPL][Elems<DT>::n], int64_t r, int32_t c, void* y,
+                                          int32_t row_vecs, int gl) {
+    constexpr int EPV = Elems<DT>::n;
+#pragma unroll
+    for (int p = 0; p < VPL; ++p) {
+        const int vi = gl + p * LPR;
+        if (vi >= row_vecs) continue;
+        float o[EPV];
+#pragma unroll
+        for (int q = 0; q < EPV; ++q) {
+            if (WEIGHTED) o[q] = acc[p][q];
+            else o[q] = c > 0 ? __fdiv_rn(acc[p][q], (float)c) : 0.f;
+        }
+        store_vec<DT>(y, r, row_vecs, vi, o);
+    }
+}
+
 // y[r] = scale_r * sum_p w_p x[col[p]] for r < n_rows (see the file comment).
 // WEIGHTED = false: w_p = 1 and scale_r = 1 / row length (forward mean).
 // WEIGHTED = true:  w_p = w[p] and scale_r = 1 (backward over the transpose).
+// A warp holds 32 / LPR groups, and group g of the grid owns rows g, g +
+// groups, ...  Rows longer than kLongRow edges (hubs of a transposed block)
+// come first, each by the whole warp of its group: the warp's groups take
+// every (32 / LPR)-th chunk of the row, and their sums are added in a fixed
+// order, so a long row is no longer a serial tail.  Then every group sums its
+// other rows alone, in edge order.
 template <int LPR, int VPL, int DT, bool WEIGHTED>
 __global__ void __launch_bounds__(kNT) k_spmm(const int32_t* __restrict__ ptr, const int32_t* __restrict__ col,
                                               const float* __restrict__ w, int32_t n_rows_cap,
@@ -105,17 +182,49 @@ __global__ void __launch_bounds__(kNT) k_spmm(const int32_t* __restrict__ ptr, c
                                               const int32_t* __restrict__ d_cols, const uint4* __restrict__ x,
                                               int32_t row_vecs, void* __restrict__ y) {
     constexpr int EPV = Elems<DT>::n;
-    constexpr int UE = VPL >= 8 ? 1 : (VPL == 4 ? 2 : 4);  // edges in flight per lane
+    constexpr int SG = 32 / LPR;  // groups per warp
     const int64_t n_rows = d_rows ? (int64_t)min(*d_rows, n_rows_cap) : n_rows_cap;
     const int32_t n_cols = d_cols ? min(*d_cols, n_cols_cap) : n_cols_cap;
     const unsigned lane = lane_id();
-    const int gl = lane % LPR;
+    const int gl = lane % LPR, sg = (int)(lane / LPR);
     // the LPR lanes of a group share a row (and so every loop trip count);
     // shuffles name only them, so groups of one warp proceed independently
     const unsigned gmask = LPR == 32 ? 0xffffffffu : (((1u << LPR) - 1u) << (lane - gl));
     const int64_t groups = (int64_t)gridDim.x * (kNT / LPR);
-    int64_t r = (blockIdx.x * (int64_t)kNT + threadIdx.x) / LPR;
-    // the next row's bounds are loaded while the current row is summed
+    const int64_t gid = (blockIdx.x * (int64_t)kNT + threadIdx.x) / LPR;
+    if (SG > 1) {
+        // long rows of this warp's groups, one at a time, by the whole warp
+        for (int64_t base = gid - sg; base < n_rows; base += groups) {
+            const int64_t rr = base + sg;
+            int32_t lo = 0, hi = 0;
+            if (rr < n_rows) {
+                lo = ptr[rr];
+                hi = ptr[rr + 1];
+            }
+            unsigned longs = __ballot_sync(0xffffffffu, gl == 0 && hi - lo > kLongRow);
+            while (longs) {
+                const int src = __ffs(longs) - 1;
+                longs &= longs - 1;
+                const int32_t rlo = __shfl_sync(0xffffffffu, lo, src), rhi = __shfl_sync(0xffffffffu, hi, src);
+                float acc[VPL][EPV];
+#pragma unroll
+                for (int p = 0; p < VPL; ++p)
+#pragma unroll
+                    for (int q = 0; q < EPV; ++q) acc[p][q] = 0.f;
+                accumulate_chunks<LPR, VPL, DT, WEIGHTED>(acc, rlo, rhi, sg, SG, col, w, n_cols, x, row_vecs, gmask, gl);
+#pragma unroll
+                for (int d = LPR; d < 32; d <<= 1)
+#pragma unroll
+                    for (int p = 0; p < VPL; ++p)
+#pragma unroll
+                        for (int q = 0; q < EPV; ++q) acc[p][q] += __shfl_xor_sync(0xffffffffu, acc[p][q], d);
+                if (sg == 0) store_row<LPR, VPL, DT, WEIGHTED>(acc, base + src / LPR, rhi - rlo, y, row_vecs, gl);
+            }
+        }
+    }
+    // the other rows, a group each; the next row's bounds are loaded while
+    // the current row is summed
+    int64_t r = gid;
     int32_t nlo = 0, nhi = 0;
     if (r < n_rows) {
         nlo = ptr[r];
@@ -127,62 +236,14 @@ __global__ void __launch_bounds__(kNT) k_spmm(const int32_t* __restrict__ ptr, c
             nlo = ptr[r + groups];
             nhi = ptr[r + groups + 1];
         }
+        if (SG > 1 && hi - lo > kLongRow) continue;
         float acc[VPL][EPV];
 #pragma unroll
         for (int p = 0; p < VPL; ++p)
 #pragma unroll
             for (int q = 0; q < EPV; ++q) acc[p][q] = 0.f;
-        for (int32_t c0 = lo; c0 < hi; c0 += LPR) {
-            const int32_t my_e = c0 + gl;
-            int32_t my_col = -1;
-            float my_w = 1.f;
-            if (my_e < hi) {
-                my_col = __ldg(col + my_e);
-                if (WEIGHTED) my_w = __ldg(w + my_e);
-            }
-            const int cnt = min(LPR, hi - c0);
-            for (int t0 = 0; t0 < cnt; t0 += UE) {
-                uint4 buf[UE][VPL];
-                float wt[UE];
-                bool ok[UE];
-#pragma unroll
-                for (int u = 0; u < UE; ++u) {
-                    const int t = t0 + u;
-                    const int32_t cu = __shfl_sync(gmask, my_col, t < cnt ? t : 0, LPR);
-                    wt[u] = WEIGHTED ? __shfl_sync(gmask, my_w, t < cnt ? t : 0, LPR) : 1.f;
-                    ok[u] = t < cnt && cu >= 0 && cu < n_cols;
-                    if (t < cnt && !ok[u] && gl == 0) dev_err(ERR_INDEX);
-                    const uint4* xr = x + (int64_t)(ok[u] ? cu : 0) * row_vecs;
-#pragma unroll
-                    for (int p = 0; p < VPL; ++p) {
-                        const int vi = gl + p * LPR;
-                        buf[u][p] = (ok[u] && vi < row_vecs) ? __ldg(xr + vi) : make_uint4(0, 0, 0, 0);
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < UE; ++u) {
-                    if (!ok[u]) continue;
-#pragma unroll
-                    for (int p = 0; p < VPL; ++p) {
-                        if (WEIGHTED) fma_vec<DT>(acc[p], buf[u][p], wt[u]);
-                        else add_vec<DT>(acc[p], buf[u][p]);
-                    }
-                }
-            }
-        }
-        const int32_t c = hi - lo;
-#pragma unroll
-        for (int p = 0; p < VPL; ++p) {
-            const int vi = gl + p * LPR;
-            if (vi >= row_vecs) continue;
-            float o[EPV];
-#pragma unroll
-            for (int q = 0; q < EPV; ++q) {
-                if (WEIGHTED) o[q] = acc[p][q];
-                else o[q] = c > 0 ? __fdiv_rn(acc[p][q], (float)c) : 0.f;
-            }
-            store_vec<DT>(y, r, row_vecs, vi, o);
-        }
+        accumulate_chunks<LPR, VPL, DT, WEIGHTED>(acc, lo, hi, 0, 1, col, w, n_cols, x, row_vecs, gmask, gl);
+        store_row<LPR, VPL, DT, WEIGHTED>(acc, r, hi - lo, y, row_vecs, gl);
     }
 }
 

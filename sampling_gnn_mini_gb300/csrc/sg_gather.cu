@@ -8,7 +8,10 @@
 // of the output: output stores are fully coalesced and each source row is
 // read as a contiguous run, from the cache or from the host table.  Every
 // thread keeps kUnroll (8) independent 16-byte loads in flight before it
-// stores, which the latency of host-link reads needs.
+// stores, which the latency of host-link reads needs.  Source rows are read
+// with the streaming hint (each is used once here); the output is stored
+// with the default policy, so that the first aggregation hop, which reads it
+// next, finds part of it in L2.
 #include "sg_internal.cuh"
 #include "sg_objects.cuh"
 
@@ -72,7 +75,7 @@ __global__ void __launch_bounds__(kThreads) k_gather(const int32_t* __restrict__
         }
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u)
-            if (dst[u] >= 0) __stcs(out + dst[u], v[u]);
+            if (dst[u] >= 0) out[dst[u]] = v[u];
     }
     if (stats) {
         hits = warp_sum(hits);
