@@ -100,18 +100,23 @@ __device__ __forceinline__ void store_vec(void* y, int64_t r, int32_t row_vecs, 
 // ..., of row [lo, hi) (a chunk is LPR consecutive edges), for the group of
 // LPR lanes named by gmask (this lane is gl): each lane holds VPL 16-byte
 // vectors of the row (vector gl + p * LPR) and keeps UE edges in flight.
+// With `pre` the column (and weight) of this lane's edge of the first chunk
+// were loaded already (pcol, pw).
 template <int LPR, int VPL, int DT, bool WEIGHTED>
 __device__ __forceinline__ void accumulate_chunks(float (&acc)[VPL][Elems<DT>::n], int32_t lo, int32_t hi, int first,
                                                   int stride, const int32_t* __restrict__ col,
                                                   const float* __restrict__ w, int32_t n_cols,
                                                   const uint4* __restrict__ x, int32_t row_vecs, unsigned gmask,
-                                                  int gl) {
+                                                  int gl, bool pre = false, int32_t pcol = -1, float pw = 1.f) {
     constexpr int UE = VPL >= 8 ? 1 : (VPL == 4 ? 2 : 4);  // edges in flight per lane
     for (int32_t c0 = lo + first * LPR; c0 < hi; c0 += stride * LPR) {
         const int32_t my_e = c0 + gl;
         int32_t my_col = -1;
         float my_w = 1.f;
-        if (my_e < hi) {
+        if (pre && c0 == lo) {
+            my_col = pcol;
+            my_w = pw;
+        } else if (my_e < hi) {
             my_col = __ldg(col + my_e);
             if (WEIGHTED) my_w = __ldg(w + my_e);
         }
@@ -147,21 +152,20 @@ __device__ __forceinline__ void accumulate_chunks(float (&acc)[VPL][Elems<DT>::n
     }
 }
 
-// Scales and stores output row r from the group's accumulators.
+// Scales and stores output row r from the group's accumulators (the mean
+// multiplies by 1 / c: within one rounding of the quotient).
 template <int LPR, int VPL, int DT, bool WEIGHTED>
 __device__ __forceinline__ void store_row(const float (&acc)[VPL][Elems<DT>::n], int64_t r, int32_t c, void* y,
                                           int32_t row_vecs, int gl) {
     constexpr int EPV = Elems<DT>::n;
+    const float rc = WEIGHTED ? 1.f : (c > 0 ? __frcp_rn((float)c) : 0.f);
 #pragma unroll
     for (int p = 0; p < VPL; ++p) {
         const int vi = gl + p * LPR;
         if (vi >= row_vecs) continue;
         float o[EPV];
 #pragma unroll
-        for (int q = 0; q < EPV; ++q) {
-            if (WEIGHTED) o[q] = acc[p][q];
-            else o[q] = c > 0 ? __fdiv_rn(acc[p][q], (float)c) : 0.f;
-        }
+        for (int q = 0; q < EPV; ++q) o[q] = WEIGHTED ? acc[p][q] : acc[p][q] * rc;
         store_vec<DT>(y, r, row_vecs, vi, o);
     }
 }
@@ -174,13 +178,13 @@ __device__ __forceinline__ void store_row(const float (&acc)[VPL][Elems<DT>::n],
 // come first, each by the whole warp of its group: the warp's groups take
 // every (32 / LPR)-th chunk of the row, and their sums are added in a fixed
 // order, so a long row is no longer a serial tail.  Then every group sums its
-// other rows alone, in edge order.
+// other rows alone, in edge order.  Three blocks fit on an SM for fp32 rows,
+// two for bf16 (twice the accumulators).
 template <int LPR, int VPL, int DT, bool WEIGHTED>
-__global__ void __launch_bounds__(kNT) k_spmm(const int32_t* __restrict__ ptr, const int32_t* __restrict__ col,
-                                              const float* __restrict__ w, int32_t n_rows_cap,
-                                              const int32_t* __restrict__ d_rows, int32_t n_cols_cap,
-                                              const int32_t* __restrict__ d_cols, const uint4* __restrict__ x,
-                                              int32_t row_vecs, void* __restrict__ y) {
+__global__ void __launch_bounds__(kNT, DT == DT_F32 ? 3 : 2)
+    k_spmm(const int32_t* __restrict__ ptr, const int32_t* __restrict__ col, const float* __restrict__ w,
+           int32_t n_rows_cap, const int32_t* __restrict__ d_rows, int32_t n_cols_cap,
+           const int32_t* __restrict__ d_cols, const uint4* __restrict__ x, int32_t row_vecs, void* __restrict__ y) {
     constexpr int EPV = Elems<DT>::n;
     constexpr int SG = 32 / LPR;  // groups per warp
     const int64_t n_rows = d_rows ? (int64_t)min(*d_rows, n_rows_cap) : n_rows_cap;
@@ -222,19 +226,39 @@ __global__ void __launch_bounds__(kNT) k_spmm(const int32_t* __restrict__ ptr, c
             }
         }
     }
-    // the other rows, a group each; the next row's bounds are loaded while
-    // the current row is summed
+    // the other rows, a group each.  Row bounds are loaded two rows ahead
+    // and the first chunk's columns one row ahead, so a row's feature loads
+    // start without waiting for its indices.
     int64_t r = gid;
-    int32_t nlo = 0, nhi = 0;
+    int32_t lo1 = 0, hi1 = 0, lo2 = 0, hi2 = 0;  // bounds of rows r and r + groups
     if (r < n_rows) {
-        nlo = ptr[r];
-        nhi = ptr[r + 1];
+        lo1 = ptr[r];
+        hi1 = ptr[r + 1];
+    }
+    if (r + groups < n_rows) {
+        lo2 = ptr[r + groups];
+        hi2 = ptr[r + groups + 1];
+    }
+    int32_t c1 = -1;  // this lane's first-chunk column (and weight) of row r
+    float w1 = 1.f;
+    if (lo1 + gl < hi1) {
+        c1 = __ldg(col + lo1 + gl);
+        if (WEIGHTED) w1 = __ldg(w + lo1 + gl);
     }
     for (; r < n_rows; r += groups) {
-        const int32_t lo = nlo, hi = nhi;
-        if (r + groups < n_rows) {
-            nlo = ptr[r + groups];
-            nhi = ptr[r + groups + 1];
+        const int32_t lo = lo1, hi = hi1, fc = c1;
+        const float fw = w1;
+        lo1 = lo2;
+        hi1 = hi2;
+        c1 = -1;
+        w1 = 1.f;
+        if (r + groups < n_rows && lo1 + gl < hi1) {
+            c1 = __ldg(col + lo1 + gl);
+            if (WEIGHTED) w1 = __ldg(w + lo1 + gl);
+        }
+        if (r + 2 * groups < n_rows) {
+            lo2 = ptr[r + 2 * groups];
+            hi2 = ptr[r + 2 * groups + 1];
         }
         if (SG > 1 && hi - lo > kLongRow) continue;
         float acc[VPL][EPV];
@@ -242,7 +266,7 @@ __global__ void __launch_bounds__(kNT) k_spmm(const int32_t* __restrict__ ptr, c
         for (int p = 0; p < VPL; ++p)
 #pragma unroll
             for (int q = 0; q < EPV; ++q) acc[p][q] = 0.f;
-        accumulate_chunks<LPR, VPL, DT, WEIGHTED>(acc, lo, hi, 0, 1, col, w, n_cols, x, row_vecs, gmask, gl);
+        accumulate_chunks<LPR, VPL, DT, WEIGHTED>(acc, lo, hi, 0, 1, col, w, n_cols, x, row_vecs, gmask, gl, true, fc, fw);
         store_row<LPR, VPL, DT, WEIGHTED>(acc, r, hi - lo, y, row_vecs, gl);
     }
 }
