@@ -170,6 +170,60 @@ __device__ __forceinline__ void store_row(const float (&acc)[VPL][Elems<DT>::n],
     }
 }
 
+// Rows longer than kLongRow edges among the rows of this warp's groups (group
+// g owns rows g, g + groups, ...), one at a time, each by the whole warp: the
+// warp's 32 / LPR groups take every (32 / LPR)-th chunk of the row and their
+// sums are added in a fixed order (xor shuffles by LPR, 2 LPR, ...).
+template <int LPR, int VPL, int DT, bool WEIGHTED>
+__device__ __forceinline__ void long_rows(const int32_t* __restrict__ ptr, const int32_t* __restrict__ col,
+                                          const float* __restrict__ w, int64_t n_rows, int32_t n_cols,
+                                          const uint4* __restrict__ x, int32_t row_vecs, void* __restrict__ y,
+                                          int64_t gid, int64_t groups) {
+    constexpr int EPV = Elems<DT>::n;
+    constexpr int SG = 32 / LPR;
+    const unsigned lane = lane_id();
+    const int gl = lane % LPR, sg = (int)(lane / LPR);
+    const unsigned gmask = LPR == 32 ? 0xffffffffu : (((1u << LPR) - 1u) << (lane - gl));
+    constexpr int kAhead = 4;  // row bounds of this many rounds are loaded together
+    for (int64_t base0 = gid - sg; base0 < n_rows; base0 += kAhead * groups) {
+      int32_t lob[kAhead], hib[kAhead];
+#pragma unroll
+      for (int u = 0; u < kAhead; ++u) {
+          const int64_t rr = base0 + u * groups + sg;
+          lob[u] = 0;
+          hib[u] = 0;
+          if (rr < n_rows) {
+              lob[u] = ptr[rr];
+              hib[u] = ptr[rr + 1];
+          }
+      }
+#pragma unroll
+      for (int u = 0; u < kAhead; ++u) {
+        const int64_t base = base0 + u * groups;
+        const int32_t lo = lob[u], hi = hib[u];
+        unsigned longs = __ballot_sync(0xffffffffu, gl == 0 && hi - lo > kLongRow);
+        while (longs) {
+            const int src = __ffs(longs) - 1;
+            longs &= longs - 1;
+            const int32_t rlo = __shfl_sync(0xffffffffu, lo, src), rhi = __shfl_sync(0xffffffffu, hi, src);
+            float acc[VPL][EPV];
+#pragma unroll
+            for (int p = 0; p < VPL; ++p)
+#pragma unroll
+                for (int q = 0; q < EPV; ++q) acc[p][q] = 0.f;
+            accumulate_chunks<LPR, VPL, DT, WEIGHTED>(acc, rlo, rhi, sg, SG, col, w, n_cols, x, row_vecs, gmask, gl);
+#pragma unroll
+            for (int d = LPR; d < 32; d <<= 1)
+#pragma unroll
+                for (int p = 0; p < VPL; ++p)
+#pragma unroll
+                    for (int q = 0; q < EPV; ++q) acc[p][q] += __shfl_xor_sync(0xffffffffu, acc[p][q], d);
+            if (sg == 0) store_row<LPR, VPL, DT, WEIGHTED>(acc, base + src / LPR, rhi - rlo, y, row_vecs, gl);
+        }
+      }
+    }
+}
+
 // y[r] = scale_r * sum_p w_p x[col[p]] for r < n_rows (see the file comment).
 // WEIGHTED = false: w_p = 1 and scale_r = 1 / row length (forward mean).
 // WEIGHTED = true:  w_p = w[p] and scale_r = 1 (backward over the transpose).
@@ -190,42 +244,13 @@ __global__ void __launch_bounds__(kNT, DT == DT_F32 ? 3 : 2)
     const int64_t n_rows = d_rows ? (int64_t)min(*d_rows, n_rows_cap) : n_rows_cap;
     const int32_t n_cols = d_cols ? min(*d_cols, n_cols_cap) : n_cols_cap;
     const unsigned lane = lane_id();
-    const int gl = lane % LPR, sg = (int)(lane / LPR);
+    const int gl = lane % LPR;
     // the LPR lanes of a group share a row (and so every loop trip count);
     // shuffles name only them, so groups of one warp proceed independently
     const unsigned gmask = LPR == 32 ? 0xffffffffu : (((1u << LPR) - 1u) << (lane - gl));
     const int64_t groups = (int64_t)gridDim.x * (kNT / LPR);
     const int64_t gid = (blockIdx.x * (int64_t)kNT + threadIdx.x) / LPR;
-    if (SG > 1) {
-        // long rows of this warp's groups, one at a time, by the whole warp
-        for (int64_t base = gid - sg; base < n_rows; base += groups) {
-            const int64_t rr = base + sg;
-            int32_t lo = 0, hi = 0;
-            if (rr < n_rows) {
-                lo = ptr[rr];
-                hi = ptr[rr + 1];
-            }
-            unsigned longs = __ballot_sync(0xffffffffu, gl == 0 && hi - lo > kLongRow);
-            while (longs) {
-                const int src = __ffs(longs) - 1;
-                longs &= longs - 1;
-                const int32_t rlo = __shfl_sync(0xffffffffu, lo, src), rhi = __shfl_sync(0xffffffffu, hi, src);
-                float acc[VPL][EPV];
-#pragma unroll
-                for (int p = 0; p < VPL; ++p)
-#pragma unroll
-                    for (int q = 0; q < EPV; ++q) acc[p][q] = 0.f;
-                accumulate_chunks<LPR, VPL, DT, WEIGHTED>(acc, rlo, rhi, sg, SG, col, w, n_cols, x, row_vecs, gmask, gl);
-#pragma unroll
-                for (int d = LPR; d < 32; d <<= 1)
-#pragma unroll
-                    for (int p = 0; p < VPL; ++p)
-#pragma unroll
-                        for (int q = 0; q < EPV; ++q) acc[p][q] += __shfl_xor_sync(0xffffffffu, acc[p][q], d);
-                if (sg == 0) store_row<LPR, VPL, DT, WEIGHTED>(acc, base + src / LPR, rhi - rlo, y, row_vecs, gl);
-            }
-        }
-    }
+    if (SG > 1) long_rows<LPR, VPL, DT, WEIGHTED>(ptr, col, w, n_rows, n_cols, x, row_vecs, y, gid, groups);
     // the other rows, a group each.  Row bounds are loaded two rows ahead
     // and the first chunk's columns one row ahead, so a row's feature loads
     // start without waiting for its indices.
@@ -573,10 +598,10 @@ sg_status run_spmm(const int32_t* ptr, const int32_t* col, const float* w, int32
         lpr = 32;
         vpl = row_vecs <= 128 ? 4 : 8;
     }
+    const bool wgt = w != nullptr;
     int64_t blocks = cdiv((int64_t)n_rows_cap * lpr, kNT);
     if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
     if (blocks < 1) blocks = 1;
-    const bool wgt = w != nullptr;
     if (dt == DT_F32) return wgt ? launch_vec<DT_F32, true>(lpr, vpl, (int)blocks, s, ptr, col, w, n_rows_cap, d_rows, n_cols_cap, d_cols, x, (int32_t)row_vecs, y)
                                  : launch_vec<DT_F32, false>(lpr, vpl, (int)blocks, s, ptr, col, w, n_rows_cap, d_rows, n_cols_cap, d_cols, x, (int32_t)row_vecs, y);
     if (dt == DT_BF16) return wgt ? launch_vec<DT_BF16, true>(lpr, vpl, (int)blocks, s, ptr, col, w, n_rows_cap, d_rows, n_cols_cap, d_cols, x, (int32_t)row_vecs, y)
