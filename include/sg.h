@@ -62,6 +62,7 @@ typedef int32_t sg_status;
 #define SG_MAX_FANOUT 256
 
 typedef void* sg_stream_t;      /* cudaStream_t */
+typedef void* sg_event_t;       /* cudaEvent_t */
 
 typedef struct sg_graph sg_graph;
 typedef struct sg_cache sg_cache;
@@ -180,11 +181,19 @@ sg_status sg_sampler_workspace_init(const sg_graph* g, int32_t n_seeds, const in
  *                run leaves cleared for the next.  Hand the same workspace to
  *                no other call in between, and do not run two calls on it at
  *                once.
+ *   h_hop_events  host array of n_hops event handles (an entry may be NULL),
+ *                or NULL.  Entry h-1 is recorded on `stream` as soon as the
+ *                node list of hop h is final, so that work on V_h (such as
+ *                gathering its feature rows) can start on another stream
+ *                while later hops are sampled.  With n_sub = 1, at that
+ *                point unique[0, |V_h|) and counts[(2H+1) + h] (= |V_h|) are
+ *                final (counts[h] and the block arrays are not yet); with
+ *                n_sub > 1 every entry is recorded at the end of the call.
  * Asynchronous on `stream`; no host synchronisation inside. */
 sg_status sg_sampler_run(const sg_graph* g, const int32_t* d_seeds, int32_t n_seeds, const int32_t* h_batch_ptr,
                          int32_t n_sub, const int32_t* h_fanouts, int32_t n_hops, uint64_t seed,
                          const uint64_t* d_seed, void* d_workspace, size_t workspace_bytes, const sg_blocks* out,
-                         sg_stream_t stream);
+                         const sg_event_t* h_hop_events, sg_stream_t stream);
 
 /* Standalone dedup + relabel (the step sampler_run fuses; FastGL explainer
  * "Fused-Map", GARDEN page Section IV-D hash-table dedup).
@@ -254,16 +263,19 @@ typedef struct sg_gather_stats {
 } sg_gather_stats;
 
 /* Feature gather through the cache (GARDEN page Section II-B, Nfeat-
- * Selecting): for i < n, out row i = feature row d_ids[i], byte for byte,
- * taken from the HBM cache when the node is cached, else read zero-copy from
- * the host table.
+ * Selecting): for first <= i < n, out row i = feature row d_ids[i], byte for
+ * byte, taken from the HBM cache when the node is cached, else read zero-copy
+ * from the host table.
  *   d_ids     device, n_cap node IDs
  *   d_n       device int32 count (n = *d_n <= n_cap) or NULL (n = n_cap)
- *   d_out     device, n_cap x dim in the cache's dtype (rows >= n untouched)
+ *   d_first   device int32 first row (0 <= first, clamped to n) or NULL (0);
+ *             with it a list can be gathered in two parts, the first while
+ *             the rest of the list is still being produced
+ *   d_out     device, n_cap x dim in the cache's dtype (other rows untouched)
  *   d_stats   device, accumulated (+=) hit/miss counters, or NULL
  * An ID out of range sets the device error word and its row is zero-filled. */
-sg_status sg_gather(const sg_cache* c, const int32_t* d_ids, int64_t n_cap, const int32_t* d_n, void* d_out,
-                    sg_gather_stats* d_stats, sg_stream_t stream);
+sg_status sg_gather(const sg_cache* c, const int32_t* d_ids, int64_t n_cap, const int32_t* d_n,
+                    const int32_t* d_first, void* d_out, sg_gather_stats* d_stats, sg_stream_t stream);
 
 /* -------------------------------------------------------------- aggregate */
 /* Mean aggregation over one block (GARDEN page Section II-A Eq. (1) with

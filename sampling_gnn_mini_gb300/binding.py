@@ -99,13 +99,13 @@ def load(build_if_missing: bool = True):
             "sg_graph_destroy": (i32, [vp]),
             "sg_graph_info": (i32, [vp, vp, vp, vp, vp]),
             "sg_sampler_bounds": (i32, [vp, i32, vp, i32, vp, i32, ctypes.POINTER(_Bounds)]),
-            "sg_sampler_run": (i32, [vp, vp, i32, vp, i32, vp, i32, u64, vp, vp, sz, ctypes.POINTER(_Blocks), vp]),
+            "sg_sampler_run": (i32, [vp, vp, i32, vp, i32, vp, i32, u64, vp, vp, sz, ctypes.POINTER(_Blocks), vp, vp]),
             "sg_relabel_workspace": (sz, [i64, i64]),
             "sg_relabel": (i32, [vp, i64, vp, i64, vp, vp, vp, vp, sz, vp]),
             "sg_cache_build": (i32, [vp, vp, i32, i64, i32, vp, i64, ctypes.POINTER(vp), vp]),
             "sg_cache_destroy": (i32, [vp]),
             "sg_cache_info": (i32, [vp, vp, vp, vp, vp, vp]),
-            "sg_gather": (i32, [vp, vp, i64, vp, vp, vp, vp]),
+            "sg_gather": (i32, [vp, vp, i64, vp, vp, vp, vp, vp]),
             "sg_aggregate_fwd": (i32, [vp, vp, i32, i32, vp, vp, i32, i32, vp, i32, vp]),
             "sg_aggregate_bwd_workspace": (sz, [i32, i32, i64]),
             "sg_aggregate_bwd": (i32, [vp, vp, i32, i32, i64, vp, vp, i32, i32, vp, i32, vp, sz, vp]),
@@ -267,15 +267,23 @@ class SampleBuffers:
 
 
 def sg_sampler_run(graph: Graph, seeds: torch.Tensor, fanouts: Sequence[int], seed: int, buffers: SampleBuffers,
-                   batch_ptr: Optional[Sequence[int]] = None, stream=None, d_seed: Optional[torch.Tensor] = None) -> None:
+                   batch_ptr: Optional[Sequence[int]] = None, stream=None, d_seed: Optional[torch.Tensor] = None,
+                   hop_events: Optional[Sequence[Optional[torch.cuda.Event]]] = None) -> None:
+    """hop_events: one entry per hop (a CUDA event that has been recorded at
+    least once, so that it exists, or None); see sg.h."""
     fo = np.ascontiguousarray(fanouts, dtype=np.int32)
     bp = None if batch_ptr is None else np.ascontiguousarray(batch_ptr, dtype=np.int32)
     assert seeds.dtype == torch.int32 and seeds.is_cuda and seeds.is_contiguous()
+    evs = None
+    if hop_events is not None:
+        if len(hop_events) != len(fo):
+            raise ValueError("sg_sampler_run: hop_events needs one entry per hop")
+        evs = (ctypes.c_void_p * len(fo))(*[None if e is None else e.cuda_event for e in hop_events])
     _check(load().sg_sampler_run(graph.handle, seeds.data_ptr(), int(seeds.numel()),
                                  None if bp is None else bp.ctypes.data, 1 if bp is None else len(bp) - 1,
                                  fo.ctypes.data, len(fo), ctypes.c_uint64(seed & 0xFFFFFFFFFFFFFFFF), _ptr(d_seed),
                                  buffers.workspace.data_ptr(), buffers.workspace.numel(),
-                                 ctypes.byref(buffers._blocks), _stream(stream)))
+                                 ctypes.byref(buffers._blocks), evs, _stream(stream)))
 
 
 def sg_relabel(ids: torch.Tensor, prefix: torch.Tensor, stream=None):
@@ -338,9 +346,9 @@ def sg_cache_build(h_feat: Optional[torch.Tensor], d_feat: Optional[torch.Tensor
 
 
 def sg_gather(cache: Cache, ids: torch.Tensor, n_cap: int, d_n: Optional[torch.Tensor], out: torch.Tensor,
-              stats: Optional[torch.Tensor] = None, stream=None) -> None:
-    _check(load().sg_gather(cache.handle, ids.data_ptr(), int(n_cap), _ptr(d_n), out.data_ptr(), _ptr(stats),
-                            _stream(stream)))
+              stats: Optional[torch.Tensor] = None, stream=None, d_first: Optional[torch.Tensor] = None) -> None:
+    _check(load().sg_gather(cache.handle, ids.data_ptr(), int(n_cap), _ptr(d_n), _ptr(d_first), out.data_ptr(),
+                            _ptr(stats), _stream(stream)))
 
 
 # --------------------------------------------------------------- aggregate

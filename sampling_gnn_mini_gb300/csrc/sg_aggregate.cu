@@ -239,6 +239,7 @@ __global__ void __launch_bounds__(kNT, DT == DT_F32 ? 3 : 2)
     k_spmm(const int32_t* __restrict__ ptr, const int32_t* __restrict__ col, const float* __restrict__ w,
            int32_t n_rows_cap, const int32_t* __restrict__ d_rows, int32_t n_cols_cap,
            const int32_t* __restrict__ d_cols, const uint4* __restrict__ x, int32_t row_vecs, void* __restrict__ y) {
+    pdl_start();
     constexpr int EPV = Elems<DT>::n;
     constexpr int SG = 32 / LPR;  // groups per warp
     const int64_t n_rows = d_rows ? (int64_t)min(*d_rows, n_rows_cap) : n_rows_cap;
@@ -303,6 +304,7 @@ __global__ void __launch_bounds__(kNT) k_spmm_scalar(const int32_t* __restrict__
                                                      const int32_t* __restrict__ d_rows, int32_t n_cols_cap,
                                                      const int32_t* __restrict__ d_cols, const void* __restrict__ x,
                                                      int32_t dim, int dt, void* __restrict__ y) {
+    pdl_start();
     const int64_t n_rows = d_rows ? (int64_t)min(*d_rows, n_rows_cap) : n_rows_cap;
     const int32_t n_cols = d_cols ? min(*d_cols, n_cols_cap) : n_cols_cap;
     const int64_t warps = (int64_t)gridDim.x * (kNT / 32);
@@ -364,6 +366,7 @@ __device__ __forceinline__ int32_t set_n_src(const TSet& t, int b) {
 }
 
 __global__ void k_tcount(TSet t) {
+    pdl_start();
     const int b = blockIdx.y;
     const int32_t E = t.indptr[b][set_n_dst(t, b)];
     const int32_t n_src = set_n_src(t, b);
@@ -380,6 +383,7 @@ constexpr int kTTile = 1024;  // entries per scan tile (4 per thread)
 
 // Exclusive scan of tcnt[0, n_src] into tptr[0, n_src] (tptr[n_src] = E).
 __global__ void __launch_bounds__(kNT) k_tscan(TSet t) {
+    pdl_start();
     __shared__ int32_t red[kNT / 32 + 1];
     __shared__ int32_t s_tile, s_excl;
     const int b = blockIdx.y;
@@ -422,6 +426,7 @@ __global__ void __launch_bounds__(kNT) k_tscan(TSet t) {
 
 // Places every edge in its src segment and records the edge's dst row.
 __global__ void k_tscatter(TSet t) {
+    pdl_start();
     const int b = blockIdx.y;
     const int32_t n_dst = set_n_dst(t, b), n_src = set_n_src(t, b);
     const int32_t* indptr = t.indptr[b];
@@ -449,6 +454,7 @@ __device__ __forceinline__ void emit_transposed(const int32_t* indptr, const int
 // Sorts each src segment by edge index.  Segments up to kWarpSortCap are
 // ranked by one warp; longer ones go to the block's list for k_tsort_long.
 __global__ void __launch_bounds__(kNT) k_tsort(TSet t) {
+    pdl_start();
     __shared__ int32_t sk[kNT / 32][kWarpSortCap];
     const int b = blockIdx.y;
     const int32_t n_src = set_n_src(t, b);
@@ -517,6 +523,7 @@ __device__ void block_bitonic_sort(int32_t* keys, int32_t len) {
 }
 
 __global__ void __launch_bounds__(kNT) k_tsort_long(TSet t) {
+    pdl_start();
     __shared__ int32_t sk[kBlockSortCap];
     const int b = blockIdx.y;
     const int32_t n = (int32_t)t.ctr[2 * b + 1];
@@ -549,7 +556,8 @@ int dt_code(int32_t in, int32_t out) {
 template <int DT, bool WGT>
 sg_status launch_vec(int lpr, int vpl, int blocks, cudaStream_t s, const int32_t* ptr, const int32_t* col, const float* w,
                      int32_t nr, const int32_t* dr, int32_t nc, const int32_t* dc, const void* x, int32_t rv, void* y) {
-#define SG_SPMM(L, V) k_spmm<L, V, DT, WGT><<<blocks, kNT, 0, s>>>(ptr, col, w, nr, dr, nc, dc, (const uint4*)x, rv, y)
+#define SG_SPMM(L, V) \
+    SG_CUDA(launch_pdl(k_spmm<L, V, DT, WGT>, dim3(blocks), dim3(kNT), 0, s, ptr, col, w, nr, dr, nc, dc, (const uint4*)x, rv, y))
     if (lpr == 4 && vpl == 1) SG_SPMM(4, 1);
     else if (lpr == 4 && vpl == 2) SG_SPMM(4, 2);
     else if (lpr == 4) SG_SPMM(4, 4);
@@ -558,7 +566,6 @@ sg_status launch_vec(int lpr, int vpl, int blocks, cudaStream_t s, const int32_t
     else if (vpl == 4) SG_SPMM(32, 4);
     else SG_SPMM(32, 8);
 #undef SG_SPMM
-    SG_CHECK_LAUNCH("k_spmm");
     return SG_OK;
 }
 
@@ -576,9 +583,8 @@ sg_status run_spmm(const int32_t* ptr, const int32_t* col, const float* w, int32
     if (!vec_ok) {
         int64_t blocks = cdiv(n_rows_cap, kNT / 32);
         if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
-        k_spmm_scalar<<<(unsigned)blocks, kNT, 0, s>>>(ptr, col, w, n_rows_cap, d_rows, n_cols_cap, d_cols, x, dim,
-                                                      dt == DT_F32 ? DT_F32 : (dt == DT_BF16 ? DT_BF16 : DT_BF16_F32), y);
-        SG_CHECK_LAUNCH("k_spmm_scalar");
+        SG_CUDA(launch_pdl(k_spmm_scalar, dim3((unsigned)blocks), dim3(kNT), 0, s, ptr, col, w, n_rows_cap, d_rows,
+                           n_cols_cap, d_cols, x, dim, dt == DT_F32 ? DT_F32 : (dt == DT_BF16 ? DT_BF16 : DT_BF16_F32), y));
         return SG_OK;
     }
     // a row goes to a group of LPR lanes holding VPL vectors each: small
@@ -680,16 +686,11 @@ sg_status run_transpose(TSet& t, const int64_t* n_dst_cap, const int64_t* n_src_
         if (g < 1) g = 1;
         return dim3((unsigned)g, (unsigned)nb, 1);
     };
-    k_tcount<<<grid(max_e, 256 * 4), 256, 0, s>>>(t);
-    SG_CHECK_LAUNCH("k_tcount");
-    k_tscan<<<grid(max_src + 1, kTTile), kNT, 0, s>>>(t);
-    SG_CHECK_LAUNCH("k_tscan");
-    k_tscatter<<<grid(max_dst, 8), 256, 0, s>>>(t);
-    SG_CHECK_LAUNCH("k_tscatter");
-    k_tsort<<<grid(max_src, kNT / 32), kNT, 0, s>>>(t);
-    SG_CHECK_LAUNCH("k_tsort");
-    k_tsort_long<<<dim3((unsigned)sms, (unsigned)nb, 1), kNT, 0, s>>>(t);
-    SG_CHECK_LAUNCH("k_tsort_long");
+    SG_CUDA(launch_pdl(k_tcount, grid(max_e, 256 * 4), dim3(256), 0, s, t));
+    SG_CUDA(launch_pdl(k_tscan, grid(max_src + 1, kTTile), dim3(kNT), 0, s, t));
+    SG_CUDA(launch_pdl(k_tscatter, grid(max_dst, 8), dim3(256), 0, s, t));
+    SG_CUDA(launch_pdl(k_tsort, grid(max_src, kNT / 32), dim3(kNT), 0, s, t));
+    SG_CUDA(launch_pdl(k_tsort_long, dim3((unsigned)sms, (unsigned)nb, 1), dim3(kNT), 0, s, t));
     return SG_OK;
 }
 

@@ -25,20 +25,27 @@ constexpr int kThreads = 256;
 constexpr int kUnroll = 8;
 
 __global__ void __launch_bounds__(kThreads) k_gather(const int32_t* __restrict__ ids, const int32_t* __restrict__ d_n,
+                                                     const int32_t* __restrict__ d_first,
                                                      int64_t n_cap, const int32_t* __restrict__ slot_of, int64_t n_nodes,
                                                      const uint4* __restrict__ cache, const uint4* __restrict__ host,
                                                      int32_t row_vecs, int64_t step_rows, int32_t step_rem,
                                                      uint4* __restrict__ out, sg_gather_stats* __restrict__ stats) {
+    pdl_start();
     int64_t n = n_cap;
     if (d_n) {
         const int64_t dn = *d_n;
         n = dn < n_cap ? (dn < 0 ? 0 : dn) : n_cap;
     }
+    int64_t first = 0;
+    if (d_first) {
+        const int64_t df = *d_first;
+        first = df < 0 ? 0 : (df < n ? df : n);
+    }
     const int64_t total = n * row_vecs;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     // (i, c) = (row, vector) of flat index t, advanced by the grid stride
     // without a division: stride = step_rows * row_vecs + step_rem.
-    int64_t t = blockIdx.x * (int64_t)kThreads + threadIdx.x;
+    int64_t t = first * row_vecs + blockIdx.x * (int64_t)kThreads + threadIdx.x;
     int64_t i = t / row_vecs;
     int32_t c = (int32_t)(t - i * row_vecs);
     unsigned long long hits = 0, misses = 0;
@@ -89,8 +96,8 @@ __global__ void __launch_bounds__(kThreads) k_gather(const int32_t* __restrict__
 
 }  // namespace
 
-extern "C" sg_status sg_gather(const sg_cache* c, const int32_t* d_ids, int64_t n_cap, const int32_t* d_n, void* d_out,
-                               sg_gather_stats* d_stats, sg_stream_t stream) {
+extern "C" sg_status sg_gather(const sg_cache* c, const int32_t* d_ids, int64_t n_cap, const int32_t* d_n,
+                               const int32_t* d_first, void* d_out, sg_gather_stats* d_stats, sg_stream_t stream) {
     if (!c) return fail(SG_ERR_INVALID_ARG, "sg_gather: NULL cache");
     if (n_cap < 0) return fail(SG_ERR_INVALID_ARG, "sg_gather: n_cap < 0");
     if (n_cap == 0) return SG_OK;
@@ -105,9 +112,8 @@ extern "C" sg_status sg_gather(const sg_cache* c, const int32_t* d_ids, int64_t 
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     const int64_t stride = blocks * kThreads;
-    k_gather<<<(unsigned)blocks, kThreads, 0, (cudaStream_t)stream>>>(
-        d_ids, d_n, n_cap, c->slot_of, c->n_nodes, (const uint4*)c->rows, (const uint4*)c->host_rows,
-        (int32_t)row_vecs, stride / row_vecs, (int32_t)(stride % row_vecs), (uint4*)d_out, d_stats);
-    SG_CHECK_LAUNCH("k_gather");
+    SG_CUDA(launch_pdl(k_gather, dim3((unsigned)blocks), dim3(kThreads), 0, (cudaStream_t)stream, d_ids, d_n, d_first,
+                       n_cap, c->slot_of, c->n_nodes, (const uint4*)c->rows, (const uint4*)c->host_rows,
+                       (int32_t)row_vecs, stride / row_vecs, (int32_t)(stride % row_vecs), (uint4*)d_out, d_stats));
     return SG_OK;
 }

@@ -48,6 +48,32 @@ unsigned fetch_err_gather(cudaStream_t);
 unsigned fetch_err_aggregate(cudaStream_t);
 unsigned fetch_err_api(cudaStream_t);
 
+// ------------------------------------------------------ dependent launches
+// Kernels of the per-batch path are launched with programmatic stream
+// serialization: a kernel may be scheduled while the previous kernel of the
+// stream still runs, and griddepcontrol.wait holds it until that kernel has
+// completed and its writes are visible.  Every such kernel calls pdl_start()
+// first, before any early return, so a grid never completes ahead of the
+// kernel before it (which keeps the usual stream order for the kernels after
+// it).  No kernel triggers early: the next grid is scheduled as this one's
+// blocks exit.
+__device__ __forceinline__ void pdl_start() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ------------------------------------------------------------ arithmetic
 __host__ __device__ __forceinline__ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 

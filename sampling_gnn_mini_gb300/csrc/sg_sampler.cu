@@ -123,6 +123,7 @@ __device__ void load_prefix_sub_n(const int32_t* counts, CountsLayout L, int K, 
 // one mini-batch or an ID out of range is reported through the error word.
 __global__ void k_seed_init(const int32_t* __restrict__ seeds, int32_t n_seeds, SubPtr bptr, int K, int64_t n_nodes,
                             uint2* table, int logT, int32_t* ustr, int64_t capU, int32_t* counts, CountsLayout L) {
+    pdl_start();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (blockIdx.x == 0) {
         if (threadIdx.x == 0) counts[L.tot_n(0)] = n_seeds;
@@ -216,6 +217,7 @@ __device__ void map_prev_edges(const HopArgs& a, int blk, int nblk, int32_t* ep,
 template <typename Off>
 __global__ void __launch_bounds__(kNT) k_rows(HopArgs a, int seed_mode, const int32_t* __restrict__ seeds,
                                               SubPtr bptr) {
+    pdl_start();
     __shared__ int32_t pre[SG_MAX_SUB + 1];
     __shared__ int32_t ep[SG_MAX_SUB + 1];
     __shared__ int32_t red[kNT / 32 + 1];
@@ -675,6 +677,7 @@ __device__ void sample_big_row(const HopArgs& a, int32_t r, const int32_t* pre, 
 // take units (a bin 2 row; four bin 1 rows, one per 8-lane group; or sixteen
 // full rows).  The grid is at most what fits on the GPU at once.
 __global__ void __launch_bounds__(kNT) k_sample(HopArgs a) {
+    pdl_start();
     __shared__ int32_t pre[SG_MAX_SUB + 1];
     __shared__ __align__(16) uint32_t s_key[kBlockPool];
     __shared__ uint32_t s_pos[kBlockPool];
@@ -735,6 +738,7 @@ __global__ void __launch_bounds__(kNT) k_sample(HopArgs a) {
 // copies the owner's neighbours into its own edge range and inserts them into
 // its own mini-batch's table at its own positions.
 __global__ void __launch_bounds__(kNT) k_copy(HopArgs a) {
+    pdl_start();
     __shared__ int32_t pre[SG_MAX_SUB + 1];
     load_prefix_sub_n(a.counts, a.L, a.K, a.h - 1, pre);
     const int64_t T = pre[a.K];
@@ -754,6 +758,7 @@ __global__ void __launch_bounds__(kNT) k_copy(HopArgs a) {
 // ----------------------------------------------------------------- relabel
 // First-occurrence flags and new local IDs; one scan chain per mini-batch.
 __global__ void __launch_bounds__(kNT) k_relabel(HopArgs a) {
+    pdl_start();
     __shared__ int32_t ep[SG_MAX_SUB + 1];
     __shared__ int32_t tpre[SG_MAX_SUB + 1];
     __shared__ int32_t red[kNT / 32 + 1];
@@ -838,6 +843,7 @@ __global__ void __launch_bounds__(kNT) k_relabel(HopArgs a) {
 // Maps the last hop's edges, writes the last total and, for a super-batch,
 // lays the mini-batches' V_H back to back.
 __global__ void __launch_bounds__(kNT) k_finish(HopArgs a, int32_t* unique_out) {
+    pdl_start();
     __shared__ int32_t pre[SG_MAX_SUB + 1];
     __shared__ int32_t ep[SG_MAX_SUB + 1];
     load_prefix_sub_n(a.counts, a.L, a.K, a.h, pre);
@@ -857,6 +863,7 @@ __global__ void __launch_bounds__(kNT) k_finish(HopArgs a, int32_t* unique_out) 
 // direct-map entry back to empty, and the scan states and counters of all
 // hops are reset (all-ones).
 __global__ void __launch_bounds__(kNT) k_cleanup(HopArgs a, uint32_t* reset, int64_t reset_words) {
+    pdl_start();
     __shared__ int32_t pre[SG_MAX_SUB + 1];
     load_prefix_sub_n(a.counts, a.L, a.K, a.h, pre);
     const int64_t n = pre[a.K];
@@ -872,6 +879,7 @@ __global__ void __launch_bounds__(kNT) k_cleanup(HopArgs a, uint32_t* reset, int
 // ------------------------------------------------------ standalone relabel
 __global__ void k_relabel_insert(const int32_t* __restrict__ ids, int64_t n_ids, uint2* table, int logT, int32_t pos_base,
                                  int32_t* enbr, int32_t* eslot, int32_t* epre) {
+    pdl_start();
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         epre[0] = 0;
         epre[1] = (int32_t)n_ids;
@@ -1058,7 +1066,7 @@ extern "C" sg_status sg_sampler_workspace_init(const sg_graph* g, int32_t n_seed
 extern "C" sg_status sg_sampler_run(const sg_graph* g, const int32_t* d_seeds, int32_t n_seeds, const int32_t* h_batch_ptr,
                                     int32_t n_sub, const int32_t* h_fanouts, int32_t n_hops, uint64_t seed,
                                     const uint64_t* d_seed, void* d_workspace, size_t workspace_bytes,
-                                    const sg_blocks* out, sg_stream_t stream) {
+                                    const sg_blocks* out, const sg_event_t* h_hop_events, sg_stream_t stream) {
     Plan p;
     sg_status st = make_plan(g, n_seeds, h_batch_ptr, n_sub, h_fanouts, n_hops, &p);
     if (st != SG_OK) return st;
@@ -1125,18 +1133,19 @@ extern "C" sg_status sg_sampler_run(const sg_graph* g, const int32_t* d_seeds, i
         const int64_t row_blocks = clamp_blocks(cdiv(nb, kTile), cap_blocks);
         const int seed_mode = h == 1;
         if (g->offset_bits == 32)
-            k_rows<int32_t><<<(unsigned)(a.map_blocks + row_blocks), kNT, 0, s>>>(a, seed_mode, d_seeds, bp);
+            SG_CUDA(launch_pdl(k_rows<int32_t>, dim3((unsigned)(a.map_blocks + row_blocks)), dim3(kNT), 0, s, a,
+                               seed_mode, d_seeds, bp));
         else
-            k_rows<int64_t><<<(unsigned)(a.map_blocks + row_blocks), kNT, 0, s>>>(a, seed_mode, d_seeds, bp);
-        SG_CHECK_LAUNCH("k_rows");
-        k_sample<<<(unsigned)clamp_blocks(cdiv(nb, kNT / 32), sample_blocks), kNT, 0, s>>>(a);
-        SG_CHECK_LAUNCH("k_sample");
+            SG_CUDA(launch_pdl(k_rows<int64_t>, dim3((unsigned)(a.map_blocks + row_blocks)), dim3(kNT), 0, s, a,
+                               seed_mode, d_seeds, bp));
+        SG_CUDA(launch_pdl(k_sample, dim3((unsigned)clamp_blocks(cdiv(nb, kNT / 32), sample_blocks)), dim3(kNT), 0, s, a));
         if (K > 1) {
-            k_copy<<<(unsigned)clamp_blocks(cdiv(nb, kNT / 32), cap_blocks), kNT, 0, s>>>(a);
-            SG_CHECK_LAUNCH("k_copy");
+            SG_CUDA(launch_pdl(k_copy, dim3((unsigned)clamp_blocks(cdiv(nb, kNT / 32), cap_blocks)), dim3(kNT), 0, s, a));
         }
-        k_relabel<<<(unsigned)clamp_blocks(cdiv(eb, kTile) + K, cap_blocks), kNT, 0, s>>>(a);
-        SG_CHECK_LAUNCH("k_relabel");
+        SG_CUDA(launch_pdl(k_relabel, dim3((unsigned)clamp_blocks(cdiv(eb, kTile) + K, cap_blocks)), dim3(kNT), 0, s, a));
+        // one mini-batch: V_h is final in `unique` (and its size in sub_n(0, h))
+        if (K == 1 && h_hop_events && h_hop_events[h - 1])
+            SG_CUDA(cudaEventRecord((cudaEvent_t)h_hop_events[h - 1], s));
     }
     // the last hop's edges, the last total and the super-batch layout
     a.prev_bidx = out->idx[H - 1];
@@ -1144,12 +1153,15 @@ extern "C" sg_status sg_sampler_run(const sg_graph* g, const int32_t* d_seeds, i
     a.prev_enbr = (const int32_t*)(ws + p.o_enbr[(H - 1) & 1]);
     a.h = H;
     const int64_t fin = p.eb_tot[H - 1] > p.nb_tot[H] ? p.eb_tot[H - 1] : p.nb_tot[H];
-    k_finish<<<(unsigned)clamp_blocks(cdiv(fin, kNT * 4), cap_blocks), kNT, 0, s>>>(a, K > 1 ? out->unique : nullptr);
-    SG_CHECK_LAUNCH("k_finish");
+    SG_CUDA(launch_pdl(k_finish, dim3((unsigned)clamp_blocks(cdiv(fin, kNT * 4), cap_blocks)), dim3(kNT), 0, s, a,
+                       K > 1 ? out->unique : nullptr));
     const int64_t reset_words = (int64_t)(p.o_rest - p.o_zero) / 4;
-    k_cleanup<<<(unsigned)clamp_blocks(cdiv(p.nb_tot[H] > reset_words ? p.nb_tot[H] : reset_words, kNT * 4), cap_blocks),
-                kNT, 0, s>>>(a, (uint32_t*)(ws + p.o_zero), reset_words);
-    SG_CHECK_LAUNCH("k_cleanup");
+    const int64_t clean = p.nb_tot[H] > reset_words ? p.nb_tot[H] : reset_words;
+    SG_CUDA(launch_pdl(k_cleanup, dim3((unsigned)clamp_blocks(cdiv(clean, kNT * 4), cap_blocks)), dim3(kNT), 0, s, a,
+                       (uint32_t*)(ws + p.o_zero), reset_words));
+    if (K > 1 && h_hop_events)  // a super-batch's `unique` is laid out by k_finish
+        for (int h = 1; h <= H; ++h)
+            if (h_hop_events[h - 1]) SG_CUDA(cudaEventRecord((cudaEvent_t)h_hop_events[h - 1], s));
     return SG_OK;
 }
 
@@ -1216,19 +1228,16 @@ sg_status relabel_launch(const RelabelPlan& p, char* ws, const int32_t* d_ids, i
     bp.v[0] = 0;
     bp.v[1] = (int32_t)n_prefix;
     const int sms = num_sms();
-    k_seed_init<<<n_prefix > 0 ? (int)cdiv(n_prefix, 256) : 1, 256, 0, s>>>(d_prefix, (int32_t)n_prefix, bp, 1, a.n_nodes,
-                                                                          a.table, p.logT, a.ustr, p.capU, a.counts, L);
-    SG_CHECK_LAUNCH("k_seed_init");
+    SG_CUDA(launch_pdl(k_seed_init, dim3(n_prefix > 0 ? (int)cdiv(n_prefix, 256) : 1), dim3(256), 0, s, d_prefix,
+                       (int32_t)n_prefix, bp, 1, a.n_nodes, a.table, p.logT, a.ustr, p.capU, a.counts, L));
     const int64_t ib = clamp_blocks(cdiv(n_ids, 256), (int64_t)sms * 8);
-    k_relabel_insert<<<(unsigned)ib, 256, 0, s>>>(d_ids, n_ids, a.table, p.logT, a.pos_base, a.enbr, a.eslot, a.epre);
-    SG_CHECK_LAUNCH("k_relabel_insert");
-    k_relabel<<<(unsigned)clamp_blocks(cdiv(n_ids, kTile) + 1, (int64_t)sms * 8), kNT, 0, s>>>(a);
-    SG_CHECK_LAUNCH("k_relabel");
+    SG_CUDA(launch_pdl(k_relabel_insert, dim3((unsigned)ib), dim3(256), 0, s, d_ids, n_ids, a.table, p.logT, a.pos_base,
+                       a.enbr, a.eslot, a.epre));
+    SG_CUDA(launch_pdl(k_relabel, dim3((unsigned)clamp_blocks(cdiv(n_ids, kTile) + 1, (int64_t)sms * 8)), dim3(kNT), 0, s, a));
     a.prev_bidx = d_local;
     a.prev_epre = a.epre;
     a.prev_eslot = a.eslot;
-    k_finish<<<(unsigned)ib, kNT, 0, s>>>(a, nullptr);
-    SG_CHECK_LAUNCH("k_finish");
+    SG_CUDA(launch_pdl(k_finish, dim3((unsigned)ib), dim3(kNT), 0, s, a, nullptr));
     SG_CUDA(cudaMemcpyAsync(d_n_unique, a.counts + L.tot_n(1), sizeof(int32_t), cudaMemcpyDeviceToDevice, s));
     return SG_OK;
 }

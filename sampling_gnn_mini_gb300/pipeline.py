@@ -12,8 +12,11 @@ seeds, aggregation inward from the input nodes):
 Every size that depends on the sample stays on the device (the calls read
 the counts the sampler wrote), so a step has no host synchronisation and can
 be captured in a CUDA graph and replayed with new seeds (written into the
-device seed buffers first).  This module only allocates buffers and orders
-the calls.
+device seed buffers first).  With one mini-batch the gather runs in two
+parts: V_{H-1} is a prefix of V_H and is final once hop H-1 is relabelled
+(the sampler records an event there), so its feature rows are gathered on a
+second stream while hop H is sampled, and only the rows new at hop H wait for
+the sampler.  This module only allocates buffers and orders the calls.
 """
 from __future__ import annotations
 
@@ -51,6 +54,18 @@ class MiniBatchPipeline:
             self.side = torch.cuda.Stream(device=device)
             self.ev_sampled = torch.cuda.Event()
             self.ev_transposed = torch.cuda.Event()
+        # split gather (one mini-batch, two hops or more): the rows of V_{H-1}
+        # go first, on their own stream
+        self.split_gather = (self.batch_ptr is None or len(self.batch_ptr) == 2) and self.H >= 2
+        if self.split_gather:
+            H = self.H
+            self.gather_stream = torch.cuda.Stream(device=device)
+            self.ev_prefix = torch.cuda.Event()
+            self.ev_prefix.record()  # creates the event, whose handle the sampler records
+            self.ev_gathered = torch.cuda.Event()
+            # |V_{H-1}| of the single mini-batch, final when ev_prefix fires
+            at = (2 * H + 1) + (H - 1)
+            self.n_prefix = self.buf.counts[at:at + 1]
 
     @property
     def counts(self) -> torch.Tensor:
@@ -67,12 +82,28 @@ class MiniBatchPipeline:
         self.seeds[: seeds.numel()].copy_(seeds, non_blocking=True)
         self.d_seed.fill_(seed if seed < (1 << 63) else seed - (1 << 64))
 
-    def sample(self, stream=None) -> None:
+    def sample(self, stream=None, hop_events=None) -> None:
         sg.sg_sampler_run(self.graph, self.seeds[: self.n_seeds], self.fanouts, 0, self.buf, self.batch_ptr,
-                          stream=stream, d_seed=self.d_seed)
+                          stream=stream, d_seed=self.d_seed, hop_events=hop_events)
+
+    def gather_prefix(self, stream=None) -> None:
+        """Rows of V_{H-1} (split gather only)."""
+        H = self.H
+        sg.sg_gather(self.cache, self.buf.unique, self.bounds.max_nodes[H - 1], self.n_prefix, self.h_feat[H],
+                     self.stats, stream=stream)
+
+    def gather_rest(self, stream=None) -> None:
+        """Rows of V_H from |V_{H-1}| on (split gather only)."""
+        H = self.H
+        sg.sg_gather(self.cache, self.buf.unique, self.bounds.max_nodes[H], self.buf.counts[H:H + 1],
+                     self.h_feat[H], self.stats, stream=stream, d_first=self.n_prefix)
 
     def gather(self, stream=None) -> None:
         H = self.H
+        if self.split_gather:
+            self.gather_prefix(stream)
+            self.gather_rest(stream)
+            return
         sg.sg_gather(self.cache, self.buf.unique, self.bounds.max_nodes[H], self.buf.counts[H:H + 1],
                      self.h_feat[H], self.stats, stream=stream)
 
@@ -95,15 +126,28 @@ class MiniBatchPipeline:
     def step(self, stream=None) -> None:
         """Sample, gather, forward and (if enabled) backward of one batch.
         The transposed blocks are built on a second stream that forks after
-        sampling and joins before the backward pass."""
+        sampling and joins before the backward pass; with the split gather,
+        V_{H-1}'s rows are gathered on a third stream during hop H."""
         main = torch.cuda.current_stream() if stream is None else stream
-        self.sample(main)
+        if self.split_gather:
+            events = [None] * self.H
+            events[self.H - 2] = self.ev_prefix
+            self.sample(main, hop_events=events)
+            self.gather_stream.wait_event(self.ev_prefix)
+            self.gather_prefix(self.gather_stream)
+            self.ev_gathered.record(self.gather_stream)
+        else:
+            self.sample(main)
         if self.backward:
             self.ev_sampled.record(main)
             self.side.wait_event(self.ev_sampled)
             self.transpose(self.side)
             self.ev_transposed.record(self.side)
-        self.gather(main)
+        if self.split_gather:
+            self.gather_rest(main)
+            main.wait_event(self.ev_gathered)
+        else:
+            self.gather(main)
         self.forward(main)
         if self.backward:
             main.wait_event(self.ev_transposed)

@@ -83,6 +83,29 @@ def test_gather_device_count_and_fill_from_device_copy():
     assert np.all(got[123:] == -7.0)
 
 
+def test_gather_in_two_parts_with_device_first_row():
+    # a list gathered as [0, first) and [first, n): each part writes only its
+    # rows, together they equal the whole gather; first is clamped to n
+    n, dim = 700, 100
+    feat = synth.features(n, dim, "f32", 5)
+    cache, _h = _cache(feat, np.arange(0, n, 3, dtype=np.int32), n // 3 + 1)
+    ids = np.random.default_rng(6).permutation(n).astype(np.int32)
+    for first, count in ((250, 600), (0, 600), (600, 600), (900, 600)):
+        out = torch.full((n, dim), -3.0, device="cuda")
+        d_first = torch.tensor([first], dtype=torch.int32, device="cuda")
+        d_n = torch.tensor([count], dtype=torch.int32, device="cuda")
+        sg.sg_gather(cache, dev_i32(ids), n, d_n, out, d_first=d_first)
+        sg.sg_stream_check()
+        got = out.cpu().numpy()
+        lo = min(first, count)
+        assert np.all(got[:lo] == -3.0) and np.all(got[count:] == -3.0)
+        assert np.array_equal(got[lo:count], feat[ids[lo:count]])
+        sg.sg_gather(cache, dev_i32(ids), n, d_first, out)  # the prefix [0, first)
+        sg.sg_stream_check()
+        got = out.cpu().numpy()
+        assert np.array_equal(got[:count], feat[ids[:count]])
+
+
 def test_gather_rejects_out_of_range_id():
     n, dim = 100, 16
     feat = synth.features(n, dim, "f32", 5)
