@@ -54,6 +54,7 @@ namespace {
 
 constexpr int kNT = 256;             // threads of every sampler kernel (8 warps)
 constexpr int kTile = 1024;          // rows / edges per scan tile (4 per thread)
+constexpr int kCtrWords = 16;       // counters of one hop (see HopArgs::ctr)
 constexpr int kGroupLambdaMax = 64;  // short random rows go to 8-lane groups when f + 2 sqrt(f) + 4 <= this
 constexpr uint32_t kEmpty = 0xFFFFFFFFu;
 
@@ -144,6 +145,14 @@ __global__ void k_seed_init(const int32_t* __restrict__ seeds, int32_t n_seeds, 
 }
 
 // ---------------------------------------------------------------- hop args
+// What k_sample needs of a row, written into its degree bin by k_rows so that
+// a unit of work is one record load: the row's CSR start and degree, its
+// node, its index in V_{h-1} and its first edge in the block.
+struct __align__(16) BinRec {
+    int32_t start_lo, start_hi, deg, v;
+    int32_t r, out0, pad0, pad1;
+};
+
 struct HopArgs {
     const void* indptr;
     const int32_t* indices;
@@ -159,10 +168,9 @@ struct HopArgs {
     int32_t* ustr;
     uint2* table;
     // this hop's rows
-    int4* rmeta;             // per row: start lo, start hi, degree, node ID
-    int32_t* bins;           // 4 lists of row indices, stride bin_stride
-    int64_t bin_stride;
-    uint32_t* ctr;           // [0] row tiles, [1] edge tiles, [2..5] bin sizes
+    struct BinRec* brec;     // the four degree bins (see bin_slot)
+    int64_t bin_cap;         // capacity of one half of brec (rows of the hop's bound)
+    uint32_t* ctr;           // [0] row tiles, [1] edge tiles, [2..9] bin sizes, [10] block rows, [11] units
     unsigned long long* row_status;
     unsigned long long* edge_status;
     int32_t* bindptr;
@@ -182,13 +190,41 @@ struct HopArgs {
     int map_blocks;
 };
 
-// bins: 0 full row, 1 small random row (group path), 2 random row (warp),
-// 3 random row longer than 4096 (warp, first)
+// Entry i of bin b.  Bins 2j and 2j+1 share quarter j of brec (the even bin
+// from its start, the odd one from its end), so the eight bins of a hop take
+// four row capacities.
+__device__ __forceinline__ BinRec* bin_slot(const HopArgs& a, int b, int64_t i) {
+    const int64_t half = (int64_t)(b >> 1) * a.bin_cap;
+    return a.brec + half + ((b & 1) ? a.bin_cap - 1 - i : i);
+}
+
+__device__ __forceinline__ BinRec load_rec(const BinRec* p) {
+    const int4 x = reinterpret_cast<const int4*>(p)[0], y = reinterpret_cast<const int4*>(p)[1];
+    BinRec rc;
+    rc.start_lo = x.x;
+    rc.start_hi = x.y;
+    rc.deg = x.z;
+    rc.v = x.w;
+    rc.r = y.x;
+    rc.out0 = y.y;
+    rc.pad0 = rc.pad1 = 0;
+    return rc;
+}
+
+// bins: 0 full row, 1 small random row (8-lane groups), 2..4 random rows up
+// to 1024, 2048 and 4096 positions (a warp each), 5..7 up to 8192, 16384 and
+// longer (a block each).  Work goes out longest first (bins 7..5, then 4..2,
+// then 1 and 0), so that no long row is started last.
+constexpr int kBins = 8;
 __device__ __forceinline__ int degree_bin(int64_t deg, int f, bool group_ok) {
     if (deg <= f) return 0;
     if (deg <= 256 && group_ok) return 1;
-    if (deg <= 4096) return 2;
-    return 3;
+    if (deg <= 1024) return 2;
+    if (deg <= 2048) return 3;
+    if (deg <= 4096) return 4;
+    if (deg <= 8192) return 5;
+    if (deg <= 16384) return 6;
+    return 7;
 }
 
 // Edge e of the previous hop gets its src row (mini-batch offset + local ID).
@@ -221,7 +257,7 @@ __global__ void __launch_bounds__(kNT) k_rows(HopArgs a, int seed_mode, const in
     __shared__ int32_t pre[SG_MAX_SUB + 1];
     __shared__ int32_t ep[SG_MAX_SUB + 1];
     __shared__ int32_t red[kNT / 32 + 1];
-    __shared__ int32_t s_tile, s_excl, s_bcnt[4], s_bbase[4];
+    __shared__ int32_t s_tile, s_excl, s_bcnt[kBins], s_bbase[kBins];
     if (seed_mode) {
         for (int k = threadIdx.x; k <= a.K; k += kNT) pre[k] = bptr.v[k];
         __syncthreads();
@@ -259,41 +295,57 @@ __global__ void __launch_bounds__(kNT) k_rows(HopArgs a, int seed_mode, const in
         const int64_t tile = s_tile;
         if (tile >= n_tiles) break;
         const int64_t r0 = tile * kTile + (int64_t)threadIdx.x * 4;
-        int32_t c[4];
-        int b[4];
+        int32_t c[4], dg[4], vv[4];
+        int64_t st[4];
+        int b[4], kq[4];
         int32_t mysum = 0;
+        // the four rows' nodes, then their CSR bounds, each set loaded at
+        // once; the side effects (seed placement, owner table) come after
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int64_t r = r0 + q;
+            kq[q] = 0;
+            vv[q] = -1;
+            if (r < T) {
+                kq[q] = find_sub(pre, a.K, r);
+                vv[q] = seed_mode ? seeds[r] : a.ustr[(int64_t)kq[q] * a.capU + (r - pre[kq[q]])];
+            }
+        }
+        int64_t en[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            st[q] = 0;
+            en[q] = 0;
+            if (r0 + q < T && vv[q] >= 0 && (int64_t)vv[q] < a.n_nodes) {
+                st[q] = (int64_t)indptr[vv[q]];
+                en[q] = (int64_t)indptr[vv[q] + 1];
+            }
+        }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int64_t r = r0 + q;
             c[q] = 0;
             b[q] = -1;
+            dg[q] = 0;
             if (r < T) {
-                const int k = find_sub(pre, a.K, r);
-                int32_t v;
+                const int k = kq[q];
+                const int32_t v = vv[q];
+                const bool ok = v >= 0 && (int64_t)v < a.n_nodes;
                 if (seed_mode) {
-                    v = seeds[r];
                     const int32_t l = (int32_t)(r - pre[k]);
                     a.ustr[(int64_t)k * a.capU + l] = v;
-                    if (v >= 0 && (int64_t)v < a.n_nodes) {
+                    if (ok) {
                         const uint32_t old = atomicMin(a.pos_of + (int64_t)k * a.n_nodes + v, (uint32_t)l);
                         if (old != kEmpty) dev_err(ERR_ARG);  // a repeated seed in one mini-batch
                     }
-                } else {
-                    v = a.ustr[(int64_t)k * a.capU + (r - pre[k])];
                 }
-                int64_t start = 0, deg = 0;
-                if (v >= 0 && (int64_t)v < a.n_nodes) {
-                    start = (int64_t)indptr[v];
-                    deg = (int64_t)indptr[v + 1] - start;
-                } else {
-                    dev_err(ERR_INDEX);
-                }
+                if (!ok) dev_err(ERR_INDEX);
+                const int64_t deg = en[q] - st[q];
                 c[q] = (int32_t)(deg < f ? deg : f);
                 b[q] = degree_bin(deg, f, group_ok);
-                a.rmeta[r] = make_int4((int32_t)(uint32_t)start, (int32_t)(start >> 32), (int32_t)deg, v);
+                dg[q] = (int32_t)deg;
                 if (a.utab) {  // super-batch: the first row of a node samples it
-                    a.rslot[r] = (v >= 0 && (int64_t)v < a.n_nodes)
-                                     ? table_insert(a.utab, a.logU, v, (uint32_t)r, nullptr) : -1;
+                    a.rslot[r] = ok ? table_insert(a.utab, a.logU, v, (uint32_t)r, nullptr) : -1;
                 }
             }
             mysum += c[q];
@@ -307,14 +359,15 @@ __global__ void __launch_bounds__(kNT) k_rows(HopArgs a, int seed_mode, const in
             if (late && threadIdx.x == 0) dev_err(ERR_TIMEOUT);
         }
         // bin sizes of the tile, then one global atomic per bin
-        if (threadIdx.x < 4) s_bcnt[threadIdx.x] = 0;
+        if (threadIdx.x < kBins) s_bcnt[threadIdx.x] = 0;
         __syncthreads();
         int brank[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) brank[q] = b[q] >= 0 ? atomicAdd(&s_bcnt[b[q]], 1) : 0;
         __syncthreads();
-        if (threadIdx.x < 4)
-            s_bbase[threadIdx.x] = s_bcnt[threadIdx.x] ? (int32_t)(atomicAdd(a.ctr + 2 + threadIdx.x, (uint32_t)s_bcnt[threadIdx.x]) + 1u) : 0;
+        if (threadIdx.x < kBins)
+            s_bbase[threadIdx.x] =
+                s_bcnt[threadIdx.x] ? (int32_t)(atomicAdd(a.ctr + 2 + threadIdx.x, (uint32_t)s_bcnt[threadIdx.x]) + 1u) : 0;
         __syncthreads();
         int32_t off = s_excl + ex;
 #pragma unroll
@@ -327,12 +380,14 @@ __global__ void __launch_bounds__(kNT) k_rows(HopArgs a, int seed_mode, const in
                     a.epre[k] = off;
                     --k;
                 }
+                if (b[q] >= 0) {
+                    int4* d = reinterpret_cast<int4*>(bin_slot(a, b[q], s_bbase[b[q]] + brank[q]));
+                    d[0] = make_int4((int32_t)(uint32_t)st[q], (int32_t)(st[q] >> 32), dg[q], vv[q]);
+                    d[1] = make_int4((int32_t)r, off, 0, 0);
+                }
             }
             off += c[q];
         }
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            if (b[q] >= 0) a.bins[b[q] * a.bin_stride + s_bbase[b[q]] + brank[q]] = (int32_t)(r0 + q);
         if (tile == n_tiles - 1 && threadIdx.x == kNT - 1) {
             const int32_t E = s_excl + tile_total;
             a.bindptr[T] = E;
@@ -545,17 +600,16 @@ __device__ void sample_random_row(const HopArgs& a, uint32_t* tab, uint32_t k0, 
     sample_exact<W>(a, tab, k0, k1, v, start, deg, out0, (int32_t*)p.sel, mask, gl);
 }
 
-// Row r of the frontier, by a group of W lanes.
+// One row of the frontier (its bin record), by a group of W lanes.
 template <int W>
-__device__ void sample_row(const HopArgs& a, int32_t r, const int32_t* pre, uint32_t k0, uint32_t k1, const Pool& p,
-                           unsigned mask, int gl) {
-    const int4 m = a.rmeta[r];
-    const int32_t v = m.w;
-    const int64_t deg = m.z;
+__device__ void sample_row(const HopArgs& a, const BinRec& rc, const int32_t* pre, uint32_t k0, uint32_t k1,
+                           const Pool& p, unsigned mask, int gl) {
+    const int32_t v = rc.v, r = rc.r;
+    const int64_t deg = rc.deg;
     if (v < 0 || (int64_t)v >= a.n_nodes || deg == 0) return;
     if (a.utab && (a.rslot[r] < 0 || (int32_t)a.utab[a.rslot[r]].y != r)) return;  // another row samples this node
-    const int64_t start = (int64_t)(uint32_t)m.x | ((int64_t)m.y << 32);
-    const int64_t out0 = a.bindptr[r];
+    const int64_t start = (int64_t)(uint32_t)rc.start_lo | ((int64_t)rc.start_hi << 32);
+    const int64_t out0 = rc.out0;
     uint32_t* tab = a.pos_of + (int64_t)(a.K == 1 ? 0 : find_sub(pre, a.K, r)) * a.n_nodes;
     if (deg <= a.fanout) {  // full node: every neighbour, in row order
         for (int64_t t = gl; t < deg; t += W) emit_edge(a, tab, out0 + t, a.indices[start + t]);
@@ -569,21 +623,21 @@ __device__ void sample_row(const HopArgs& a, int32_t r, const int32_t* pre, uint
 // with per-group predicates, so the groups stay converged: diverged groups
 // would take turns.  A group whose pool overflows, keeps fewer than f keys or
 // holds equal keys finishes alone (rare).
-__device__ void sample_rows_x4(const HopArgs& a, int32_t r, bool valid, const int32_t* pre, uint32_t k0, uint32_t k1,
-                               const Pool& p, unsigned gmask, int gl) {
+__device__ void sample_rows_x4(const HopArgs& a, const BinRec& rc, bool valid, const int32_t* pre, uint32_t k0,
+                               uint32_t k1, const Pool& p, unsigned gmask, int gl) {
     const int f = a.fanout;
     int32_t v = 0;
     uint32_t deg = 0;
     int64_t start = 0, out0 = 0;
     uint32_t* tab = a.pos_of;
     if (valid) {
-        const int4 m = a.rmeta[r];
-        v = m.w;
-        deg = (uint32_t)m.z;
+        const int32_t r = rc.r;
+        v = rc.v;
+        deg = (uint32_t)rc.deg;
         valid = v >= 0 && (int64_t)v < a.n_nodes && (int64_t)deg > f;
         if (valid && a.utab && (a.rslot[r] < 0 || (int32_t)a.utab[a.rslot[r]].y != r)) valid = false;
-        start = (int64_t)(uint32_t)m.x | ((int64_t)m.y << 32);
-        out0 = a.bindptr[r];
+        start = (int64_t)(uint32_t)rc.start_lo | ((int64_t)rc.start_hi << 32);
+        out0 = rc.out0;
         tab = a.pos_of + (int64_t)(a.K == 1 ? 0 : find_sub(pre, a.K, r)) * a.n_nodes;
     }
     const uint32_t tau = valid ? threshold_for(a.lambda_num, deg) : 0u;
@@ -640,15 +694,14 @@ __device__ void sample_rows_x4(const HopArgs& a, int32_t r, bool valid, const in
 
 // A random row longer than 4096 by the whole block (the same steps as
 // sample_random_row, with 256 threads and the block's pool).
-__device__ void sample_big_row(const HopArgs& a, int32_t r, const int32_t* pre, uint32_t k0, uint32_t k1,
+__device__ void sample_big_row(const HopArgs& a, const BinRec& rc, const int32_t* pre, uint32_t k0, uint32_t k1,
                                const Pool& p) {
-    const int4 m = a.rmeta[r];
-    const int32_t v = m.w;
-    const int64_t deg = m.z;
+    const int32_t v = rc.v, r = rc.r;
+    const int64_t deg = rc.deg;
     if (v < 0 || (int64_t)v >= a.n_nodes || deg <= a.fanout) return;
     if (a.utab && (a.rslot[r] < 0 || (int32_t)a.utab[a.rslot[r]].y != r)) return;
-    const int64_t start = (int64_t)(uint32_t)m.x | ((int64_t)m.y << 32);
-    const int64_t out0 = a.bindptr[r];
+    const int64_t start = (int64_t)(uint32_t)rc.start_lo | ((int64_t)rc.start_hi << 32);
+    const int64_t out0 = rc.out0;
     uint32_t* tab = a.pos_of + (int64_t)(a.K == 1 ? 0 : find_sub(pre, a.K, r)) * a.n_nodes;
     const int f = a.fanout;
     uint32_t tau = threshold_for(a.lambda_num, deg);
@@ -673,10 +726,11 @@ __device__ void sample_big_row(const HopArgs& a, int32_t r, const int32_t* pre, 
 }
 
 // Rows by bin, largest first, handed out by counters so that no SM is left
-// with a long tail: blocks take the rows of bin 3 one at a time, then warps
-// take units (a bin 2 row; four bin 1 rows, one per 8-lane group; or sixteen
-// full rows).  The grid is at most what fits on the GPU at once.
-__global__ void __launch_bounds__(kNT) k_sample(HopArgs a) {
+// with a long tail: blocks take the rows of bins 7, 6 and 5 one at a time,
+// then warps take units (a row of bins 4, 3 or 2; four bin 1 rows, one per
+// 8-lane group; or sixteen full rows).  The grid is at most what fits on the
+// GPU at once.
+__global__ void __launch_bounds__(kNT, 4) k_sample(HopArgs a) {
     pdl_start();
     __shared__ int32_t pre[SG_MAX_SUB + 1];
     __shared__ __align__(16) uint32_t s_key[kBlockPool];
@@ -692,19 +746,28 @@ __global__ void __launch_bounds__(kNT) k_sample(HopArgs a) {
         k1 = (uint32_t)(sd >> 32);
     }
     // the counters start at all-ones, so a count is the word + 1
-    const int64_t n0 = (uint32_t)(a.ctr[2] + 1u), n1 = (uint32_t)(a.ctr[3] + 1u), n2 = (uint32_t)(a.ctr[4] + 1u),
-                  n3 = (uint32_t)(a.ctr[5] + 1u);
+    // bin sizes (row counts fit in 32 bits); b7, b76 and bblk are prefixes of
+    // the block bins in work order, w4, w43 and u2 those of the warp bins
+    const int32_t n0 = (int32_t)(a.ctr[2] + 1u), n1 = (int32_t)(a.ctr[3] + 1u);
+    const int32_t b7 = (int32_t)(a.ctr[9] + 1u), b76 = b7 + (int32_t)(a.ctr[8] + 1u), bblk = b76 + (int32_t)(a.ctr[7] + 1u);
+    const int32_t w4 = (int32_t)(a.ctr[6] + 1u), w43 = w4 + (int32_t)(a.ctr[5] + 1u), u2 = w43 + (int32_t)(a.ctr[4] + 1u);
     const Pool bpool{s_key, s_pos, s_sel, &s_n[0], kBlockPool};
     for (;;) {
-        if (threadIdx.x == 0) s_item = (int)(atomicAdd(a.ctr + 6, 1u) + 1u);
+        if (threadIdx.x == 0) s_item = (int)(atomicAdd(a.ctr + 10, 1u) + 1u);
         __syncthreads();
         const int64_t i = s_item;
         __syncthreads();
-        if (i >= n3) break;
-        sample_big_row(a, a.bins[3 * a.bin_stride + i], pre, k0, k1, bpool);
+        if (i >= bblk) break;
+        const BinRec* slot = i < b7 ? bin_slot(a, 7, i) : (i < b76 ? bin_slot(a, 6, i - b7) : bin_slot(a, 5, i - b76));
+        sample_big_row(a, load_rec(slot), pre, k0, k1, bpool);
     }
-    const int64_t u2 = n2, u1 = (n1 + 3) / 4, u0 = (n0 + 15) / 16;
-    const int64_t units = u2 + u1 + u0;
+    // units: the warp rows of bins 4, 3, 2 (u2 of them), then four bin 1 rows
+    // a unit, then sixteen full rows a unit
+    const int32_t u1 = (n1 + 3) / 4, u0 = (n0 + 15) / 16;
+    const int32_t units = u2 + u1 + u0;
+    auto warp_slot = [&](int32_t uu) {
+        return uu < w4 ? bin_slot(a, 4, uu) : (uu < w43 ? bin_slot(a, 3, uu - w4) : bin_slot(a, 2, uu - w43));
+    };
     const unsigned lane = lane_id();
     const int wib = threadIdx.x >> 5;
     const int g = (int)(lane >> 3), gl = (int)(lane & 7);
@@ -712,24 +775,43 @@ __global__ void __launch_bounds__(kNT) k_sample(HopArgs a) {
     const Pool wpool{s_key + wib * kWarpPool, s_pos + wib * kWarpPool, s_sel + wib * kWarpSel, &s_n[4 * wib], kWarpPool};
     const Pool gpool{s_key + wib * kWarpPool + g * kGroupPool, s_pos + wib * kWarpPool + g * kGroupPool,
                      s_sel + wib * kWarpSel + g * kGroupSel, &s_n[4 * wib + g], kGroupPool};
+    // The unit counter runs two units ahead, and the records of the next unit
+    // (this lane's row of a bin 2 or bin 1 unit) load while this one is
+    // processed, so a unit starts without waiting for its row metadata.
+    auto unit_rec = [&](int32_t uu, BinRec& rc) {
+        rc.v = -1;
+        if (uu < u2) {
+            rc = load_rec(warp_slot(uu));
+        } else if (uu < u2 + u1) {
+            const int32_t i = (uu - u2) * 4 + g;
+            if (i < n1) rc = load_rec(bin_slot(a, 1, i));
+        }
+    };
     uint32_t nxt = 0;
-    if (lane == 0) nxt = atomicAdd(a.ctr + 7, 1u) + 1u;
-    int64_t u = __shfl_sync(0xffffffffu, nxt, 0);
+    if (lane == 0) nxt = atomicAdd(a.ctr + 11, 1u) + 1u;
+    int32_t u = (int32_t)__shfl_sync(0xffffffffu, nxt, 0);
+    if (lane == 0 && u < units) nxt = atomicAdd(a.ctr + 11, 1u) + 1u;
+    BinRec rec;
+    unit_rec(u, rec);
     while (u < units) {
-        if (lane == 0) nxt = atomicAdd(a.ctr + 7, 1u) + 1u;  // the next unit, fetched ahead
+        const int32_t un = (int32_t)__shfl_sync(0xffffffffu, nxt, 0);
+        if (lane == 0 && un < units) nxt = atomicAdd(a.ctr + 11, 1u) + 1u;  // the unit after next
+        BinRec recn;
+        unit_rec(un, recn);
         if (u < u2) {
-            sample_row<32>(a, a.bins[2 * a.bin_stride + u], pre, k0, k1, wpool, 0xffffffffu, (int)lane);
+            sample_row<32>(a, rec, pre, k0, k1, wpool, 0xffffffffu, (int)lane);
         } else if (u < u2 + u1) {
-            const int64_t i = (u - u2) * 4 + g;
-            sample_rows_x4(a, i < n1 ? a.bins[a.bin_stride + i] : 0, i < n1, pre, k0, k1, gpool, gmask, gl);
+            const int32_t i = (u - u2) * 4 + g;
+            sample_rows_x4(a, rec, i < n1, pre, k0, k1, gpool, gmask, gl);
         } else {
             for (int t = 0; t < 4; ++t) {
-                const int64_t i = (u - u2 - u1) * 16 + 4 * t + g;
-                if (i < n0) sample_row<8>(a, a.bins[i], pre, k0, k1, gpool, gmask, gl);
+                const int32_t i = (u - u2 - u1) * 16 + 4 * t + g;
+                if (i < n0) sample_row<8>(a, load_rec(bin_slot(a, 0, i)), pre, k0, k1, gpool, gmask, gl);
             }
         }
         __syncwarp();
-        u = __shfl_sync(0xffffffffu, nxt, 0);
+        u = un;
+        rec = recn;
     }
 }
 
@@ -764,12 +846,13 @@ __global__ void __launch_bounds__(kNT) k_relabel(HopArgs a) {
     __shared__ int32_t red[kNT / 32 + 1];
     __shared__ int32_t s_tile, s_excl;
     const int K = a.K;
+    for (int k = threadIdx.x; k <= K; k += kNT) ep[k] = a.epre[k];
+    __syncthreads();
     if (threadIdx.x == 0) {
         int32_t acc = 0;
         for (int k = 0; k <= K; ++k) {
-            ep[k] = a.epre[k];
             tpre[k] = acc;
-            if (k < K) acc += (a.epre[k + 1] - a.epre[k] + kTile - 1) / kTile;
+            if (k < K) acc += (ep[k + 1] - ep[k] + kTile - 1) / kTile;
         }
         tpre[K] = acc;
     }
@@ -789,6 +872,7 @@ __global__ void __launch_bounds__(kNT) k_relabel(HopArgs a) {
         const int t = s_tile;
         if (t >= n_tiles) break;
         const int k = find_sub(tpre, K, t);
+        const int32_t n_prev = a.counts[a.L.sub_n(k, a.h - 1)];  // needed after the scan; loaded now
         const int64_t e_end = ep[k + 1];
         const int64_t e0 = ep[k] + (int64_t)(t - tpre[k]) * kTile + (int64_t)threadIdx.x * 4;
         bool fl[4];
@@ -816,7 +900,6 @@ __global__ void __launch_bounds__(kNT) k_relabel(HopArgs a) {
             if (late && threadIdx.x == 0) dev_err(ERR_TIMEOUT);
         }
         __syncthreads();
-        const int32_t n_prev = a.counts[a.L.sub_n(k, a.h - 1)];
         int32_t rank = s_excl + ex;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -919,7 +1002,7 @@ struct Plan {
     // the rest is scratch
     size_t o_pos, o_zero, o_rstat[SG_MAX_HOPS], o_estat[SG_MAX_HOPS], o_ctr, o_rest;
     size_t o_utab[SG_MAX_HOPS], o_scratch;
-    size_t o_ustr, o_rmeta, o_rslot, o_bins, o_enbr[2], o_epre, total;
+    size_t o_ustr, o_rslot, o_bins, o_enbr[2], o_epre, total;
 };
 
 sg_status make_plan(const sg_graph* g, int32_t n_seeds, const int32_t* h_bptr, int32_t n_sub, const int32_t* h_fan,
@@ -984,7 +1067,7 @@ sg_status make_plan(const sg_graph* g, int32_t n_seeds, const int32_t* h_bptr, i
         o = align256(o + (size_t)(p->eb_tot[h] / kTile + K + 2) * 8);
     }
     p->o_ctr = o;
-    o = align256(o + (size_t)n_hops * 8 * 4);
+    o = align256(o + (size_t)n_hops * kCtrWords * 4);
     p->o_rest = o;
     for (int h = 0; h < n_hops; ++h) {
         p->logU[h] = K > 1 ? pow2_log(2 * p->nb_tot[h]) : 0;
@@ -994,12 +1077,10 @@ sg_status make_plan(const sg_graph* g, int32_t n_seeds, const int32_t* h_bptr, i
     p->o_scratch = o;
     p->o_ustr = o;
     o = align256(o + (K > 1 ? (size_t)K * (size_t)p->capU * 4 : 0));
-    p->o_rmeta = o;
-    o = align256(o + (size_t)p->nb_max * 16);
     p->o_rslot = o;
     o = align256(o + (K > 1 ? (size_t)p->nb_max * 4 : 0));
     p->o_bins = o;
-    o = align256(o + 4 * (size_t)p->nb_max * 4);
+    o = align256(o + (size_t)(kBins / 2) * (size_t)p->nb_max * sizeof(BinRec));
     for (int i = 0; i < 2; ++i) {  // edge arrays alternate between hops (k_rows maps the previous hop's)
         p->o_enbr[i] = o;
         o = align256(o + (size_t)p->eb_max * 4);
@@ -1097,9 +1178,8 @@ extern "C" sg_status sg_sampler_run(const sg_graph* g, const int32_t* d_seeds, i
     a.counts = out->counts;
     a.ustr = K > 1 ? (int32_t*)(ws + p.o_ustr) : out->unique;
     a.pos_of = (uint32_t*)(ws + p.o_pos);
-    a.rmeta = (int4*)(ws + p.o_rmeta);
-    a.bins = (int32_t*)(ws + p.o_bins);
-    a.bin_stride = p.nb_max;
+    a.brec = (BinRec*)(ws + p.o_bins);
+    a.bin_cap = p.nb_max;
     a.rslot = K > 1 ? (int32_t*)(ws + p.o_rslot) : nullptr;
     int32_t* epre_all = (int32_t*)(ws + p.o_epre);
 
@@ -1119,7 +1199,7 @@ extern "C" sg_status sg_sampler_run(const sg_graph* g, const int32_t* d_seeds, i
         a.bindptr = out->indptr[h - 1];
         a.epre = epre_all + (size_t)h * (SG_MAX_SUB + 1);
         a.enbr = (int32_t*)(ws + p.o_enbr[cur]);
-        a.ctr = (uint32_t*)(ws + p.o_ctr) + (size_t)(h - 1) * 8;
+        a.ctr = (uint32_t*)(ws + p.o_ctr) + (size_t)(h - 1) * kCtrWords;
         a.row_status = (unsigned long long*)(ws + p.o_rstat[h - 1]);
         a.edge_status = (unsigned long long*)(ws + p.o_estat[h - 1]);
         a.utab = K > 1 ? (uint2*)(ws + p.o_utab[h - 1]) : nullptr;
