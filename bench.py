@@ -167,6 +167,26 @@ class Workload:
         return self.batches.seeds(batch)
 
 
+def replica_batches(rank: int, world: int, n: int):
+    """Batch indices of one rank: rank, rank + world, ...; the ranks' lists
+    are disjoint and together are 0 .. n * world - 1."""
+    return [rank + world * i for i in range(n)]
+
+
+def combine_ranks(torch, elapsed_ms: float, counters, device):
+    """Whole-job figures of a replica run: the slowest rank's time and the
+    sums of the integer counters over ranks (unchanged for one rank)."""
+    counters = [int(c) for c in counters]
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return elapsed_ms, counters
+    import torch.distributed as dist
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    c = torch.tensor(counters, dtype=torch.int64, device=device)
+    dist.all_reduce(c)
+    return float(t.item()), [int(x) for x in c.tolist()]
+
+
 def kernels_per_step(H: int, n_sub: int) -> int:
     """Kernels one step launches: sampler 3 per hop (+1 per hop for a
     super-batch) + 2, transposes 5, gather 1, forward 1 per hop, backward 1
@@ -218,7 +238,7 @@ def run_ours(args, rank, world, local):
 
     # batches of this rank (replicas: disjoint batch indices per rank)
     n_batches = args.warmup + args.steps
-    bidx = [rank + world * i for i in range(n_batches)]
+    bidx = replica_batches(rank, world, n_batches)
     seeds_host = np.stack([W.seeds(b) for b in bidx]).astype(np.int32)
     seeds_pool = torch.from_numpy(seeds_host).to(dev)
     hseed_pool = torch.tensor([w.sampler_seed(b) for b in bidx], dtype=torch.int64, device=dev)
@@ -311,11 +331,6 @@ def run_ours(args, rank, world, local):
             one_step_staged(args.warmup + s_, ev[s_])
     torch.cuda.synchronize(dev)
     sg.sg_stream_check(stream)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
     stage_ms = {name: 0.0 for name, _ in graphs}
     for s_ in range(args.steps):
         for j, (name, _) in enumerate(graphs):
@@ -324,13 +339,7 @@ def run_ours(args, rank, world, local):
     nodes = counts[:, : H + 1].astype(np.int64)
     edges = counts[:, H + 1: 2 * H + 1].astype(np.int64)
     total_edges = int(edges.sum())
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_edges, hits, misses], dtype=torch.int64, device=dev)
-        dist.all_reduce(t)
-        total_edges_all = int(t[0].item())
-    else:
-        total_edges_all = total_edges
+    elapsed_ms, (total_edges_all, _, _) = combine_ranks(torch, elapsed_ms, [total_edges, hits, misses], dev)
     value = total_edges_all / (elapsed_ms / 1e3)
 
     # ---- roofline bookkeeping (outside the timed region) ----
