@@ -297,6 +297,236 @@ __global__ void __launch_bounds__(kNT, DT == DT_F32 ? 3 : 2)
     }
 }
 
+// ------------------------------------------------------- copy-engine SpMM
+// The same product with the feature rows brought into shared memory by the
+// copy engine: one cp.async.bulk per edge moves a whole source row and
+// completes on the mbarrier of its slot.  A warp owns a contiguous range of
+// rows, so its edges are one run of the CSR, and walks the run in stages of
+// C edges.  A ring of kTmaStages stage buffers keeps kTmaStages - 1 stages of
+// copies in flight ahead of the one being summed (columns load one stage
+// before their copies are issued); lane v adds up vectors v, v + 32, ... of
+// the current row and rows end where the edge index reaches the next row
+// pointer (32 row pointers in a register, the next 32 already loading).  The
+// parity each slot's mbarrier is next waited on is kept in a bitmask (the same
+// in every lane), so stages that leave slots unused keep no stale phase.
+// Every wait on an mbarrier is bounded: a wait that gives up sets the error
+// word (SG_ERR_TIMEOUT), and the warp then waits (bounded) for its copies
+// still in flight before it exits.
+constexpr int kTmaWarps = 4;        // warps per block
+constexpr int kTmaStages = 6;       // stage buffers per warp
+constexpr int kTmaStageMax = 8;     // edges per stage at most (slots per warp <= 48)
+constexpr int kTmaSpins = 1 << 16;  // polls of one mbarrier before giving up
+constexpr int kTmaRowsMax = 4096;   // forward blocks up to this many rows take this path
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+// true once the phase of the given parity has completed; false after
+// kTmaSpins polls
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    for (int i = 0; i < kTmaSpins; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(done)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+// bytes (a multiple of 16) from 16-byte aligned global src to shared dst,
+// completing on bar
+__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// Shared memory of one warp: kTmaStages * C slots of row_bytes, then as many
+// mbarriers, weights and validity flags.
+__host__ __device__ __forceinline__ size_t tma_warp_bytes(int C, int row_bytes) {
+    return (size_t)kTmaStages * C * row_bytes + (size_t)kTmaStages * C * (8 + 4 + 4);
+}
+
+template <int VPL, int DT, bool WEIGHTED>
+__global__ void __launch_bounds__(32 * kTmaWarps) k_spmm_tma(
+    const int32_t* __restrict__ ptr, const int32_t* __restrict__ col, const float* __restrict__ w, int32_t n_rows_cap,
+    const int32_t* __restrict__ d_rows, int32_t n_cols_cap, const int32_t* __restrict__ d_cols,
+    const uint4* __restrict__ x, int32_t row_vecs, int32_t C, void* __restrict__ y) {
+    pdl_start();
+    constexpr int EPV = Elems<DT>::n;
+    constexpr int NS = kTmaStages;
+    extern __shared__ __align__(16) unsigned char tsm[];
+    const int64_t n_rows = d_rows ? (int64_t)min(*d_rows, n_rows_cap) : n_rows_cap;
+    const int32_t n_cols = d_cols ? min(*d_cols, n_cols_cap) : n_cols_cap;
+    const int lane = (int)lane_id();
+    const int wib = threadIdx.x >> 5;
+    const int row_bytes = row_vecs * 16;
+    const int S = NS * C;  // slots
+    unsigned char* base = tsm + (size_t)wib * tma_warp_bytes(C, row_bytes);
+    uint4* slots = (uint4*)base;
+    uint64_t* bars = (uint64_t*)(base + (size_t)S * row_bytes);
+    float* sw = (float*)(bars + S);
+    int32_t* sval = (int32_t*)(sw + S);
+    for (int i = lane; i < S; i += 32) mbar_init(bars + i);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    __syncwarp();
+
+    const int64_t n_warps = (int64_t)gridDim.x * kTmaWarps;
+    const int64_t per = (n_rows + n_warps - 1) / n_warps;
+    const int64_t ra = min(((int64_t)blockIdx.x * kTmaWarps + wib) * per, n_rows);
+    const int64_t rb = min(ra + per, n_rows);
+    if (ra >= rb) return;
+    const int32_t E0 = ptr[ra], E1 = ptr[rb];
+    const int32_t n_st = (E1 - E0 + C - 1) / C;
+    uint64_t phase = 0;    // bit i: parity of slot i's next completion
+    uint64_t pending = 0;  // bit i: a copy into slot i was issued and not yet waited on
+
+    // columns (and weights) of stage s are held by lanes k < C (edge E0 + s C + k)
+    auto load_col = [&](int32_t s, int32_t& c, float& wt) {
+        const int32_t e = E0 + s * C + lane;
+        c = -1;
+        wt = 0.f;
+        if (lane < C && s < n_st && e < E1) {
+            c = __ldg(col + e);
+            if (WEIGHTED) wt = __ldg(w + e);
+        }
+    };
+    auto issue = [&](int32_t s, int32_t c, float wt) {
+        if (s >= n_st) return;
+        const int grp = s % NS;
+        const int n_e = min(C, E1 - (E0 + s * C));
+        pending |= ((1ull << n_e) - 1ull) << (grp * C);
+        if (lane < n_e) {
+            const int slot = grp * C + lane;
+            uint64_t* bar = bars + slot;
+            if (c >= 0 && c < n_cols) {
+                sval[slot] = 1;
+                if (WEIGHTED) sw[slot] = wt;
+                asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // earlier reads of the slot first
+                mbar_expect_tx(bar, (uint32_t)row_bytes);
+                bulk_copy(slots + (size_t)slot * row_vecs, x + (int64_t)c * row_vecs, (uint32_t)row_bytes, bar);
+            } else {
+                dev_err(ERR_INDEX);
+                sval[slot] = 0;
+                mbar_arrive(bar);
+            }
+        }
+    };
+    // stages 0 .. NS-2 (at most 40 edges): their columns in two loads a lane
+    {
+        const int span = (NS - 1) * C;
+        int32_t ca = -1, cb = -1;
+        float wa = 0.f, wb = 0.f;
+        if (lane < span && E0 + lane < E1) {
+            ca = __ldg(col + E0 + lane);
+            if (WEIGHTED) wa = __ldg(w + E0 + lane);
+        }
+        if (lane + 32 < span && E0 + lane + 32 < E1) {
+            cb = __ldg(col + E0 + lane + 32);
+            if (WEIGHTED) wb = __ldg(w + E0 + lane + 32);
+        }
+        for (int s = 0; s < NS - 1; ++s) {
+            const int src = s * C + lane;  // this lane's edge of stage s, as a position of the first span
+            const int32_t c_lo = __shfl_sync(0xffffffffu, ca, src & 31), c_hi = __shfl_sync(0xffffffffu, cb, src & 31);
+            const float w_lo = __shfl_sync(0xffffffffu, wa, src & 31), w_hi = __shfl_sync(0xffffffffu, wb, src & 31);
+            issue(s, src < 32 ? c_lo : c_hi, src < 32 ? w_lo : w_hi);
+        }
+    }
+    int32_t cn;
+    float wn;
+    load_col(NS - 1, cn, wn);
+
+    // row ends: lane i of pcur holds ptr[pb + i]; pnext the next 32
+    int64_t pb = ra + 1;
+    int32_t pcur = pb + lane <= rb ? ptr[pb + lane] : E1;
+    int32_t pnext = pb + 32 + lane <= rb ? ptr[pb + 32 + lane] : E1;
+    int64_t r = ra;
+    int32_t rstart = E0;
+    int32_t rend = __shfl_sync(0xffffffffu, pcur, 0);
+    float acc[VPL][EPV];
+#pragma unroll
+    for (int p = 0; p < VPL; ++p)
+#pragma unroll
+        for (int q = 0; q < EPV; ++q) acc[p][q] = 0.f;
+    auto finish_row = [&]() {
+        const int32_t cnt = rend - rstart;
+        const float rc = WEIGHTED ? 1.f : (cnt > 0 ? __frcp_rn((float)cnt) : 0.f);
+#pragma unroll
+        for (int p = 0; p < VPL; ++p) {
+            const int vi = lane + 32 * p;
+            if (vi < row_vecs) {
+                float o[EPV];
+#pragma unroll
+                for (int q = 0; q < EPV; ++q) o[q] = WEIGHTED ? acc[p][q] : acc[p][q] * rc;
+                store_vec<DT>(y, r, row_vecs, vi, o);
+            }
+#pragma unroll
+            for (int q = 0; q < EPV; ++q) acc[p][q] = 0.f;
+        }
+        ++r;
+        rstart = rend;
+        if (r + 1 - pb == 32) {
+            pb += 32;
+            pcur = pnext;
+            pnext = pb + 32 + lane <= rb ? ptr[pb + 32 + lane] : E1;
+        }
+        rend = r < rb ? __shfl_sync(0xffffffffu, pcur, (int)((r + 1 - pb) & 31)) : E1;
+    };
+
+    bool failed = false;
+    for (int32_t st = 0; st < n_st; ++st) {
+        issue(st + NS - 1, cn, wn);  // into the buffer that stage st - 1 has freed
+        load_col(st + NS, cn, wn);
+        const int grp = st % NS;
+        const int32_t e0 = E0 + st * C;
+        const int n_e = min(C, E1 - e0);
+        bool ok = true;
+        for (int k = 0; k < n_e; ++k) ok &= mbar_wait(bars + grp * C + k, (uint32_t)((phase >> (grp * C + k)) & 1ull));
+        if (!__all_sync(0xffffffffu, ok)) {  // (this stage's slots stay pending for the drain below)
+            if (lane == 0) dev_err(ERR_TIMEOUT);
+            failed = true;
+            break;
+        }
+        const uint64_t used = ((1ull << n_e) - 1ull) << (grp * C);
+        phase ^= used;
+        pending &= ~used;
+        for (int k = 0; k < n_e; ++k) {
+            while (e0 + k >= rend) finish_row();
+            const int slot = grp * C + k;
+            if (!sval[slot]) continue;
+            const float wt = WEIGHTED ? sw[slot] : 1.f;
+            const uint4* sb = slots + (size_t)slot * row_vecs;
+#pragma unroll
+            for (int p = 0; p < VPL; ++p) {
+                const int vi = lane + 32 * p;
+                if (vi < row_vecs) {
+                    const uint4 v = sb[vi];
+                    if (WEIGHTED) fma_vec<DT>(acc[p], v, wt);
+                    else add_vec<DT>(acc[p], v);
+                }
+            }
+        }
+        __syncwarp();
+    }
+    if (failed) {  // let this warp's copies in flight land before it exits (bounded)
+        for (int i = lane; i < S; i += 32)
+            if ((pending >> i) & 1ull) (void)mbar_wait(bars + i, (uint32_t)((phase >> i) & 1ull));
+        return;
+    }
+    while (r < rb) finish_row();
+}
+
 // Element-wise variant for rows whose byte size is not a multiple of 16 or is
 // larger than 4 KB: a warp per row, lanes over the elements.
 __global__ void __launch_bounds__(kNT) k_spmm_scalar(const int32_t* __restrict__ ptr, const int32_t* __restrict__ col,
@@ -569,6 +799,44 @@ sg_status launch_vec(int lpr, int vpl, int blocks, cudaStream_t s, const int32_t
     return SG_OK;
 }
 
+template <int VPL, int DT, bool WGT>
+sg_status launch_tma_t(int64_t n_rows_cap, size_t smem, cudaStream_t s, const int32_t* ptr, const int32_t* col,
+                       const float* w, int32_t nr, const int32_t* dr, int32_t nc, const int32_t* dc, const void* x,
+                       int32_t rv, int32_t C, void* y) {
+    static size_t smem_set = 0;  // the kernel's dynamic shared-memory limit, raised once per size
+    if (smem > smem_set) {
+        SG_CUDA(cudaFuncSetAttribute(k_spmm_tma<VPL, DT, WGT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        smem_set = smem;
+    }
+    int per_sm = 0;
+    SG_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_spmm_tma<VPL, DT, WGT>, 32 * kTmaWarps, smem));
+    if (per_sm < 1) return fail(SG_ERR_UNSUPPORTED, "aggregate: rows of %d bytes do not fit the copy-engine path", rv * 16);
+    int64_t blocks = cdiv(n_rows_cap, kTmaWarps);  // a warp per row at most
+    const int64_t cap = (int64_t)per_sm * num_sms();
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    SG_CUDA(launch_pdl(k_spmm_tma<VPL, DT, WGT>, dim3((unsigned)blocks), dim3(32 * kTmaWarps), smem, s, ptr, col, w, nr,
+                       dr, nc, dc, (const uint4*)x, rv, C, y));
+    return SG_OK;
+}
+
+// The copy-engine SpMM for rows of row_vecs (<= 256) 16-byte vectors.
+template <int DT, bool WGT>
+sg_status launch_tma(const int32_t* ptr, const int32_t* col, const float* w, int32_t n_rows_cap,
+                     const int32_t* d_rows, int32_t n_cols_cap, const int32_t* d_cols, const void* x, int32_t row_vecs,
+                     void* y, cudaStream_t s) {
+    const int row_bytes = row_vecs * 16;
+    int C = 4096 / row_bytes;  // edges a stage: about 4 KB of rows, 2..8
+    if (C > kTmaStageMax) C = kTmaStageMax;
+    if (C < 2) C = 2;
+    const size_t smem = (size_t)kTmaWarps * tma_warp_bytes(C, row_bytes);
+    const int vpl = row_vecs <= 32 ? 1 : (row_vecs <= 64 ? 2 : (row_vecs <= 128 ? 4 : 8));
+    if (vpl == 1) return launch_tma_t<1, DT, WGT>(n_rows_cap, smem, s, ptr, col, w, n_rows_cap, d_rows, n_cols_cap, d_cols, x, row_vecs, C, y);
+    if (vpl == 2) return launch_tma_t<2, DT, WGT>(n_rows_cap, smem, s, ptr, col, w, n_rows_cap, d_rows, n_cols_cap, d_cols, x, row_vecs, C, y);
+    if (vpl == 4) return launch_tma_t<4, DT, WGT>(n_rows_cap, smem, s, ptr, col, w, n_rows_cap, d_rows, n_cols_cap, d_cols, x, row_vecs, C, y);
+    return launch_tma_t<8, DT, WGT>(n_rows_cap, smem, s, ptr, col, w, n_rows_cap, d_rows, n_cols_cap, d_cols, x, row_vecs, C, y);
+}
+
 // Runs y = A x for the row-split CSR (ptr, col, w) with n_rows rows.
 sg_status run_spmm(const int32_t* ptr, const int32_t* col, const float* w, int32_t n_rows_cap, const int32_t* d_rows,
                    int32_t n_cols_cap, const int32_t* d_cols, const void* x, int32_t dtype_in, int32_t dim, void* y,
@@ -603,6 +871,15 @@ sg_status run_spmm(const int32_t* ptr, const int32_t* col, const float* w, int32
     } else {
         lpr = 32;
         vpl = row_vecs <= 128 ? 4 : 8;
+    }
+    // forward blocks of few rows (the hop next to the seeds): the copy-engine
+    // path, whose warps keep several stages of whole rows in flight; larger
+    // blocks: the register path (the copy engine moved 400-byte rows at only
+    // ~1.6 TB/s there, against ~3.5 TB/s for k_spmm on the 52K-row hop)
+    if (w == nullptr && n_rows_cap <= kTmaRowsMax) {
+        if (dt == DT_F32) return launch_tma<DT_F32, false>(ptr, col, w, n_rows_cap, d_rows, n_cols_cap, d_cols, x, (int32_t)row_vecs, y, s);
+        if (dt == DT_BF16) return launch_tma<DT_BF16, false>(ptr, col, w, n_rows_cap, d_rows, n_cols_cap, d_cols, x, (int32_t)row_vecs, y, s);
+        return launch_tma<DT_BF16_F32, false>(ptr, col, w, n_rows_cap, d_rows, n_cols_cap, d_cols, x, (int32_t)row_vecs, y, s);
     }
     const bool wgt = w != nullptr;
     int64_t blocks = cdiv((int64_t)n_rows_cap * lpr, kNT);
