@@ -775,9 +775,10 @@ __global__ void __launch_bounds__(kNT, 4) k_sample(HopArgs a) {
     const Pool wpool{s_key + wib * kWarpPool, s_pos + wib * kWarpPool, s_sel + wib * kWarpSel, &s_n[4 * wib], kWarpPool};
     const Pool gpool{s_key + wib * kWarpPool + g * kGroupPool, s_pos + wib * kWarpPool + g * kGroupPool,
                      s_sel + wib * kWarpSel + g * kGroupSel, &s_n[4 * wib + g], kGroupPool};
-    // The unit counter runs two units ahead, and the records of the next unit
-    // (this lane's row of a bin 2 or bin 1 unit) load while this one is
-    // processed, so a unit starts without waiting for its row metadata.
+    // The next unit is reserved while this one runs only when units are
+    // plentiful (more than two per warp left); near the end of the queue a warp
+    // takes its next unit once it is done, so that no unit waits behind a busy
+    // warp while others are idle.
     auto unit_rec = [&](int32_t uu, BinRec& rc) {
         rc.v = -1;
         if (uu < u2) {
@@ -787,17 +788,15 @@ __global__ void __launch_bounds__(kNT, 4) k_sample(HopArgs a) {
             if (i < n1) rc = load_rec(bin_slot(a, 1, i));
         }
     };
+    const int32_t n_warps = (int32_t)(gridDim.x * (kNT / 32));
     uint32_t nxt = 0;
     if (lane == 0) nxt = atomicAdd(a.ctr + 11, 1u) + 1u;
     int32_t u = (int32_t)__shfl_sync(0xffffffffu, nxt, 0);
-    if (lane == 0 && u < units) nxt = atomicAdd(a.ctr + 11, 1u) + 1u;
-    BinRec rec;
-    unit_rec(u, rec);
     while (u < units) {
-        const int32_t un = (int32_t)__shfl_sync(0xffffffffu, nxt, 0);
-        if (lane == 0 && un < units) nxt = atomicAdd(a.ctr + 11, 1u) + 1u;  // the unit after next
-        BinRec recn;
-        unit_rec(un, recn);
+        const bool ahead = u + 2 * n_warps < units;
+        if (ahead && lane == 0) nxt = atomicAdd(a.ctr + 11, 1u) + 1u;
+        BinRec rec;
+        unit_rec(u, rec);
         if (u < u2) {
             sample_row<32>(a, rec, pre, k0, k1, wpool, 0xffffffffu, (int)lane);
         } else if (u < u2 + u1) {
@@ -810,8 +809,8 @@ __global__ void __launch_bounds__(kNT, 4) k_sample(HopArgs a) {
             }
         }
         __syncwarp();
-        u = un;
-        rec = recn;
+        if (!ahead && lane == 0) nxt = atomicAdd(a.ctr + 11, 1u) + 1u;
+        u = (int32_t)__shfl_sync(0xffffffffu, nxt, 0);
     }
 }
 
