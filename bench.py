@@ -189,9 +189,11 @@ def combine_ranks(torch, elapsed_ms: float, counters, device):
 
 def kernels_per_step(H: int, n_sub: int) -> int:
     """Kernels one step launches: sampler 3 per hop (+1 per hop for a
-    super-batch) + 2, transposes 5, gather 1, forward 1 per hop, backward 1
+    super-batch) + 2, transposes 5, gather 1 (2 when one mini-batch of two
+    hops or more is gathered in two parts), forward 1 per hop, backward 1
     per hop."""
-    return (2 + 3 * H + (H if n_sub > 1 else 0)) + 5 + 1 + H + H
+    gathers = 2 if (n_sub == 1 and H >= 2) else 1
+    return (2 + 3 * H + (H if n_sub > 1 else 0)) + 5 + gathers + H + H
 
 
 def run_ours(args, rank, world, local):

@@ -170,20 +170,44 @@ __device__ __forceinline__ void store_row(const float (&acc)[VPL][Elems<DT>::n],
     }
 }
 
-// Rows longer than kLongRow edges among the rows of this warp's groups (group
-// g owns rows g, g + groups, ...), one at a time, each by the whole warp: the
-// warp's 32 / LPR groups take every (32 / LPR)-th chunk of the row and their
-// sums are added in a fixed order (xor shuffles by LPR, 2 LPR, ...).
+// Row r = [rlo, rhi), longer than kLongRow edges, summed by the whole warp:
+// the warp's 32 / LPR groups take every (32 / LPR)-th chunk of the row and
+// their sums are added in a fixed order (xor shuffles by LPR, 2 LPR, ...), so
+// the result does not depend on which warp sums the row.
 template <int LPR, int VPL, int DT, bool WEIGHTED>
-__device__ __forceinline__ void long_rows(const int32_t* __restrict__ ptr, const int32_t* __restrict__ col,
-                                          const float* __restrict__ w, int64_t n_rows, int32_t n_cols,
-                                          const uint4* __restrict__ x, int32_t row_vecs, void* __restrict__ y,
-                                          int64_t gid, int64_t groups) {
+__device__ __forceinline__ void long_row(int64_t r, int32_t rlo, int32_t rhi, const int32_t* __restrict__ col,
+                                         const float* __restrict__ w, int32_t n_cols, const uint4* __restrict__ x,
+                                         int32_t row_vecs, void* __restrict__ y) {
     constexpr int EPV = Elems<DT>::n;
     constexpr int SG = 32 / LPR;
     const unsigned lane = lane_id();
     const int gl = lane % LPR, sg = (int)(lane / LPR);
     const unsigned gmask = LPR == 32 ? 0xffffffffu : (((1u << LPR) - 1u) << (lane - gl));
+    float acc[VPL][EPV];
+#pragma unroll
+    for (int p = 0; p < VPL; ++p)
+#pragma unroll
+        for (int q = 0; q < EPV; ++q) acc[p][q] = 0.f;
+    accumulate_chunks<LPR, VPL, DT, WEIGHTED>(acc, rlo, rhi, sg, SG, col, w, n_cols, x, row_vecs, gmask, gl);
+#pragma unroll
+    for (int d = LPR; d < 32; d <<= 1)
+#pragma unroll
+        for (int p = 0; p < VPL; ++p)
+#pragma unroll
+            for (int q = 0; q < EPV; ++q) acc[p][q] += __shfl_xor_sync(0xffffffffu, acc[p][q], d);
+    if (sg == 0) store_row<LPR, VPL, DT, WEIGHTED>(acc, r, rhi - rlo, y, row_vecs, gl);
+}
+
+// Rows longer than kLongRow edges among the rows of this warp's groups (group
+// g owns rows g, g + groups, ...), found by a pass over their bounds ahead of
+// the other rows and summed one at a time by the whole warp.
+template <int LPR, int VPL, int DT, bool WEIGHTED>
+__device__ __forceinline__ void long_rows(const int32_t* __restrict__ ptr, const int32_t* __restrict__ col,
+                                          const float* __restrict__ w, int64_t n_rows, int32_t n_cols,
+                                          const uint4* __restrict__ x, int32_t row_vecs, void* __restrict__ y,
+                                          int64_t gid, int64_t groups) {
+    const unsigned lane = lane_id();
+    const int gl = lane % LPR, sg = (int)(lane / LPR);
     constexpr int kAhead = 4;  // row bounds of this many rounds are loaded together
     for (int64_t base0 = gid - sg; base0 < n_rows; base0 += kAhead * groups) {
       int32_t lob[kAhead], hib[kAhead];
@@ -206,19 +230,7 @@ __device__ __forceinline__ void long_rows(const int32_t* __restrict__ ptr, const
             const int src = __ffs(longs) - 1;
             longs &= longs - 1;
             const int32_t rlo = __shfl_sync(0xffffffffu, lo, src), rhi = __shfl_sync(0xffffffffu, hi, src);
-            float acc[VPL][EPV];
-#pragma unroll
-            for (int p = 0; p < VPL; ++p)
-#pragma unroll
-                for (int q = 0; q < EPV; ++q) acc[p][q] = 0.f;
-            accumulate_chunks<LPR, VPL, DT, WEIGHTED>(acc, rlo, rhi, sg, SG, col, w, n_cols, x, row_vecs, gmask, gl);
-#pragma unroll
-            for (int d = LPR; d < 32; d <<= 1)
-#pragma unroll
-                for (int p = 0; p < VPL; ++p)
-#pragma unroll
-                    for (int q = 0; q < EPV; ++q) acc[p][q] += __shfl_xor_sync(0xffffffffu, acc[p][q], d);
-            if (sg == 0) store_row<LPR, VPL, DT, WEIGHTED>(acc, base + src / LPR, rhi - rlo, y, row_vecs, gl);
+            long_row<LPR, VPL, DT, WEIGHTED>(base + src / LPR, rlo, rhi, col, w, n_cols, x, row_vecs, y);
         }
       }
     }
@@ -228,17 +240,22 @@ __device__ __forceinline__ void long_rows(const int32_t* __restrict__ ptr, const
 // WEIGHTED = false: w_p = 1 and scale_r = 1 / row length (forward mean).
 // WEIGHTED = true:  w_p = w[p] and scale_r = 1 (backward over the transpose).
 // A warp holds 32 / LPR groups, and group g of the grid owns rows g, g +
-// groups, ...  Rows longer than kLongRow edges (hubs of a transposed block)
-// come first, each by the whole warp of its group: the warp's groups take
-// every (32 / LPR)-th chunk of the row, and their sums are added in a fixed
-// order, so a long row is no longer a serial tail.  Then every group sums its
-// other rows alone, in edge order.  Three blocks fit on an SM for fp32 rows,
-// two for bf16 (twice the accumulators).
+// groups, ...; every group sums its rows alone, in edge order.  Rows longer
+// than kLongRow edges (hubs of a transposed block) are summed by a whole warp
+// instead (long_row), so a long row is no longer a serial tail.  With
+// long_cap > 0 a group that meets one appends it to a list in shared memory
+// (long_cap entries: at least the rows of the block's groups) and the block's
+// warps sum the list once every group is done; with long_cap = 0 a pass over
+// the bounds finds them first.  Three blocks fit on an SM for fp32 rows, two
+// for bf16 (twice the accumulators).
 template <int LPR, int VPL, int DT, bool WEIGHTED>
 __global__ void __launch_bounds__(kNT, DT == DT_F32 ? 3 : 2)
     k_spmm(const int32_t* __restrict__ ptr, const int32_t* __restrict__ col, const float* __restrict__ w,
            int32_t n_rows_cap, const int32_t* __restrict__ d_rows, int32_t n_cols_cap,
-           const int32_t* __restrict__ d_cols, const uint4* __restrict__ x, int32_t row_vecs, void* __restrict__ y) {
+           const int32_t* __restrict__ d_cols, const uint4* __restrict__ x, int32_t row_vecs, void* __restrict__ y,
+           int32_t long_cap) {
+    extern __shared__ int32_t s_long[];  // long_cap row indices
+    __shared__ int32_t s_nlong;
     pdl_start();
     constexpr int EPV = Elems<DT>::n;
     constexpr int SG = 32 / LPR;  // groups per warp
@@ -251,10 +268,16 @@ __global__ void __launch_bounds__(kNT, DT == DT_F32 ? 3 : 2)
     const unsigned gmask = LPR == 32 ? 0xffffffffu : (((1u << LPR) - 1u) << (lane - gl));
     const int64_t groups = (int64_t)gridDim.x * (kNT / LPR);
     const int64_t gid = (blockIdx.x * (int64_t)kNT + threadIdx.x) / LPR;
-    if (SG > 1) long_rows<LPR, VPL, DT, WEIGHTED>(ptr, col, w, n_rows, n_cols, x, row_vecs, y, gid, groups);
-    // the other rows, a group each.  Row bounds are loaded two rows ahead
-    // and the first chunk's columns one row ahead, so a row's feature loads
-    // start without waiting for its indices.
+    const bool defer = SG > 1 && long_cap > 0;  // the same in every thread
+    if (defer) {
+        if (threadIdx.x == 0) s_nlong = 0;
+        __syncthreads();
+    } else if (SG > 1) {
+        long_rows<LPR, VPL, DT, WEIGHTED>(ptr, col, w, n_rows, n_cols, x, row_vecs, y, gid, groups);
+    }
+    // the rows of this group.  Row bounds are loaded two rows ahead and the
+    // first chunk's columns one row ahead, so a row's feature loads start
+    // without waiting for its indices.
     int64_t r = gid;
     int32_t lo1 = 0, hi1 = 0, lo2 = 0, hi2 = 0;  // bounds of rows r and r + groups
     if (r < n_rows) {
@@ -286,7 +309,14 @@ __global__ void __launch_bounds__(kNT, DT == DT_F32 ? 3 : 2)
             lo2 = ptr[r + 2 * groups];
             hi2 = ptr[r + 2 * groups + 1];
         }
-        if (SG > 1 && hi - lo > kLongRow) continue;
+        if (SG > 1 && hi - lo > kLongRow) {
+            if (defer && gl == 0) {
+                const int32_t k = atomicAdd(&s_nlong, 1);
+                if (k < long_cap) s_long[k] = (int32_t)r;
+                else dev_err(ERR_CAPACITY);
+            }
+            continue;
+        }
         float acc[VPL][EPV];
 #pragma unroll
         for (int p = 0; p < VPL; ++p)
@@ -294,6 +324,14 @@ __global__ void __launch_bounds__(kNT, DT == DT_F32 ? 3 : 2)
             for (int q = 0; q < EPV; ++q) acc[p][q] = 0.f;
         accumulate_chunks<LPR, VPL, DT, WEIGHTED>(acc, lo, hi, 0, 1, col, w, n_cols, x, row_vecs, gmask, gl, true, fc, fw);
         store_row<LPR, VPL, DT, WEIGHTED>(acc, r, hi - lo, y, row_vecs, gl);
+    }
+    if (defer) {
+        __syncthreads();
+        const int32_t n_long = min(s_nlong, long_cap);
+        for (int32_t i = (int32_t)(threadIdx.x / 32); i < n_long; i += kNT / 32) {
+            const int32_t rr = s_long[i];
+            long_row<LPR, VPL, DT, WEIGHTED>(rr, ptr[rr], ptr[rr + 1], col, w, n_cols, x, row_vecs, y);
+        }
     }
 }
 
@@ -783,20 +821,50 @@ int dt_code(int32_t in, int32_t out) {
     return -1;
 }
 
-template <int DT, bool WGT>
-sg_status launch_vec(int lpr, int vpl, int blocks, cudaStream_t s, const int32_t* ptr, const int32_t* col, const float* w,
-                     int32_t nr, const int32_t* dr, int32_t nc, const int32_t* dc, const void* x, int32_t rv, void* y) {
-#define SG_SPMM(L, V) \
-    SG_CUDA(launch_pdl(k_spmm<L, V, DT, WGT>, dim3(blocks), dim3(kNT), 0, s, ptr, col, w, nr, dr, nc, dc, (const uint4*)x, rv, y))
-    if (lpr == 4 && vpl == 1) SG_SPMM(4, 1);
-    else if (lpr == 4 && vpl == 2) SG_SPMM(4, 2);
-    else if (lpr == 4) SG_SPMM(4, 4);
-    else if (lpr == 8) SG_SPMM(8, 4);
-    else if (lpr == 16) SG_SPMM(16, 4);
-    else if (vpl == 4) SG_SPMM(32, 4);
-    else SG_SPMM(32, 8);
-#undef SG_SPMM
+constexpr int kLongListBytes = 16384;  // shared-memory list of long rows a block, at most
+
+// k_spmm with LPR = L, VPL = V, no more groups than rows.  Forward: a grid
+// of what fits on the GPU at once, and the long-row list when the rows of a
+// block's groups fit kLongListBytes.  Backward (weighted, the transposed
+// blocks, whose hubs make long rows common): up to 8 blocks an SM in waves
+// and the pass over the bounds, which start the long rows first (measured
+// faster there: a list summed at the end of a block leaves a tail).
+template <int L, int V, int DT, bool WGT>
+sg_status launch_spmm_lv(cudaStream_t s, const int32_t* ptr, const int32_t* col, const float* w, int32_t nr,
+                         const int32_t* dr, int32_t nc, const int32_t* dc, const void* x, int32_t rv, void* y) {
+    static int per_sm = 0;  // resident blocks an SM with the largest list (occupancy calculator, once)
+    if (per_sm == 0) {
+        int p = 0;
+        SG_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&p, k_spmm<L, V, DT, WGT>, kNT, kLongListBytes));
+        per_sm = p > 0 ? p : 1;
+    }
+    int64_t blocks = (int64_t)(WGT ? 8 : per_sm) * num_sms();
+    const int64_t need = cdiv((int64_t)nr * L, kNT);
+    if (blocks > need) blocks = need;
+    if (blocks < 1) blocks = 1;
+    int32_t long_cap = 0;
+    if (!WGT && L < 32) {
+        const int64_t per_block = kNT / L;  // groups
+        const int64_t cap = per_block * cdiv((int64_t)nr, blocks * per_block);
+        if (cap * (int64_t)sizeof(int32_t) <= kLongListBytes) long_cap = (int32_t)cap;
+    }
+    SG_CUDA(launch_pdl(k_spmm<L, V, DT, WGT>, dim3((unsigned)blocks), dim3(kNT), (size_t)long_cap * sizeof(int32_t), s,
+                       ptr, col, w, nr, dr, nc, dc, (const uint4*)x, rv, y, long_cap));
     return SG_OK;
+}
+
+template <int DT, bool WGT>
+sg_status launch_vec(int lpr, int vpl, cudaStream_t s, const int32_t* ptr, const int32_t* col, const float* w,
+                     int32_t nr, const int32_t* dr, int32_t nc, const int32_t* dc, const void* x, int32_t rv, void* y) {
+#define SG_SPMM(L, V) return launch_spmm_lv<L, V, DT, WGT>(s, ptr, col, w, nr, dr, nc, dc, x, rv, y)
+    if (lpr == 4 && vpl == 1) SG_SPMM(4, 1);
+    if (lpr == 4 && vpl == 2) SG_SPMM(4, 2);
+    if (lpr == 4) SG_SPMM(4, 4);
+    if (lpr == 8) SG_SPMM(8, 4);
+    if (lpr == 16) SG_SPMM(16, 4);
+    if (vpl == 4) SG_SPMM(32, 4);
+    SG_SPMM(32, 8);
+#undef SG_SPMM
 }
 
 template <int VPL, int DT, bool WGT>
@@ -882,15 +950,13 @@ sg_status run_spmm(const int32_t* ptr, const int32_t* col, const float* w, int32
         return launch_tma<DT_BF16_F32, false>(ptr, col, w, n_rows_cap, d_rows, n_cols_cap, d_cols, x, (int32_t)row_vecs, y, s);
     }
     const bool wgt = w != nullptr;
-    int64_t blocks = cdiv((int64_t)n_rows_cap * lpr, kNT);
-    if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
-    if (blocks < 1) blocks = 1;
-    if (dt == DT_F32) return wgt ? launch_vec<DT_F32, true>(lpr, vpl, (int)blocks, s, ptr, col, w, n_rows_cap, d_rows, n_cols_cap, d_cols, x, (int32_t)row_vecs, y)
-                                 : launch_vec<DT_F32, false>(lpr, vpl, (int)blocks, s, ptr, col, w, n_rows_cap, d_rows, n_cols_cap, d_cols, x, (int32_t)row_vecs, y);
-    if (dt == DT_BF16) return wgt ? launch_vec<DT_BF16, true>(lpr, vpl, (int)blocks, s, ptr, col, w, n_rows_cap, d_rows, n_cols_cap, d_cols, x, (int32_t)row_vecs, y)
-                                  : launch_vec<DT_BF16, false>(lpr, vpl, (int)blocks, s, ptr, col, w, n_rows_cap, d_rows, n_cols_cap, d_cols, x, (int32_t)row_vecs, y);
-    return wgt ? launch_vec<DT_BF16_F32, true>(lpr, vpl, (int)blocks, s, ptr, col, w, n_rows_cap, d_rows, n_cols_cap, d_cols, x, (int32_t)row_vecs, y)
-               : launch_vec<DT_BF16_F32, false>(lpr, vpl, (int)blocks, s, ptr, col, w, n_rows_cap, d_rows, n_cols_cap, d_cols, x, (int32_t)row_vecs, y);
+    const int32_t rv = (int32_t)row_vecs;
+    if (dt == DT_F32) return wgt ? launch_vec<DT_F32, true>(lpr, vpl, s, ptr, col, w, n_rows_cap, d_rows, n_cols_cap, d_cols, x, rv, y)
+                                 : launch_vec<DT_F32, false>(lpr, vpl, s, ptr, col, w, n_rows_cap, d_rows, n_cols_cap, d_cols, x, rv, y);
+    if (dt == DT_BF16) return wgt ? launch_vec<DT_BF16, true>(lpr, vpl, s, ptr, col, w, n_rows_cap, d_rows, n_cols_cap, d_cols, x, rv, y)
+                                  : launch_vec<DT_BF16, false>(lpr, vpl, s, ptr, col, w, n_rows_cap, d_rows, n_cols_cap, d_cols, x, rv, y);
+    return wgt ? launch_vec<DT_BF16_F32, true>(lpr, vpl, s, ptr, col, w, n_rows_cap, d_rows, n_cols_cap, d_cols, x, rv, y)
+               : launch_vec<DT_BF16_F32, false>(lpr, vpl, s, ptr, col, w, n_rows_cap, d_rows, n_cols_cap, d_cols, x, rv, y);
 }
 
 size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }

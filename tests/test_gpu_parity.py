@@ -178,6 +178,58 @@ def test_aggregate_bwd_matches_oracle_and_is_deterministic(tin, tout, dim):
     assert_close(as_f64(outs[0]), want, am, TOL_F32 if tin == "f32" else TOL_BF16, "bwd")
 
 
+def _long_row_block(rng, n_dst, n_src):
+    """A block where a fifth of the rows are longer than the per-group limit
+    (17 to 80 edges) and the rest have 0 to 8."""
+    c = rng.integers(0, 9, size=n_dst)
+    hub = rng.random(n_dst) < 0.2
+    c[hub] = rng.integers(17, 81, size=int(hub.sum()))
+    indptr = np.concatenate([[0], np.cumsum(c)]).astype(np.int32)
+    idx = rng.integers(0, n_src, size=int(indptr[-1])).astype(np.int32)
+    return indptr, idx
+
+
+@pytest.mark.parametrize("tin,tout,dim", [("f32", "f32", 100), ("f32", "f32", 256), ("f32", "f32", 16),
+                                          ("bf16", "bf16", 64), ("bf16", "f32", 128)])
+def test_aggregate_long_rows_by_list_and_by_pass_agree(tin, tout, dim):
+    # Rows longer than a group's limit are summed by whole warps.  The forward
+    # finds them through a shared-memory list when the row capacity is small
+    # enough and through a pass over the bounds when it is large (device
+    # counts give the rows): the same sums, bit for bit, and the oracle's.
+    # The backward (always the pass) must not depend on the capacity either.
+    rng = np.random.default_rng(300 + dim)
+    n_dst, n_src, big = 20000, 30000, 8_000_000
+    indptr, idx = _long_row_block(rng, n_dst, n_src)
+    odt = torch.float32 if tout == "f32" else torch.bfloat16
+    tol = TOL_F32 if tin == "f32" else TOL_BF16
+    x = synth.features(n_src, dim, tin, 11)
+    d_ip, d_idx, d_x = dev_i32(indptr), dev_i32(idx), feat_tensor(x, "cuda")
+    dims = torch.tensor([n_dst, n_src], dtype=torch.int32, device="cuda")
+    want, am = oracle.aggregate_fwd(indptr, idx, x)
+    outs = []
+    for cap in (n_dst, big):
+        out = torch.empty((n_dst, dim), dtype=odt, device="cuda")
+        sg.sg_aggregate_fwd(d_ip, d_idx, cap, n_src, dims, d_x, out)
+        sg.sg_stream_check()
+        outs.append(torch_to_np(out))
+    assert np.array_equal(outs[0].view(np.uint8), outs[1].view(np.uint8)), "forward: list and pass differ"
+    assert_close(as_f64(outs[0]), want, am, tol, "fwd")
+    # backward: the transposed rows of popular sources are long
+    g = synth.features(n_dst, dim, tin, 12)
+    want, am = oracle.aggregate_bwd(indptr, idx, n_src, g)
+    d_g = feat_tensor(g, "cuda")
+    outs = []
+    for cap in (n_src, big):
+        ws = sg.aligned_workspace(sg.sg_aggregate_bwd_workspace(n_dst, cap, len(idx)))
+        out = torch.empty((n_src, dim), dtype=odt, device="cuda")
+        sg.sg_aggregate_bwd(d_ip, d_idx, n_dst, cap, len(idx), dims, d_g, out, ws)
+        sg.sg_stream_check()
+        outs.append(torch_to_np(out))
+        del ws
+    assert np.array_equal(outs[0].view(np.uint8), outs[1].view(np.uint8)), "backward: list and pass differ"
+    assert_close(as_f64(outs[0]), want, am, tol, "bwd")
+
+
 def test_aggregate_uses_device_counts():
     rng = np.random.default_rng(9)
     n_dst, n_src, dim = 300, 800, 64
