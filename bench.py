@@ -41,6 +41,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="bound on the CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--depth", type=int, default=4, help="pipelines the overlapped batches rotate through")
     return ap.parse_args()
 
 
@@ -199,7 +200,7 @@ def kernels_per_step(H: int, n_sub: int) -> int:
 def run_ours(args, rank, world, local):
     import torch
     from sampling_gnn_mini_gb300 import binding as sg
-    from sampling_gnn_mini_gb300.pipeline import MiniBatchPipeline
+    from sampling_gnn_mini_gb300.pipeline import MiniBatchPipeline, OverlappedPipeline
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -302,12 +303,33 @@ def run_ours(args, rank, world, local):
             cg.replay()
             events[j + 1].record(stream)
 
+    # the headline: consecutive batches overlapped on two pipelines (batch
+    # i+1 is sampled and gathered while batch i's forward and backward run;
+    # batch i+1's forward still waits for batch i's backward)
+    ov = OverlappedPipeline(G, cache, w.fanouts, w.batch, depth=args.depth, device=dev)
     with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            one_step(i)
+        load_batch(0)
+    for p in ov.pipes:
+        p.set_batch(pipe.seeds[: w.batch].clone(), w.sampler_seed(bidx[0]))
     torch.cuda.synchronize(dev)
-    sg.sg_stream_check(stream)
-    pipe.stats.zero_()
+    ov.capture()
+
+    def ov_inputs(i):
+        def f(p, s):
+            p.seeds[: w.batch].copy_(seeds_pool[i], non_blocking=True)
+            p.d_seed.copy_(hseed_pool[i: i + 1], non_blocking=True)
+        return f
+
+    def ov_after(i):
+        def f(p, s):
+            counts_log[i].copy_(p.buf.counts, non_blocking=True)
+        return f
+
+    for i in range(args.warmup):
+        ov.step(ov_inputs(i), ov_after(i))
+    torch.cuda.synchronize(dev)
+    for s_ in ov.streams:
+        sg.sg_stream_check(s_)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
@@ -316,23 +338,43 @@ def run_ours(args, rank, world, local):
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     torch.cuda.nvtx.range_push("timed")
-    with torch.cuda.stream(stream):
-        t_start.record(stream)
-        for s_ in range(args.steps):
-            one_step(args.warmup + s_)
-        t_end.record(stream)
+    t_start.record(stream)
+    ov.start_after(stream)
+    for s_ in range(args.steps):
+        i = args.warmup + s_
+        ov.step(ov_inputs(i), ov_after(i))
+    ov.wait_all(stream)
+    t_end.record(stream)
     torch.cuda.synchronize(dev)
     torch.cuda.nvtx.range_pop()
     clk = clocks.stop()
     elapsed_ms = t_start.elapsed_time(t_end)
+    for s_ in ov.streams:
+        sg.sg_stream_check(s_)
+    # batch latency: the same batches one at a time (a step graph each)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            one_step(i)
+    torch.cuda.synchronize(dev)
+    l_start = torch.cuda.Event(enable_timing=True)
+    l_end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        l_start.record(stream)
+        for s_ in range(args.steps):
+            one_step(args.warmup + s_)
+        l_end.record(stream)
+    torch.cuda.synchronize(dev)
+    latency_ms = l_start.elapsed_time(l_end) / args.steps
     sg.sg_stream_check(stream)
-    hits, misses = [int(x) for x in pipe.stats.cpu().tolist()]
-    # second timed region: the same batches stage by stage, for the breakdown
+    # the same batches stage by stage, for the breakdown (and the cache hits
+    # of exactly these batches' gathers)
+    pipe.stats.zero_()
     with torch.cuda.stream(stream):
         for s_ in range(args.steps):
             one_step_staged(args.warmup + s_, ev[s_])
     torch.cuda.synchronize(dev)
     sg.sg_stream_check(stream)
+    hits, misses = [int(x) for x in pipe.stats.cpu().tolist()]
     stage_ms = {name: 0.0 for name, _ in graphs}
     for s_ in range(args.steps):
         for j, (name, _) in enumerate(graphs):
@@ -427,14 +469,18 @@ def run_ours(args, rank, world, local):
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (CSR %.0f MB, features %.0f MB); a new batch every step"
                          % ((g.indptr.nbytes + g.indices.nbytes) / 1e6, w.n_nodes * R / 1e6)},
-        "batch_latency_ms": elapsed_ms / args.steps,
+        "batch_latency_ms": latency_ms,
+        "overlap": "%d pipelines in turn: batch i+1 is sampled, transposed and gathered while batch i's forward "
+                   "and backward run; batch i+1's forward waits for batch i's backward. batch_latency_ms is one "
+                   "batch alone (a step graph per batch, batches back to back)" % args.depth,
         "gathered_feature_gbs": n_H.sum() * R / (elapsed_ms / 1e3) / 1e9,
         "gather_kernel_gbs": n_H.sum() * R / t_gather / 1e9,
         "memory_roofline_frac": {k: v["frac"] for k, v in stage_roof.items()},
         "hit_rate": hits / max(1, hits + misses),
         "stage_ms": stage_ms,
-        "stage_note": "per-stage times from a second timed region replaying per-stage graphs in sequence "
-                      "(the headline step overlaps the transposes with gather and forward)",
+        "stage_note": "per-stage times from a third timed region replaying per-stage graphs in sequence, one "
+                      "batch at a time (the headline overlaps batches; within a batch the transposes overlap "
+                      "gather and forward)",
         "stages": stage_roof,
         "roofline": roof,
         "host_link_gbs": link_gbs,
@@ -443,7 +489,7 @@ def run_ours(args, rank, world, local):
         "clocks": clk,
     }
     if rank == 0 and not args.no_e2e:
-        result["e2e"] = measure_e2e(sg, torch, pipe, seeds_host, [w.sampler_seed(b) for b in bidx], dev, args, H, w)
+        result["e2e"] = measure_e2e(sg, torch, ov, seeds_host, [w.sampler_seed(b) for b in bidx], dev, args, H, w)
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
@@ -485,51 +531,58 @@ def measure_hash(sg, torch, dev, stream, n_calls=1 << 30):
     return best
 
 
-def measure_e2e(sg, torch, pipe, seeds_host, hseeds, dev, args, H, w):
+def measure_e2e(sg, torch, ov, seeds_host, hseeds, dev, args, H, w):
     """Same metric through the public API with host buffers: per step the
     seeds go host -> device from pinned memory and the step's result (the
-    seed rows H_0 and the counts) comes back device -> host.  Steps are
-    pipelined as a training loop would run them: step i+1 is enqueued before
-    the host waits for and reads step i's result (stream order keeps step i+1
-    from overwriting H_0 before step i's copy has read it); the host result
-    buffers alternate between two pinned sets."""
-    stream = torch.cuda.Stream(device=dev)
+    seed rows H_0 and the counts) comes back device -> host, with batches
+    overlapped as in the headline (OverlappedPipeline, its CUDA graphs).  The
+    host reads step j's result after enqueuing step j + depth - 1: step j +
+    depth reuses step j's pipeline and could not start earlier anyway.  The
+    pinned result buffers form a ring of depth + 1 sets."""
     B = w.batch
+    lag = ov.depth
+    ring = lag + 1
+    p0 = ov.pipes[0]
     h_seeds = torch.from_numpy(seeds_host).pin_memory()
     h_hseed = torch.tensor(hseeds, dtype=torch.int64).pin_memory()
-    out_rows = [torch.empty((B, w.dim), dtype=pipe.dtype, pin_memory=True) for _ in range(2)]
-    out_counts = [torch.empty(pipe.buf.counts.numel(), dtype=torch.int32, pin_memory=True) for _ in range(2)]
-    done = [torch.cuda.Event() for _ in range(2)]
-    with torch.cuda.stream(stream):
-        pipe.step()
-    torch.cuda.synchronize(dev)
-    cg = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(cg, stream=stream):
-        pipe.step()
+    out_rows = [torch.empty((B, w.dim), dtype=p0.dtype, pin_memory=True) for _ in range(ring)]
+    out_counts = [torch.empty(p0.buf.counts.numel(), dtype=torch.int32, pin_memory=True) for _ in range(ring)]
+    done = [torch.cuda.Event() for _ in range(ring)]
+
+    def inputs(i):
+        def f(p, s):
+            p.seeds[:B].copy_(h_seeds[i], non_blocking=True)
+            p.d_seed.copy_(h_hseed[i: i + 1], non_blocking=True)
+        return f
+
+    def after(i):
+        k = i % ring
+
+        def f(p, s):
+            out_rows[k].copy_(p.h_feat[0][:B], non_blocking=True)
+            out_counts[k].copy_(p.buf.counts, non_blocking=True)
+            done[k].record(s)
+        return f
+
     torch.cuda.synchronize(dev)
     n = len(seeds_host)
     edges = 0
     t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for i in range(n + 1):
-            if i < n:
-                k = i & 1
-                pipe.seeds[:B].copy_(h_seeds[i], non_blocking=True)
-                pipe.d_seed.copy_(h_hseed[i: i + 1], non_blocking=True)
-                cg.replay()
-                out_rows[k].copy_(pipe.h_feat[0][:B], non_blocking=True)
-                out_counts[k].copy_(pipe.buf.counts, non_blocking=True)
-                done[k].record(stream)
-            if i > 0:  # the previous step's result, read while this step runs
-                k = (i - 1) & 1
-                done[k].synchronize()
-                edges += int(out_counts[k][H + 1: 2 * H + 1].sum())
+    for i in range(n + lag):
+        if i < n:
+            ov.step(inputs(i), after(i))
+        j = i - lag + 1  # the oldest step not read yet, once `lag` steps are in flight
+        if i >= lag - 1 and j < n:
+            done[j % ring].synchronize()
+            edges += int(out_counts[j % ring][H + 1: 2 * H + 1].sum())
     dt = time.perf_counter() - t0
-    sg.sg_stream_check(stream)
+    for s in ov.streams:
+        sg.sg_stream_check(s)
     return {"value": edges / dt, "unit": "sampled edges/s", "ms_per_step": dt / n * 1e3, "steps": n,
-            "h2d_bytes_per_step": B * 4 + 8, "d2h_bytes_per_step": B * w.row_bytes + pipe.buf.counts.numel() * 4,
-            "note": "one CUDA-graph replay per step between the step's H2D and D2H copies; step i+1 is enqueued "
-                    "before the host reads step i's result"}
+            "h2d_bytes_per_step": B * 4 + 8, "d2h_bytes_per_step": B * w.row_bytes + p0.buf.counts.numel() * 4,
+            "note": "per step: seeds copied in from pinned memory, the step's two CUDA graphs (batches overlapped "
+                    "on %d pipelines), H_0 and the counts copied out to pinned memory; the host reads step j's result "
+                    "after enqueuing step j + %d" % (ov.depth, lag - 1)}
 
 
 # -------------------------------------------------------------- CPU baseline

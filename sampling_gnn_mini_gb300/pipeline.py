@@ -16,7 +16,10 @@ device seed buffers first).  With one mini-batch the gather runs in two
 parts: V_{H-1} is a prefix of V_H and is final once hop H-1 is relabelled
 (the sampler records an event there), so its feature rows are gathered on a
 second stream while hop H is sampled, and only the rows new at hop H wait for
-the sampler.  This module only allocates buffers and orders the calls.
+the sampler.  OverlappedPipeline runs consecutive batches on several such
+pipelines, so that one batch's sampling and gather overlap the previous
+batch's forward and backward.  This module only allocates buffers and orders
+the calls.
 """
 from __future__ import annotations
 
@@ -123,11 +126,13 @@ class MiniBatchPipeline:
             sg.sg_aggregate_bwd_t(t.tptr[h - 1], t.tdst[h - 1], t.tw[h - 1], nb[h], nb[h - 1], self.buf.dims(h),
                                   self.g_feat[h - 1], self.g_feat[h], stream=stream)
 
-    def step(self, stream=None) -> None:
-        """Sample, gather, forward and (if enabled) backward of one batch.
-        The transposed blocks are built on a second stream that forks after
-        sampling and joins before the backward pass; with the split gather,
-        V_{H-1}'s rows are gathered on a third stream during hop H."""
+    def load(self, stream=None, join: bool = False) -> None:
+        """Sampling, the transposed blocks and the gather of the current batch.
+        The transposes fork onto a second stream after sampling; with join
+        they are joined back before this returns (as a CUDA graph capture of
+        this part alone needs), otherwise train() joins them before the
+        backward pass.  With the split gather, V_{H-1}'s rows are gathered on a
+        third stream during hop H."""
         main = torch.cuda.current_stream() if stream is None else stream
         if self.split_gather:
             events = [None] * self.H
@@ -148,12 +153,123 @@ class MiniBatchPipeline:
             main.wait_event(self.ev_gathered)
         else:
             self.gather(main)
+        if self.backward and join:
+            main.wait_event(self.ev_transposed)
+
+    def train(self, stream=None, joined: bool = False) -> None:
+        """Forward and (if enabled) backward of the batch load() prepared;
+        joined: load() joined the transposes already (no wait here, as a CUDA
+        graph capture of this part alone needs)."""
+        main = torch.cuda.current_stream() if stream is None else stream
         self.forward(main)
         if self.backward:
-            main.wait_event(self.ev_transposed)
+            if not joined:
+                main.wait_event(self.ev_transposed)
             self.backward_pass(main)
+
+    def step(self, stream=None) -> None:
+        """Sample, gather, forward and (if enabled) backward of one batch; the
+        transposes overlap the gather and the forward."""
+        self.load(stream)
+        self.train(stream)
 
     def host_counts(self):
         c = self.buf.counts.cpu().tolist()
         H = self.H
         return {"nodes": c[: H + 1], "edges": c[H + 1: 2 * H + 1]}
+
+
+class OverlappedPipeline:
+    """Consecutive batches overlapped: `depth` MiniBatchPipelines (each with
+    its own buffers and streams) take batches in turn, so batch i+1 is
+    sampled, transposed and gathered while batch i's forward and backward run
+    (the sampler and the zero-copy gather are latency- and link-bound and
+    leave most of the GPU's issue slots free).  Batch i+1's forward waits for
+    batch i's backward, the order a training loop that updates weights between
+    batches needs.  A pipeline is reused `depth` batches later, after its own
+    stream has finished with the earlier batch.
+
+    step() enqueues one batch and returns the pipeline that holds it; its
+    results (counts, h_feat, g_feat) are valid once that pipeline's stream
+    reaches them.  capture() records each pipeline's two parts as CUDA graphs,
+    which step() then replays."""
+
+    def __init__(self, graph: sg.Graph, cache: sg.Cache, fanouts: Sequence[int], n_seeds: int, depth: int = 2,
+                 backward: bool = True, device="cuda"):
+        if depth < 1:
+            raise ValueError("OverlappedPipeline: depth must be at least 1")
+        self.pipes = [MiniBatchPipeline(graph, cache, fanouts, n_seeds, backward=backward, device=device)
+                      for _ in range(depth)]
+        self.streams = [torch.cuda.Stream(device=device) for _ in range(depth)]
+        self.ev_trained = torch.cuda.Event()
+        self.ev_trained.record()  # nothing is training yet
+        self.graphs = None
+        self.i = 0
+
+    @property
+    def depth(self) -> int:
+        return len(self.pipes)
+
+    def next_slot(self) -> int:
+        """Index of the pipeline the next step() uses."""
+        return self.i % self.depth
+
+    def capture(self) -> None:
+        graphs = []
+        for p, s in zip(self.pipes, self.streams):
+            with torch.cuda.stream(s):  # warm-up outside the capture
+                p.load(s, join=True)
+                p.train(s, joined=True)
+            s.synchronize()
+            gl, gt = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gl, stream=s):
+                p.load(s, join=True)
+            with torch.cuda.graph(gt, stream=s):
+                p.train(s, joined=True)
+            graphs.append((gl, gt))
+        torch.cuda.synchronize()
+        self.graphs = graphs
+
+    def step(self, set_inputs=None, after=None) -> MiniBatchPipeline:
+        """Enqueues one batch.  set_inputs(pipe, stream), if given, is called
+        first on the pipeline's stream to write the batch's seeds (for
+        instance pipe.set_batch, or copies from pinned memory); after(pipe,
+        stream), if given, is called on it once the batch is enqueued (for
+        instance to copy results out before the pipeline is reused)."""
+        k = self.next_slot()
+        p, s = self.pipes[k], self.streams[k]
+        with torch.cuda.stream(s):
+            if set_inputs is not None:
+                set_inputs(p, s)
+            if self.graphs is None:
+                p.load(s, join=True)
+            else:
+                self.graphs[k][0].replay()
+            s.wait_event(self.ev_trained)
+            if self.graphs is None:
+                p.train(s, joined=True)
+            else:
+                self.graphs[k][1].replay()
+            self.ev_trained.record(s)
+            if after is not None:
+                after(p, s)
+        self.i += 1
+        return p
+
+    def wait_all(self, stream=None) -> None:
+        """Makes `stream` (default: the current one) wait for every step
+        enqueued so far."""
+        st = torch.cuda.current_stream() if stream is None else stream
+        for s in self.streams:
+            ev = torch.cuda.Event()
+            ev.record(s)
+            st.wait_event(ev)
+
+    def start_after(self, stream=None) -> None:
+        """Makes the pipelines' streams wait for `stream` (default: the
+        current one), e.g. for inputs written there."""
+        st = torch.cuda.current_stream() if stream is None else stream
+        ev = torch.cuda.Event()
+        ev.record(st)
+        for s in self.streams:
+            s.wait_event(ev)

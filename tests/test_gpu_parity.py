@@ -15,7 +15,7 @@ import synth
 from helpers import (GpuSample, as_f64, assert_blocks_equal, assert_close, assert_super_equal, dev_i32,
                      feat_tensor, torch_to_np)
 from sampling_gnn_mini_gb300 import binding as sg
-from sampling_gnn_mini_gb300.pipeline import MiniBatchPipeline
+from sampling_gnn_mini_gb300.pipeline import MiniBatchPipeline, OverlappedPipeline
 
 pytestmark = pytest.mark.gpu
 
@@ -479,6 +479,54 @@ def test_pipeline_cuda_graph_replay_with_new_batches():
         torch.cuda.synchronize()
         sg.sg_stream_check()
         _check_pipeline_against_oracle(pipe, w, g, feat, seeds, w.sampler_seed(b))
+
+
+@pytest.mark.parametrize("depth,graphs", [(2, True), (3, False)])
+def test_overlapped_pipeline_matches_batches_run_alone(depth, graphs):
+    # Batches overlapped on `depth` pipelines (sampling and gather of one
+    # batch during the forward and backward of the previous) give, batch by
+    # batch, the same counts, sample, H_0 and input gradient, bit for bit, as
+    # the same batches run one at a time.
+    w, g, feat, single, host = _tiny_pipeline()
+    H = single.H
+    ov = OverlappedPipeline(single.graph, single.cache, w.fanouts, w.batch, depth=depth)
+    batches = list(range(10, 17))
+    seeds = {b: dev_i32(synth.batch_seeds(g.n, w.p_mask, b, w.batch)) for b in batches}
+    if graphs:
+        for p in ov.pipes:
+            p.set_batch(seeds[batches[0]], w.sampler_seed(batches[0]))
+        torch.cuda.synchronize()
+        ov.capture()
+    got = {}
+
+    def inputs(b):
+        def f(p, s):
+            sd = w.sampler_seed(b)
+            p.seeds[: w.batch].copy_(seeds[b], non_blocking=True)
+            p.d_seed.fill_(sd if sd < (1 << 63) else sd - (1 << 64))
+        return f
+
+    def after(b):
+        def f(p, s):
+            got[b] = (p.buf.counts.clone(), p.buf.unique.clone(), p.h_feat[0].clone(), p.g_feat[H].clone())
+        return f
+
+    for b in batches:
+        ov.step(inputs(b), after(b))
+    torch.cuda.synchronize()
+    for s_ in ov.streams:
+        sg.sg_stream_check(s_)
+    for b in batches:
+        single.set_batch(seeds[b], w.sampler_seed(b))
+        single.step()
+        torch.cuda.synchronize()
+        sg.sg_stream_check()
+        counts, unique, h0, gx = got[b]
+        assert torch.equal(counts, single.buf.counts), "counts, batch %d" % b
+        n = single.host_counts()["nodes"]
+        assert torch.equal(unique[: n[H]], single.buf.unique[: n[H]]), "sample, batch %d" % b
+        assert torch.equal(h0[: n[0]], single.h_feat[0][: n[0]]), "H_0, batch %d" % b
+        assert torch.equal(gx[: n[H]], single.g_feat[H][: n[H]]), "input gradient, batch %d" % b
 
 
 def test_transpose_blocks_match_stable_sort():
