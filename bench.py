@@ -41,7 +41,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="bound on the CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--depth", type=int, default=4, help="pipelines the overlapped batches rotate through")
+    ap.add_argument("--depth", type=int, default=0,
+                    help="pipelines the overlapped batches rotate through (0: OverlappedPipeline.suggested_depth)")
     return ap.parse_args()
 
 
@@ -158,7 +159,11 @@ class Workload:
         self.t_graph = time.time() - t0
         dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
         t0 = time.time()
-        self.feat = torch.empty((w.n_nodes, w.dim), dtype=dt, pin_memory=pinned_features)
+        if pinned_features:
+            from sampling_gnn_mini_gb300.hostmem import pinned_table
+            self.feat = pinned_table(w.n_nodes, w.dim, dt)
+        else:
+            self.feat = torch.empty((w.n_nodes, w.dim), dtype=dt)
         synth.features_into(self.feat.data_ptr(), 0, w.n_nodes, w.dim, w.dtype, w.rng_seed)
         self.t_feat = time.time() - t0
         self.batches = synth.BatchStream(w, epoch0=0)
@@ -188,12 +193,26 @@ def combine_ranks(torch, elapsed_ms: float, counters, device):
     return float(t.item()), [int(x) for x in c.tolist()]
 
 
-def kernels_per_step(H: int, n_sub: int) -> int:
+def frontier_ids(counts, unique, H: int, n_sub: int, h: int) -> np.ndarray:
+    """Distinct global IDs of V_h over the mini-batches of a step.  unique
+    holds each mini-batch's V_H back to back, V_h being a prefix of it; the
+    per-mini-batch sizes follow the totals in counts."""
+    if n_sub == 1:
+        return unique[: counts[h]]
+    parts, u0 = [], 0
+    for k in range(n_sub):
+        base = (2 * H + 1) * (1 + k)
+        parts.append(unique[u0: u0 + counts[base + h]])
+        u0 += counts[base + H]
+    return np.unique(np.concatenate(parts))
+
+
+def kernels_per_step(H: int, n_sub: int, by_region: bool = False) -> int:
     """Kernels one step launches: sampler 3 per hop (+1 per hop for a
-    super-batch) + 2, transposes 5, gather 1 (2 when one mini-batch of two
-    hops or more is gathered in two parts), forward 1 per hop, backward 1
-    per hop."""
-    gathers = 2 if (n_sub == 1 and H >= 2) else 1
+    super-batch) + 2, transposes 5, gather 1 a call (4 when misses are read
+    grouped by host-table region) and 2 calls when one mini-batch of two hops
+    or more is gathered in two parts, forward 1 per hop, backward 1 per hop."""
+    gathers = (2 if (n_sub == 1 and H >= 2) else 1) * (4 if by_region else 1)
     return (2 + 3 * H + (H if n_sub > 1 else 0)) + 5 + gathers + H + H
 
 
@@ -237,12 +256,18 @@ def run_ours(args, rank, world, local):
     cache = sg.sg_cache_build(W.feat if w.host_features else None,
                               None if w.host_features else W.feat.to(dev), dtype_code, w.n_nodes, w.dim,
                               ranked, cache_rows)
-    pipe = MiniBatchPipeline(G, cache, w.fanouts, w.batch, device=dev)
+    # a step is one batch, or one super-batch of w.n_sub mini-batches that
+    # share the hash seed (mini-batches b * n_sub .. b * n_sub + n_sub - 1)
+    n_sub = w.n_sub
+    SB = w.batch * n_sub  # seeds a step
+    bptr = [w.batch * k for k in range(n_sub + 1)] if n_sub > 1 else None
+    pipe = MiniBatchPipeline(G, cache, w.fanouts, SB, batch_ptr=bptr, device=dev)
 
     # batches of this rank (replicas: disjoint batch indices per rank)
     n_batches = args.warmup + args.steps
     bidx = replica_batches(rank, world, n_batches)
-    seeds_host = np.stack([W.seeds(b) for b in bidx]).astype(np.int32)
+    seeds_host = np.stack([np.concatenate([W.seeds(b * n_sub + k) for k in range(n_sub)])
+                           for b in bidx]).astype(np.int32)
     seeds_pool = torch.from_numpy(seeds_host).to(dev)
     hseed_pool = torch.tensor([w.sampler_seed(b) for b in bidx], dtype=torch.int64, device=dev)
     stream = torch.cuda.Stream(device=dev)
@@ -268,7 +293,7 @@ def run_ours(args, rank, world, local):
         stages.append(("bwd%d" % h, bwd_hop(h)))
 
     def load_batch(i):
-        pipe.seeds[: w.batch].copy_(seeds_pool[i], non_blocking=True)
+        pipe.seeds[:SB].copy_(seeds_pool[i], non_blocking=True)
         pipe.d_seed.copy_(hseed_pool[i: i + 1], non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -306,17 +331,18 @@ def run_ours(args, rank, world, local):
     # the headline: consecutive batches overlapped on two pipelines (batch
     # i+1 is sampled and gathered while batch i's forward and backward run;
     # batch i+1's forward still waits for batch i's backward)
-    ov = OverlappedPipeline(G, cache, w.fanouts, w.batch, depth=args.depth, device=dev)
+    depth = args.depth if args.depth > 0 else OverlappedPipeline.suggested_depth(cache)
+    ov = OverlappedPipeline(G, cache, w.fanouts, SB, depth=depth, batch_ptr=bptr, device=dev)
     with torch.cuda.stream(stream):
         load_batch(0)
     for p in ov.pipes:
-        p.set_batch(pipe.seeds[: w.batch].clone(), w.sampler_seed(bidx[0]))
+        p.set_batch(pipe.seeds[:SB].clone(), w.sampler_seed(bidx[0]))
     torch.cuda.synchronize(dev)
     ov.capture()
 
     def ov_inputs(i):
         def f(p, s):
-            p.seeds[: w.batch].copy_(seeds_pool[i], non_blocking=True)
+            p.seeds[:SB].copy_(seeds_pool[i], non_blocking=True)
             p.d_seed.copy_(hseed_pool[i: i + 1], non_blocking=True)
         return f
 
@@ -380,6 +406,7 @@ def run_ours(args, rank, world, local):
         for j, (name, _) in enumerate(graphs):
             stage_ms[name] += ev[s_][j].elapsed_time(ev[s_][j + 1]) / args.steps
     counts = counts_log[args.warmup:].cpu().numpy()
+    counts_all = counts.astype(np.int64)
     nodes = counts[:, : H + 1].astype(np.int64)
     edges = counts[:, H + 1: 2 * H + 1].astype(np.int64)
     total_edges = int(edges.sum())
@@ -405,7 +432,8 @@ def run_ours(args, rank, world, local):
         for h in range(1, H + 1):
             idx = pipe.buf.idx[h - 1][: edges[s, h - 1]].cpu().numpy()
             uniq_src[s, h - 1] = len(np.unique(idx))
-            d = deg[uq[: nodes[s, h - 1]]]
+            # every distinct node of the frontier V_{h-1} is sampled once
+            d = deg[frontier_ids(counts_all[s], uq, H, n_sub, h - 1)]
             hashed[s, h - 1] = int(d[d > w.fanouts[h - 1]].sum())
     n_H = nodes[:, H].astype(np.float64)
     gather_hbm = (8.0 * n_H).sum() + hits * R + n_H.sum() * R
@@ -463,16 +491,24 @@ def run_ours(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int32 sampling / " + w.dtype + " features, fp32 accumulation",
         "data": "synthetic Chung-Lu graph and N(0,1) features (seeded); no dataset",
-        "config": {"workload": "%s: %d nodes, %d edges, exponent %.1f, mean %.0f, dim %d %s, fanouts %s, batch %d, "
+        "config": {"workload": "%s: %d nodes, %d edges, exponent %.1f, mean %.0f, dim %d %s, fanouts %s, batch %s, "
                                "cache %d rows (%.0f%%)" % (w.name, g.n, g.m, w.gamma, w.mean_deg, w.dim, w.dtype,
-                                                          w.fanouts, w.batch, cache_rows, 100.0 * cache_rows / w.n_nodes),
+                                                          w.fanouts, "%d x %d (super-batch)" % (n_sub, w.batch)
+                                                          if n_sub > 1 else "%d" % w.batch,
+                                                          cache_rows, 100.0 * cache_rows / w.n_nodes),
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (CSR %.0f MB, features %.0f MB); a new batch every step"
                          % ((g.indptr.nbytes + g.indices.nbytes) / 1e6, w.n_nodes * R / 1e6)},
         "batch_latency_ms": latency_ms,
-        "overlap": "%d pipelines in turn: batch i+1 is sampled, transposed and gathered while batch i's forward "
-                   "and backward run; batch i+1's forward waits for batch i's backward. batch_latency_ms is one "
-                   "batch alone (a step graph per batch, batches back to back)" % args.depth,
+        "overlap": ("%d pipelines in turn: batch i+1 is sampled, transposed and gathered while batch i's forward "
+                    "and backward run; batch i+1's forward waits for batch i's backward" % depth if depth > 1 else
+                    "none: one batch at a time, a step graph each (misses come from a host table read by region, "
+                    "which concurrent gathers would interleave)") +
+                   ". batch_latency_ms is one batch alone (a step graph per batch, batches back to back)",
+        "host_table": None if not w.host_features else {
+            "bytes": w.n_nodes * R,
+            "huge_page_bytes": getattr(getattr(W.feat, "_sg_owner", None), "huge", 0),
+            "allocation": "huge-page mmap + cudaHostRegister" if hasattr(W.feat, "_sg_owner") else "cudaHostAlloc"},
         "gathered_feature_gbs": n_H.sum() * R / (elapsed_ms / 1e3) / 1e9,
         "gather_kernel_gbs": n_H.sum() * R / t_gather / 1e9,
         "memory_roofline_frac": {k: v["frac"] for k, v in stage_roof.items()},
@@ -485,7 +521,7 @@ def run_ours(args, rank, world, local):
         "roofline": roof,
         "host_link_gbs": link_gbs,
         "per_step": {"nodes": nodes.mean(axis=0).tolist(), "edges": edges.mean(axis=0).tolist()},
-        "gpu_launches": kernels_per_step(H, 1) * args.steps,
+        "gpu_launches": kernels_per_step(H, n_sub, pipe.gather_ws[0] is not None) * args.steps,
         "clocks": clk,
     }
     if rank == 0 and not args.no_e2e:
@@ -539,7 +575,7 @@ def measure_e2e(sg, torch, ov, seeds_host, hseeds, dev, args, H, w):
     host reads step j's result after enqueuing step j + depth - 1: step j +
     depth reuses step j's pipeline and could not start earlier anyway.  The
     pinned result buffers form a ring of depth + 1 sets."""
-    B = w.batch
+    B = ov.pipes[0].n_seeds
     lag = ov.depth
     ring = lag + 1
     p0 = ov.pipes[0]

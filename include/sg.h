@@ -273,9 +273,25 @@ typedef struct sg_gather_stats {
  *             the rest of the list is still being produced
  *   d_out     device, n_cap x dim in the cache's dtype (other rows untouched)
  *   d_stats   device, accumulated (+=) hit/miss counters, or NULL
+ *   d_workspace, workspace_bytes
+ *             device scratch of sg_gather_workspace(c, n_cap) bytes (256-byte
+ *             aligned; one per gather in flight), or NULL.  With it, and a
+ *             host table large enough that sg_gather_workspace is non-zero,
+ *             the misses are read grouped by 2 MB region of the host table
+ *             (a counting sort of the missed rows by region) instead of in
+ *             row order: on a table of tens of GB, random zero-copy reads
+ *             lose most of their rate to address translation, and reads of
+ *             one region in a row share it.  The output is the same either
+ *             way.
  * An ID out of range sets the device error word and its row is zero-filled. */
 sg_status sg_gather(const sg_cache* c, const int32_t* d_ids, int64_t n_cap, const int32_t* d_n,
-                    const int32_t* d_first, void* d_out, sg_gather_stats* d_stats, sg_stream_t stream);
+                    const int32_t* d_first, void* d_out, sg_gather_stats* d_stats, void* d_workspace,
+                    size_t workspace_bytes, sg_stream_t stream);
+
+/* Bytes of the workspace sg_gather uses to read the misses of up to n_cap
+ * rows grouped by host-table region; 0 when the cache has no host table or
+ * the table is small enough (under 32 GiB) that row order reads as fast. */
+size_t sg_gather_workspace(const sg_cache* c, int64_t n_cap);
 
 /* -------------------------------------------------------------- aggregate */
 /* Mean aggregation over one block (GARDEN page Section II-A Eq. (1) with

@@ -41,7 +41,7 @@ EXPORTS = ["sg_version", "sg_last_error", "sg_stream_check", "sg_graph_load", "s
            "sg_sampler_bounds", "sg_sampler_run", "sg_relabel_workspace", "sg_relabel", "sg_cache_build",
            "sg_cache_destroy", "sg_cache_info", "sg_gather", "sg_aggregate_fwd", "sg_aggregate_bwd_workspace",
            "sg_aggregate_bwd", "sg_read_probe", "sg_hash_probe", "sg_relabel_noalloc", "sg_transpose_workspace",
-           "sg_transpose_blocks", "sg_aggregate_bwd_t", "sg_sampler_workspace_init"]
+           "sg_transpose_blocks", "sg_aggregate_bwd_t", "sg_sampler_workspace_init", "sg_gather_workspace"]
 
 
 class SgError(RuntimeError):
@@ -105,7 +105,8 @@ def load(build_if_missing: bool = True):
             "sg_cache_build": (i32, [vp, vp, i32, i64, i32, vp, i64, ctypes.POINTER(vp), vp]),
             "sg_cache_destroy": (i32, [vp]),
             "sg_cache_info": (i32, [vp, vp, vp, vp, vp, vp]),
-            "sg_gather": (i32, [vp, vp, i64, vp, vp, vp, vp, vp]),
+            "sg_gather": (i32, [vp, vp, i64, vp, vp, vp, vp, vp, sz, vp]),
+            "sg_gather_workspace": (sz, [vp, i64]),
             "sg_aggregate_fwd": (i32, [vp, vp, i32, i32, vp, vp, i32, i32, vp, i32, vp]),
             "sg_aggregate_bwd_workspace": (sz, [i32, i32, i64]),
             "sg_aggregate_bwd": (i32, [vp, vp, i32, i32, i64, vp, vp, i32, i32, vp, i32, vp, sz, vp]),
@@ -345,10 +346,16 @@ def sg_cache_build(h_feat: Optional[torch.Tensor], d_feat: Optional[torch.Tensor
     return Cache(out.value, h_feat)
 
 
+def sg_gather_workspace(cache: Cache, n_cap: int) -> int:
+    return int(load().sg_gather_workspace(cache.handle, int(n_cap)))
+
+
 def sg_gather(cache: Cache, ids: torch.Tensor, n_cap: int, d_n: Optional[torch.Tensor], out: torch.Tensor,
-              stats: Optional[torch.Tensor] = None, stream=None, d_first: Optional[torch.Tensor] = None) -> None:
+              stats: Optional[torch.Tensor] = None, stream=None, d_first: Optional[torch.Tensor] = None,
+              workspace: Optional[torch.Tensor] = None) -> None:
     _check(load().sg_gather(cache.handle, ids.data_ptr(), int(n_cap), _ptr(d_n), _ptr(d_first), out.data_ptr(),
-                            _ptr(stats), _stream(stream)))
+                            _ptr(stats), _ptr(workspace), 0 if workspace is None else workspace.numel(),
+                            _stream(stream)))
 
 
 # --------------------------------------------------------------- aggregate

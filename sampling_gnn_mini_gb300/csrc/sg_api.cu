@@ -283,6 +283,16 @@ extern "C" sg_status sg_cache_build(const void* h_feat, const void* d_feat, int3
     c->row_bytes = row_bytes;
     c->n_cache = n_cache;
     c->host_rows = host_dev;
+    // Tables of 32 GiB and more: misses can be read grouped by 2 MB region
+    // (sg_gather with a workspace).  Measured on GB300 with random 512-byte
+    // rows: a 16 GB pinned table reads at ~208 GB/s in any order, a 60 GB one
+    // at ~10 GB/s in random order and ~40 GB/s grouped by region.
+    if (host_dev && n_cache < n_nodes && n_nodes * row_bytes >= (int64_t(32) << 30)) {
+        int32_t shift = 0;
+        while ((int64_t(row_bytes) << (shift + 1)) <= (int64_t(2) << 20)) ++shift;
+        c->region_shift = shift > 0 ? shift : 1;
+        c->n_regions = ((n_nodes - 1) >> c->region_shift) + 1;
+    }
     int32_t* d_ranked = nullptr;
     unsigned* d_bad = nullptr;
     cudaError_t e = cudaMalloc((void**)&c->slot_of, (size_t)n_nodes * sizeof(int32_t));

@@ -12,6 +12,15 @@
 // with the streaming hint (each is used once here); the output is stored
 // with the default policy, so that the first aggregation hop, which reads it
 // next, finds part of it in L2.
+//
+// Large host tables (32 GiB and more) with a workspace: random zero-copy
+// reads there lose most of their rate to address translation (measured on
+// GB300, 512-byte rows: ~208 GB/s from a 16 GB pinned table in any order,
+// ~10 GB/s from a 60 GB one in random order, ~40 GB/s grouped by 2 MB
+// region).  So k_gather leaves the misses out and counts them per region;
+// k_region_scan turns the counts into offsets, k_region_scatter lists the
+// missed rows region by region (any order within a region), and
+// k_gather_list copies them in list order.
 #include "sg_internal.cuh"
 #include "sg_objects.cuh"
 
@@ -29,7 +38,8 @@ __global__ void __launch_bounds__(kThreads) k_gather(const int32_t* __restrict__
                                                      int64_t n_cap, const int32_t* __restrict__ slot_of, int64_t n_nodes,
                                                      const uint4* __restrict__ cache, const uint4* __restrict__ host,
                                                      int32_t row_vecs, int64_t step_rows, int32_t step_rem,
-                                                     uint4* __restrict__ out, sg_gather_stats* __restrict__ stats) {
+                                                     uint4* __restrict__ out, sg_gather_stats* __restrict__ stats,
+                                                     uint32_t* __restrict__ region_cnt, int32_t region_shift) {
     pdl_start();
     int64_t n = n_cap;
     if (d_n) {
@@ -66,6 +76,10 @@ __global__ void __launch_bounds__(kThreads) k_gather(const int32_t* __restrict__
                     if (s >= 0) {
                         v[u] = __ldcs(cache + (int64_t)s * row_vecs + c);
                         hits += (c == 0);
+                    } else if (region_cnt) {  // left for k_gather_list
+                        if (c == 0) atomicAdd(region_cnt + (g >> region_shift), 1u);
+                        dst[u] = -1;
+                        misses += (c == 0);
                     } else {
                         v[u] = __ldcs(host + (int64_t)g * row_vecs + c);
                         misses += (c == 0);
@@ -94,10 +108,123 @@ __global__ void __launch_bounds__(kThreads) k_gather(const int32_t* __restrict__
     }
 }
 
+// Rows [first, n) of the call, from the device counts (as k_gather).
+__device__ __forceinline__ void gather_range(const int32_t* d_n, const int32_t* d_first, int64_t n_cap, int64_t& first,
+                                             int64_t& n) {
+    n = n_cap;
+    if (d_n) {
+        const int64_t dn = *d_n;
+        n = dn < n_cap ? (dn < 0 ? 0 : dn) : n_cap;
+    }
+    first = 0;
+    if (d_first) {
+        const int64_t df = *d_first;
+        first = df < 0 ? 0 : (df < n ? df : n);
+    }
+}
+
+// Exclusive scan of the n_regions miss counts in place (one block); the
+// total goes to cnt[n_regions].  Each thread scans a contiguous run.
+constexpr int kScanThreads = 1024;
+__global__ void __launch_bounds__(kScanThreads) k_region_scan(uint32_t* __restrict__ cnt, int64_t n_regions) {
+    pdl_start();
+    __shared__ uint32_t sh[kScanThreads];
+    const int64_t per = (n_regions + kScanThreads - 1) / kScanThreads;
+    const int64_t a = min((int64_t)threadIdx.x * per, n_regions), b = min(a + per, n_regions);
+    uint32_t sum = 0;
+    for (int64_t r = a; r < b; ++r) sum += cnt[r];
+    sh[threadIdx.x] = sum;
+    __syncthreads();
+    for (int d = 1; d < kScanThreads; d <<= 1) {  // inclusive scan of the run totals
+        const uint32_t x = threadIdx.x >= (unsigned)d ? sh[threadIdx.x - d] : 0u;
+        __syncthreads();
+        sh[threadIdx.x] += x;
+        __syncthreads();
+    }
+    uint32_t run = sh[threadIdx.x] - sum;
+    for (int64_t r = a; r < b; ++r) {
+        const uint32_t k = cnt[r];
+        cnt[r] = run;
+        run += k;
+    }
+    if (threadIdx.x == kScanThreads - 1) cnt[n_regions] = sh[kScanThreads - 1];
+}
+
+// Lists the missed rows i in [first, n) by region: list[pos] = i, pos taken
+// from the region's offset.
+__global__ void __launch_bounds__(kThreads) k_region_scatter(const int32_t* __restrict__ ids,
+                                                             const int32_t* __restrict__ d_n,
+                                                             const int32_t* __restrict__ d_first, int64_t n_cap,
+                                                             const int32_t* __restrict__ slot_of, int64_t n_nodes,
+                                                             uint32_t* __restrict__ cnt, int32_t region_shift,
+                                                             int32_t* __restrict__ list) {
+    pdl_start();
+    int64_t first, n;
+    gather_range(d_n, d_first, n_cap, first, n);
+    for (int64_t i = first + blockIdx.x * (int64_t)kThreads + threadIdx.x; i < n; i += (int64_t)gridDim.x * kThreads) {
+        const int32_t g = __ldg(ids + i);
+        if (g < 0 || (int64_t)g >= n_nodes) continue;
+        if (__ldg(slot_of + g) >= 0) continue;
+        const uint32_t pos = atomicAdd(cnt + (g >> region_shift), 1u);
+        if ((int64_t)pos < n_cap) list[pos] = (int32_t)i;
+        else dev_err(ERR_CAPACITY);
+    }
+}
+
+// Copies the listed rows from the host table, flattened over (entry,
+// vector) with kUnroll loads in flight, in list order.
+__global__ void __launch_bounds__(kThreads) k_gather_list(const int32_t* __restrict__ list,
+                                                          const uint32_t* __restrict__ total,
+                                                          const int32_t* __restrict__ ids,
+                                                          const uint4* __restrict__ host, int32_t row_vecs,
+                                                          int64_t n_cap, int64_t step_rows, int32_t step_rem,
+                                                          uint4* __restrict__ out) {
+    pdl_start();
+    int64_t m = *total;
+    if (m > n_cap) m = n_cap;
+    const int64_t work = m * row_vecs;
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    int64_t t = blockIdx.x * (int64_t)kThreads + threadIdx.x;
+    int64_t j = t / row_vecs;
+    int32_t c = (int32_t)(t - j * row_vecs);
+    while (t < work) {
+        uint4 v[kUnroll];
+        int64_t dst[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            dst[u] = -1;
+            if (t < work) {
+                const int32_t i = __ldg(list + j);
+                const int32_t g = __ldg(ids + i);
+                v[u] = __ldcs(host + (int64_t)g * row_vecs + c);
+                dst[u] = (int64_t)i * row_vecs + c;
+            }
+            t += stride;
+            j += step_rows;
+            c += step_rem;
+            if (c >= row_vecs) {
+                c -= row_vecs;
+                ++j;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+            if (dst[u] >= 0) out[dst[u]] = v[u];
+    }
+}
+
+size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
+
 }  // namespace
 
+extern "C" size_t sg_gather_workspace(const sg_cache* c, int64_t n_cap) {
+    if (!c || c->region_shift <= 0 || n_cap <= 0) return 0;
+    return a256((size_t)(c->n_regions + 1) * sizeof(uint32_t)) + a256((size_t)n_cap * sizeof(int32_t));
+}
+
 extern "C" sg_status sg_gather(const sg_cache* c, const int32_t* d_ids, int64_t n_cap, const int32_t* d_n,
-                               const int32_t* d_first, void* d_out, sg_gather_stats* d_stats, sg_stream_t stream) {
+                               const int32_t* d_first, void* d_out, sg_gather_stats* d_stats, void* d_workspace,
+                               size_t workspace_bytes, sg_stream_t stream) {
     if (!c) return fail(SG_ERR_INVALID_ARG, "sg_gather: NULL cache");
     if (n_cap < 0) return fail(SG_ERR_INVALID_ARG, "sg_gather: n_cap < 0");
     if (n_cap == 0) return SG_OK;
@@ -112,8 +239,30 @@ extern "C" sg_status sg_gather(const sg_cache* c, const int32_t* d_ids, int64_t 
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     const int64_t stride = blocks * kThreads;
-    SG_CUDA(launch_pdl(k_gather, dim3((unsigned)blocks), dim3(kThreads), 0, (cudaStream_t)stream, d_ids, d_n, d_first,
+    cudaStream_t s = (cudaStream_t)stream;
+    // misses grouped by host-table region (large tables, with a workspace)
+    const size_t need = sg_gather_workspace(c, n_cap);
+    const bool by_region = d_workspace && need > 0;
+    if (by_region && workspace_bytes < need)
+        return fail(SG_ERR_INVALID_ARG, "sg_gather: workspace needs %zu bytes", need);
+    if (by_region && ((uintptr_t)d_workspace) % 256)
+        return fail(SG_ERR_INVALID_ARG, "sg_gather: workspace must be 256-byte aligned");
+    uint32_t* cnt = by_region ? (uint32_t*)d_workspace : nullptr;
+    int32_t* list = by_region ? (int32_t*)((char*)d_workspace + a256((size_t)(c->n_regions + 1) * sizeof(uint32_t)))
+                              : nullptr;
+    if (by_region) SG_CUDA(cudaMemsetAsync(cnt, 0, (size_t)(c->n_regions + 1) * sizeof(uint32_t), s));
+    SG_CUDA(launch_pdl(k_gather, dim3((unsigned)blocks), dim3(kThreads), 0, s, d_ids, d_n, d_first,
                        n_cap, c->slot_of, c->n_nodes, (const uint4*)c->rows, (const uint4*)c->host_rows,
-                       (int32_t)row_vecs, stride / row_vecs, (int32_t)(stride % row_vecs), (uint4*)d_out, d_stats));
+                       (int32_t)row_vecs, stride / row_vecs, (int32_t)(stride % row_vecs), (uint4*)d_out, d_stats,
+                       cnt, c->region_shift));
+    if (!by_region) return SG_OK;
+    SG_CUDA(launch_pdl(k_region_scan, dim3(1), dim3(kScanThreads), 0, s, cnt, c->n_regions));
+    int64_t sblocks = cdiv(n_cap, (int64_t)kThreads);
+    if (sblocks > cap) sblocks = cap;
+    SG_CUDA(launch_pdl(k_region_scatter, dim3((unsigned)sblocks), dim3(kThreads), 0, s, d_ids, d_n, d_first, n_cap,
+                       c->slot_of, c->n_nodes, cnt, c->region_shift, list));
+    SG_CUDA(launch_pdl(k_gather_list, dim3((unsigned)blocks), dim3(kThreads), 0, s, (const int32_t*)list,
+                       (const uint32_t*)(cnt + c->n_regions), d_ids, (const uint4*)c->host_rows, (int32_t)row_vecs,
+                       n_cap, stride / row_vecs, (int32_t)(stride % row_vecs), (uint4*)d_out));
     return SG_OK;
 }

@@ -21,4 +21,6 @@ struct sg_cache {
     void* rows = nullptr;            // device, n_cache x row_bytes (slot order)
     int32_t* slot_of = nullptr;      // device, n_nodes: slot of a cached node, else -1
     const void* host_rows = nullptr; // device-usable address of the host table (may be NULL)
+    int32_t region_shift = 0;        // log2 rows of a 2 MB host-table region; 0: misses read in row order
+    int64_t n_regions = 0;           // regions of the host table when region_shift > 0
 };

@@ -50,6 +50,10 @@ class MiniBatchPipeline:
         # h_feat[h] holds H_h: rows V_h, h = 0..H (h = H is X)
         self.h_feat = [torch.empty(max(1, nb[h]), d, dtype=dt, device=device) for h in range(self.H + 1)]
         self.stats = torch.zeros(2, dtype=torch.int64, device=device)
+        # gather scratch for reading misses grouped by host-table region (large
+        # host tables only); the two parts of a split gather may overlap, so
+        # each has its own
+        self.gather_ws = [self._gather_ws(nb[self.H], device), self._gather_ws(nb[self.H - 1], device)]
         if backward:
             self.g_feat = [self.h_feat[0]] + [torch.empty(max(1, nb[h]), d, dtype=dt, device=device)
                                               for h in range(1, self.H + 1)]
@@ -69,6 +73,10 @@ class MiniBatchPipeline:
             # |V_{H-1}| of the single mini-batch, final when ev_prefix fires
             at = (2 * H + 1) + (H - 1)
             self.n_prefix = self.buf.counts[at:at + 1]
+
+    def _gather_ws(self, n_cap: int, device) -> Optional[torch.Tensor]:
+        nbytes = sg.sg_gather_workspace(self.cache, n_cap)
+        return sg.aligned_workspace(nbytes, device) if nbytes > 0 else None
 
     @property
     def counts(self) -> torch.Tensor:
@@ -93,13 +101,13 @@ class MiniBatchPipeline:
         """Rows of V_{H-1} (split gather only)."""
         H = self.H
         sg.sg_gather(self.cache, self.buf.unique, self.bounds.max_nodes[H - 1], self.n_prefix, self.h_feat[H],
-                     self.stats, stream=stream)
+                     self.stats, stream=stream, workspace=self.gather_ws[1])
 
     def gather_rest(self, stream=None) -> None:
         """Rows of V_H from |V_{H-1}| on (split gather only)."""
         H = self.H
         sg.sg_gather(self.cache, self.buf.unique, self.bounds.max_nodes[H], self.buf.counts[H:H + 1],
-                     self.h_feat[H], self.stats, stream=stream, d_first=self.n_prefix)
+                     self.h_feat[H], self.stats, stream=stream, d_first=self.n_prefix, workspace=self.gather_ws[0])
 
     def gather(self, stream=None) -> None:
         H = self.H
@@ -108,7 +116,7 @@ class MiniBatchPipeline:
             self.gather_rest(stream)
             return
         sg.sg_gather(self.cache, self.buf.unique, self.bounds.max_nodes[H], self.buf.counts[H:H + 1],
-                     self.h_feat[H], self.stats, stream=stream)
+                     self.h_feat[H], self.stats, stream=stream, workspace=self.gather_ws[0])
 
     def forward(self, stream=None) -> None:
         nb = self.bounds.max_nodes
@@ -191,15 +199,25 @@ class OverlappedPipeline:
 
     step() enqueues one batch and returns the pipeline that holds it; its
     results (counts, h_feat, g_feat) are valid once that pipeline's stream
-    reaches them.  capture() records each pipeline's two parts as CUDA graphs,
-    which step() then replays."""
+    reaches them.  capture() records each pipeline's two parts as CUDA graphs
+    (depth 1: the whole step as one graph), which step() then replays.
+
+    suggested_depth() picks the depth: 4, or 1 when misses are read from a
+    host table large enough that the gather reads them grouped by region
+    there, concurrent gathers of several batches interleave their regions and
+    lose that grouping (measured on the 61 GB Wide table: 3.6 ms a step with
+    four pipelines against 2.8 ms one batch at a time)."""
+
+    @staticmethod
+    def suggested_depth(cache: sg.Cache) -> int:
+        return 1 if sg.sg_gather_workspace(cache, 1) > 0 else 4
 
     def __init__(self, graph: sg.Graph, cache: sg.Cache, fanouts: Sequence[int], n_seeds: int, depth: int = 2,
-                 backward: bool = True, device="cuda"):
+                 batch_ptr: Optional[Sequence[int]] = None, backward: bool = True, device="cuda"):
         if depth < 1:
             raise ValueError("OverlappedPipeline: depth must be at least 1")
-        self.pipes = [MiniBatchPipeline(graph, cache, fanouts, n_seeds, backward=backward, device=device)
-                      for _ in range(depth)]
+        self.pipes = [MiniBatchPipeline(graph, cache, fanouts, n_seeds, batch_ptr=batch_ptr, backward=backward,
+                                        device=device) for _ in range(depth)]
         self.streams = [torch.cuda.Stream(device=device) for _ in range(depth)]
         self.ev_trained = torch.cuda.Event()
         self.ev_trained.record()  # nothing is training yet
@@ -216,6 +234,17 @@ class OverlappedPipeline:
 
     def capture(self) -> None:
         graphs = []
+        if self.depth == 1:  # no overlap: the whole step, transposes beside gather and forward
+            p, s = self.pipes[0], self.streams[0]
+            with torch.cuda.stream(s):
+                p.step(s)
+            s.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                p.step(s)
+            torch.cuda.synchronize()
+            self.graphs = [(g, None)]
+            return
         for p, s in zip(self.pipes, self.streams):
             with torch.cuda.stream(s):  # warm-up outside the capture
                 p.load(s, join=True)
@@ -241,6 +270,15 @@ class OverlappedPipeline:
         with torch.cuda.stream(s):
             if set_inputs is not None:
                 set_inputs(p, s)
+            if self.depth == 1:
+                if self.graphs is None:
+                    p.step(s)
+                else:
+                    self.graphs[0][0].replay()
+                if after is not None:
+                    after(p, s)
+                self.i += 1
+                return p
             if self.graphs is None:
                 p.load(s, join=True)
             else:

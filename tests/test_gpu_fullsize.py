@@ -16,6 +16,7 @@ import oracle
 import synth
 from helpers import as_f64, assert_close, dev_i32, torch_to_np
 from sampling_gnn_mini_gb300 import binding as sg
+from sampling_gnn_mini_gb300.hostmem import pinned_table
 from sampling_gnn_mini_gb300.pipeline import MiniBatchPipeline
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
@@ -37,7 +38,7 @@ class PinnedTable:
     holds it), with a numpy view for the checks (bf16 as uint16 bits)."""
 
     def __init__(self, n, dim, dtype, seed):
-        self.t = torch.empty((n, dim), dtype=torch.float32 if dtype == "f32" else torch.bfloat16, pin_memory=True)
+        self.t = pinned_table(n, dim, torch.float32 if dtype == "f32" else torch.bfloat16)
         synth.features_into(self.t.data_ptr(), 0, n, dim, dtype, seed)
         self.arr = self.t.numpy() if dtype == "f32" else self.t.view(torch.int16).numpy().view(np.uint16)
 
@@ -190,3 +191,50 @@ def test_host_feature_workloads_full_size(name):
     del table, G, g
     gc.collect()
     torch.cuda.empty_cache()
+
+
+# ------------------------------------- misses grouped by host-table region
+def test_gather_large_host_table_by_region():
+    # A 34 GiB host table (over the size from which misses are read grouped by
+    # 2 MB region): with the workspace the gather lists the misses region by
+    # region and copies them in that order; rows must equal the table's and
+    # the plain row-order gather's, bit for bit, in one part and in two.
+    dim, n = 128, (34 << 30) // 512
+    t = pinned_table(n, dim, torch.float32)
+    tv = t.view(torch.int32)
+    tv[:, 0] = torch.arange(n, dtype=torch.int32)  # row i starts with i; pages are zero-filled
+    tv[:, dim - 1] = -torch.arange(n, dtype=torch.int32)
+    rng = np.random.default_rng(5)
+    ranked = rng.choice(n, size=n // 3, replace=False).astype(np.int32)
+    cache = sg.sg_cache_build(t, None, sg.SG_F32, n, dim, ranked, len(ranked))
+    m = 400_000
+    ids = rng.integers(0, n, size=m).astype(np.int32)
+    d_ids = dev_i32(ids)
+    nbytes = sg.sg_gather_workspace(cache, m)
+    assert nbytes > 0
+    ws = sg.aligned_workspace(nbytes)
+    outs = []
+    for workspace in (None, ws):
+        out = torch.zeros((m, dim), dtype=torch.float32, device="cuda")
+        stats = torch.zeros(2, dtype=torch.int64, device="cuda")
+        sg.sg_gather(cache, d_ids, m, None, out, stats, workspace=workspace)
+        sg.sg_stream_check()
+        hits, misses = stats.cpu().tolist()
+        assert hits + misses == m and misses > m // 2
+        outs.append(out.view(torch.int32).cpu().numpy())
+    assert np.array_equal(outs[0], outs[1])
+    assert np.array_equal(outs[1][:, 0], ids) and np.array_equal(outs[1][:, dim - 1], -ids)
+    assert not outs[1][:, 1: dim - 1].any()
+    # two parts: rows [0, first) then [first, m2) (device counts), the rest untouched
+    first, m2 = 150_000, 350_000
+    out = torch.full((m, dim), 7.0, device="cuda")
+    d_first = torch.tensor([first], dtype=torch.int32, device="cuda")
+    d_n = torch.tensor([m2], dtype=torch.int32, device="cuda")
+    sg.sg_gather(cache, d_ids, m, d_first, out, workspace=ws)  # n = first
+    sg.sg_gather(cache, d_ids, m, d_n, out, d_first=d_first, workspace=ws)
+    sg.sg_stream_check()
+    got = out.view(torch.int32).cpu().numpy()
+    assert np.array_equal(got[:m2], outs[0][:m2])
+    assert np.all(out[m2:].cpu().numpy() == 7.0)
+    del cache, t
+    gc.collect()
