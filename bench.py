@@ -624,22 +624,26 @@ def measure_e2e(sg, torch, ov, seeds_host, hseeds, dev, args, H, w):
 # -------------------------------------------------------------- CPU baseline
 def run_oracle_steps(W, batches, budget_s):
     """The oracle's whole step (sample+relabel, gather, forward and backward
-    chains in fp64) on the given batches, stopping once budget_s is spent."""
+    chains in fp64) on the given batches, stopping once budget_s is spent.  A
+    step of a super-batch config is its n_sub mini-batches with the shared
+    hash seed (a super-batch equals that many separate runs)."""
     import oracle
     w, g = W.w, W.g
     feat = W.feat.numpy() if w.dtype == "f32" else W.feat.view(__import__("torch").int16).numpy().view(np.uint16)
     edges, done, t0 = 0, 0, time.perf_counter()
     for b in batches:
-        seeds = W.seeds(b)
-        r = oracle.sampler_run(g.indptr, g.indices, seeds, w.fanouts, w.sampler_seed(b))
-        x = oracle.gather(feat, r.unique)
-        hh = x
-        for h in range(w.n_hops, 0, -1):
-            hh, _ = oracle.aggregate_fwd(r.indptr[h - 1], r.idx[h - 1], hh.astype(np.float32) if hh.dtype != np.uint16 else hh)
-        gg = hh.astype(np.float32)
-        for h in range(1, w.n_hops + 1):
-            gg, _ = oracle.aggregate_bwd(r.indptr[h - 1], r.idx[h - 1], r.hop_off[h], gg.astype(np.float32))
-        edges += sum(len(i) for i in r.idx)
+        for k in range(w.n_sub):
+            seeds = W.seeds(b * w.n_sub + k)
+            r = oracle.sampler_run(g.indptr, g.indices, seeds, w.fanouts, w.sampler_seed(b))
+            x = oracle.gather(feat, r.unique)
+            hh = x
+            for h in range(w.n_hops, 0, -1):
+                hh, _ = oracle.aggregate_fwd(r.indptr[h - 1], r.idx[h - 1],
+                                             hh.astype(np.float32) if hh.dtype != np.uint16 else hh)
+            gg = hh.astype(np.float32)
+            for h in range(1, w.n_hops + 1):
+                gg, _ = oracle.aggregate_bwd(r.indptr[h - 1], r.idx[h - 1], r.hop_off[h], gg.astype(np.float32))
+            edges += sum(len(i) for i in r.idx)
         done += 1
         if time.perf_counter() - t0 > budget_s:
             break
@@ -651,8 +655,9 @@ def cpu_baseline(W, budget_s):
     import oracle
     edges, done, dt = run_oracle_steps(W, range(5000, 6000), budget_s)
     return {"value": edges / dt, "unit": "sampled edges/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": "%d %s batches, whole step (sample+relabel, gather, %d-hop forward and backward), %.1f s"
-                      % (done, W.w.name, W.w.n_hops, dt)}
+            "sample": "%d %s %s, whole step (sample+relabel, gather, %d-hop forward and backward), %.1f s"
+                      % (done, W.w.name, "batches" if W.w.n_sub == 1 else "super-batches of %d" % W.w.n_sub,
+                         W.w.n_hops, dt)}
 
 
 def run_reference(args, rank, world):
@@ -674,7 +679,8 @@ def run_reference(args, rank, world):
             "data": "synthetic Chung-Lu graph and N(0,1) features (seeded); no dataset",
             "config": {"workload": "%s (same graph, features and batches as the GPU arm)" % w.name},
             "cpu_baseline": {"value": value, "unit": "sampled edges/s", "cores": oracle.num_threads(), "kind": "oracle",
-                             "sample": "%d batches, one whole step each" % done},
+                             "sample": "%d %s, one whole step each" % (
+                                 done, "batches" if w.n_sub == 1 else "super-batches of %d" % w.n_sub)},
             "e2e": {"value": value, "unit": "sampled edges/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
