@@ -21,21 +21,28 @@ import torch
 HUGE_TABLE_BYTES = 32 << 30  # from this size on, back the table with huge pages
 
 
+def huge_bytes_in(addr: int, smaps_lines) -> int:
+    """AnonHugePages (bytes) of the mapping that starts at addr, from the
+    lines of a /proc/<pid>/smaps listing; 0 if no mapping starts there."""
+    found = False
+    for line in smaps_lines:
+        parts = line.split(None, 1)
+        if not parts:
+            continue
+        head = parts[0]
+        if "-" in head and not head.endswith(":"):
+            found = int(head.split("-")[0], 16) == addr
+        elif found and head == "AnonHugePages:":
+            return int(line.split()[1]) * 1024
+    return 0
+
+
 def _huge_bytes(addr: int) -> int:
-    """AnonHugePages of the mapping that starts at addr, from /proc/self/smaps
-    (0 when unknown)."""
     try:
         with open("/proc/self/smaps") as f:
-            found = False
-            for line in f:
-                head = line.split(None, 1)[0]
-                if "-" in head and not head.endswith(":"):
-                    found = int(head.split("-")[0], 16) == addr
-                elif found and line.startswith("AnonHugePages:"):
-                    return int(line.split()[1]) * 1024
+            return huge_bytes_in(addr, f)
     except (OSError, ValueError):
-        pass
-    return 0
+        return 0
 
 
 class _Registered:
