@@ -65,6 +65,10 @@ def _load():
         lib.orc_aggregate_fwd.argtypes = [vp, vp, i64, vp, ctypes.c_int, i32, vp, vp]
         lib.orc_aggregate_bwd.restype = None
         lib.orc_aggregate_bwd.argtypes = [vp, vp, i64, i64, vp, ctypes.c_int, i32, vp, vp]
+        lib.orc_sage_fwd.restype = None
+        lib.orc_sage_fwd.argtypes = [vp, vp, i32, vp, i32, i64, i32, i32, vp, vp, vp]
+        lib.orc_sage_bwd.restype = None
+        lib.orc_sage_bwd.argtypes = [vp, vp, i32, vp, i32, vp, vp, i32, i64, i32, i32, vp, vp, vp, vp, vp]
         _lib = lib
         return lib
 
@@ -259,6 +263,48 @@ def aggregate_bwd(indptr, idx, n_src: int, gdst: np.ndarray):
     am = np.zeros((n_src, dim), np.float64)
     _load().orc_aggregate_bwd(_p(ip), _p(ix), n_dst, n_src, _p(g), _dtype_code(g), dim, _p(out), _p(am))
     return out, am
+
+
+def _feat(a: np.ndarray) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    _dtype_code(a)
+    return a
+
+
+def sage_fwd(h: np.ndarray, m: np.ndarray, W: np.ndarray):
+    """SAGE UPDATE forward: y = [h | m] W^T, out = ReLU(y).  h, m: [n, d]
+    (float32 or bf16 bits, the same type); W: [d_out, 2d] (float32 or bf16
+    bits).  Returns (y, out, absum) as float64 [n, d_out]."""
+    hh, mm, ww = _feat(h), _feat(m), _feat(W)
+    if hh.shape != mm.shape or hh.dtype != mm.dtype:
+        raise ValueError("sage_fwd: h and m differ in shape or type")
+    n, d = hh.shape
+    d_out = ww.shape[0]
+    if ww.shape[1] != 2 * d:
+        raise ValueError("sage_fwd: W must have 2 * d columns")
+    y = np.zeros((n, d_out), np.float64)
+    out = np.zeros((n, d_out), np.float64)
+    am = np.zeros((n, d_out), np.float64)
+    _load().orc_sage_fwd(_p(hh), _p(mm), _dtype_code(hh), _p(ww), _dtype_code(ww), n, d, d_out, _p(y), _p(out), _p(am))
+    return y, out, am
+
+
+def sage_bwd(h: np.ndarray, m: np.ndarray, W: np.ndarray, y: np.ndarray, g: np.ndarray):
+    """Backward of sage_fwd for g = dL/dout [n, d_out] (float32 or bf16 bits)
+    and the forward's y (float64).  Returns (dW, absum_dW, dh, dm, absum_dz):
+    dW [d_out, 2d], dh and dm [n, d], absum_dz [n, 2d], all float64."""
+    hh, mm, ww, gg = _feat(h), _feat(m), _feat(W), _feat(g)
+    yy = np.ascontiguousarray(y, dtype=np.float64)
+    n, d = hh.shape
+    d_out = ww.shape[0]
+    dW = np.zeros((d_out, 2 * d), np.float64)
+    am_w = np.zeros((d_out, 2 * d), np.float64)
+    dh = np.zeros((n, d), np.float64)
+    dm = np.zeros((n, d), np.float64)
+    am_z = np.zeros((n, 2 * d), np.float64)
+    _load().orc_sage_bwd(_p(hh), _p(mm), _dtype_code(hh), _p(ww), _dtype_code(ww), _p(yy), _p(gg), _dtype_code(gg),
+                         n, d, d_out, _p(dW), _p(am_w), _p(dh), _p(dm), _p(am_z))
+    return dW, am_w, dh, dm, am_z
 
 
 def bf16_to_f32(bits: np.ndarray) -> np.ndarray:

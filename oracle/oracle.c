@@ -296,3 +296,73 @@ void orc_aggregate_bwd(const int64_t* indptr, const int32_t* idx, int64_t n_dst,
         }
     }
 }
+
+/* SAGE UPDATE of one layer (GARDEN page, Section II-A, Eq. (2) with UPDATE a
+ * learnable map of the node's previous state and its aggregated message;
+ * GraphSAGE's form: a linear layer over the concatenation, then ReLU):
+ *   y[r][o]   = sum_{k<d} W[o][k] h[r][k] + sum_{k<d} W[o][d+k] m[r][k]
+ *   out[r][o] = y[r][o] > 0 ? y[r][o] : 0
+ * for r < n, o < d_out, with W of d_out rows of 2d.  h holds the dst rows'
+ * own previous states, m their mean-aggregated messages.  Sums in fp64, in k
+ * order; absum[r][o] is the sum of |terms| (the tolerance scale). */
+void orc_sage_fwd(const void* h, const void* m, int dtype, const void* W, int wtype, int64_t n, int32_t d,
+                  int32_t d_out, double* y, double* out, double* absum) {
+    #pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t r = 0; r < n; r++) {
+        for (int32_t o = 0; o < d_out; o++) {
+            double s = 0.0, a = 0.0;
+            for (int32_t k = 0; k < 2 * d; k++) {
+                double z = k < d ? load_elem(h, dtype, r * d + k) : load_elem(m, dtype, r * d + (k - d));
+                double t = load_elem(W, wtype, (int64_t)o * 2 * d + k) * z;
+                s += t;
+                a += t < 0 ? -t : t;
+            }
+            y[r * d_out + o] = s;
+            out[r * d_out + o] = s > 0 ? s : 0.0;
+            if (absum) absum[r * d_out + o] = a;
+        }
+    }
+}
+
+/* Backward of orc_sage_fwd for the loss gradient g = dL/dout [n x d_out]
+ * (ReLU's derivative is 1 where y > 0, else 0, y from the forward):
+ *   dy[r][o] = g[r][o] * (y[r][o] > 0)
+ *   dW[o][k] = sum_r dy[r][o] z[r][k]          z = [h | m], k < 2d
+ *   dh[r][k] = sum_o dy[r][o] W[o][k]          k < d
+ *   dm[r][k] = sum_o dy[r][o] W[o][d + k]      k < d
+ * Sums in fp64 (dW in r order, dh and dm in o order); the absum arrays hold
+ * the sums of |terms|. */
+void orc_sage_bwd(const void* h, const void* m, int dtype, const void* W, int wtype, const double* y,
+                  const void* g, int gtype, int64_t n, int32_t d, int32_t d_out, double* dW, double* absum_dW,
+                  double* dh, double* dm, double* absum_dz) {
+    #pragma omp parallel for schedule(dynamic, 4)
+    for (int32_t o = 0; o < d_out; o++) {
+        for (int32_t k = 0; k < 2 * d; k++) {
+            double s = 0.0, a = 0.0;
+            for (int64_t r = 0; r < n; r++) {
+                if (!(y[r * d_out + o] > 0)) continue;
+                double z = k < d ? load_elem(h, dtype, r * d + k) : load_elem(m, dtype, r * d + (k - d));
+                double t = load_elem(g, gtype, r * d_out + o) * z;
+                s += t;
+                a += t < 0 ? -t : t;
+            }
+            dW[(int64_t)o * 2 * d + k] = s;
+            if (absum_dW) absum_dW[(int64_t)o * 2 * d + k] = a;
+        }
+    }
+    #pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t r = 0; r < n; r++) {
+        for (int32_t k = 0; k < 2 * d; k++) {
+            double s = 0.0, a = 0.0;
+            for (int32_t o = 0; o < d_out; o++) {
+                if (!(y[r * d_out + o] > 0)) continue;
+                double t = load_elem(g, gtype, r * d_out + o) * load_elem(W, wtype, (int64_t)o * 2 * d + k);
+                s += t;
+                a += t < 0 ? -t : t;
+            }
+            if (k < d) dh[r * d + k] = s;
+            else dm[r * d + (k - d)] = s;
+            if (absum_dz) absum_dz[r * 2 * d + k] = a;
+        }
+    }
+}

@@ -354,3 +354,101 @@ def test_key_tie_rows_pin_the_position_tie_break():
         got = oracle.sample_positions(indptr, v, f, 1, seed)
         want = np.sort(np.concatenate([np.nonzero(keys < key)[0], [j_lo]]))
         assert np.array_equal(got, want)
+
+
+# ------------------------------------------------------- SAGE UPDATE (NEXT-1)
+def _to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 values exactly representable in bf16 -> their bf16 bits."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    assert not (b & 0xFFFF).any()
+    return (b >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_sage_fwd_reduces_to_sums_for_identity_blocks(bf16):
+    # W = [I | I]: y = h + m; W = [0 | I]: out = ReLU(m); W = [I | 0]: ReLU(h).
+    # Small integers are exact in bf16 and in every sum.
+    rng = np.random.default_rng(40)
+    n, d = 7, 5
+    h = rng.integers(-4, 5, size=(n, d)).astype(np.float32)
+    m = rng.integers(-4, 5, size=(n, d)).astype(np.float32)
+    eye, zero = np.eye(d, dtype=np.float32), np.zeros((d, d), np.float32)
+    conv = _to_bf16_bits if bf16 else (lambda a: a)
+    for W, want_y in ((np.hstack([eye, eye]), h + m), (np.hstack([zero, eye]), m), (np.hstack([eye, zero]), h)):
+        y, out, am = oracle.sage_fwd(conv(h), conv(m), conv(W))
+        assert np.array_equal(y, want_y)
+        assert np.array_equal(out, np.maximum(want_y, 0))
+        assert np.all(am >= np.abs(y))
+
+
+def _sage_case(rng, n, d, d_out, margin=0.05):
+    """Random float32 inputs whose pre-activations all stay at least `margin`
+    away from 0 (so small perturbations cross no ReLU kink)."""
+    while True:
+        h = rng.standard_normal((n, d)).astype(np.float32)
+        m = rng.standard_normal((n, d)).astype(np.float32)
+        W = rng.standard_normal((d_out, 2 * d)).astype(np.float32)
+        y, _, _ = oracle.sage_fwd(h, m, W)
+        if np.abs(y).min() > margin and (y > 0).any() and (y < 0).any():
+            return h, m, W
+
+
+def test_sage_bwd_matches_central_differences():
+    # The loss L = sum g * ReLU(y) is linear in each input away from ReLU kinks,
+    # so a central difference with a power-of-two step is exact up to fp64
+    # rounding: it pins dW, dh and dm without retyping the formulas.
+    rng = np.random.default_rng(41)
+    n, d, d_out = 4, 3, 5
+    h, m, W = _sage_case(rng, n, d, d_out)
+    g = rng.standard_normal((n, d_out)).astype(np.float32)
+    y, _, _ = oracle.sage_fwd(h, m, W)
+    dW, _, dh, dm, _ = oracle.sage_bwd(h, m, W, y, g)
+    step = np.float32(2.0 ** -12)
+
+    def loss(hh, mm, ww):
+        return float((oracle.sage_fwd(hh, mm, ww)[1] * g.astype(np.float64)).sum())
+
+    for name, arr, grad in (("W", W, dW), ("h", h, dh), ("m", m, dm)):
+        num = np.zeros_like(grad)
+        for idx in np.ndindex(arr.shape):
+            hi, lo = arr.copy(), arr.copy()
+            hi[idx] += step
+            lo[idx] -= step
+            args = {"h": (h, m, W), "m": (h, m, W), "W": (h, m, W)}[name]
+            a_hi = [hi if x is arr else x for x in args]
+            a_lo = [lo if x is arr else x for x in args]
+            num[idx] = (loss(*a_hi) - loss(*a_lo)) / (2 * float(step))
+        assert np.allclose(num, grad, rtol=1e-9, atol=1e-9), name
+
+
+def test_sage_adjoint_identity_where_relu_is_active():
+    # With every pre-activation positive the layer is the linear map
+    # z -> z W^T, so <y, g> = <z, dz> = <W, dW> (z = [h | m]).
+    rng = np.random.default_rng(42)
+    n, d, d_out = 6, 4, 3
+    h = rng.random((n, d)).astype(np.float32) + 0.1
+    m = rng.random((n, d)).astype(np.float32) + 0.1
+    W = rng.random((d_out, 2 * d)).astype(np.float32) + 0.1
+    g = rng.standard_normal((n, d_out)).astype(np.float32)
+    y, out, _ = oracle.sage_fwd(h, m, W)
+    assert (y > 0).all() and np.array_equal(y, out)
+    dW, _, dh, dm, _ = oracle.sage_bwd(h, m, W, y, g)
+    z = np.hstack([h, m]).astype(np.float64)
+    a = float((y * g).sum())
+    assert np.isclose(a, float((z * np.hstack([dh, dm])).sum()), rtol=1e-12)
+    assert np.isclose(a, float((W.astype(np.float64) * dW).sum()), rtol=1e-12)
+
+
+def test_sage_bwd_zero_where_relu_is_off():
+    # y <= 0 (including y exactly 0: h = -m with W = [I | I]) passes no gradient.
+    d = 3
+    h = np.array([[1, -2, 3], [0, 0, 0]], np.float32)
+    m = np.array([[-1, 1, 1], [0, 0, 0]], np.float32)
+    W = np.hstack([np.eye(d), np.eye(d)]).astype(np.float32)
+    y, out, _ = oracle.sage_fwd(h, m, W)
+    assert y.tolist() == [[0, -1, 4], [0, 0, 0]]
+    g = np.ones((2, d), np.float32)
+    dW, _, dh, dm, _ = oracle.sage_bwd(h, m, W, y, g)
+    assert dh.tolist() == [[0, 0, 1], [0, 0, 0]] and dm.tolist() == dh.tolist()
+    # only (row 0, output 2) is active, with dy = 1: dW's row 2 is z's row 0
+    assert dW.tolist() == [[0] * 6, [0] * 6, [1, -2, 3, -1, 1, 1]]
