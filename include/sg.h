@@ -356,6 +356,31 @@ sg_status sg_aggregate_bwd_t(const int32_t* d_tptr, const int32_t* d_tdst, const
                              int32_t n_dst_cap, const int32_t* d_dims, const void* d_gdst, int32_t dtype_in,
                              int32_t dim, void* d_gsrc, int32_t dtype_out, sg_stream_t stream);
 
+/* ----------------------------------------------------- SAGE UPDATE (GEMM) */
+/* The UPDATE of one GraphSAGE layer (GARDEN page Section II-A, Eq. (2); the
+ * linear layer over the concatenation of a node's previous state and its
+ * mean-aggregated message, then ReLU; hidden width 128 as in Section VI-A):
+ *   y[r, o]   = sum_{k<d} W[o, k] h[r, k] + sum_{k<d} W[o, d + k] m[r, k]
+ *   out[r, o] = max(y[r, o], 0)          r < n, o < d_out
+ * on the tensor cores (fp32 inputs as tf32, bf16 inputs as bf16; fp32
+ * accumulation).
+ *   d_h       device [n_cap x dim], the dst rows' previous states (in a
+ *             pipeline: the first n_dst rows of H_h, since V_{h-1} is a
+ *             prefix of V_h)
+ *   d_m       device [n_cap x dim], their aggregated messages (the output of
+ *             sg_aggregate_fwd for the block)
+ *   d_W       device [d_out x 2 dim] row-major, same dtype as d_h and d_m
+ *   dtype     SG_F32 or SG_BF16 (of d_h, d_m and d_W)
+ *   d_n       device int32 count (n = *d_n <= n_cap) or NULL (n = n_cap)
+ *   dim       dim * element size a multiple of 16 bytes
+ *   d_out     128
+ *   d_out_act device [n_cap x d_out] fp32: rows r < n written
+ *   d_y       device [n_cap x d_out] fp32 pre-activations, or NULL
+ * All arrays 16-byte aligned; nothing is allocated. */
+sg_status sg_sage_fwd(const void* d_h, const void* d_m, const void* d_W, int32_t dtype, int32_t n_cap,
+                      const int32_t* d_n, int32_t dim, int32_t d_out, float* d_out_act, float* d_y,
+                      sg_stream_t stream);
+
 /* ------------------------------------------------------------ measurement */
 /* Streams `bytes` of device-accessible memory at d_src with 16-byte loads
  * (a read roofline probe: HBM when d_src is device memory, the host link when

@@ -41,7 +41,8 @@ EXPORTS = ["sg_version", "sg_last_error", "sg_stream_check", "sg_graph_load", "s
            "sg_sampler_bounds", "sg_sampler_run", "sg_relabel_workspace", "sg_relabel", "sg_cache_build",
            "sg_cache_destroy", "sg_cache_info", "sg_gather", "sg_aggregate_fwd", "sg_aggregate_bwd_workspace",
            "sg_aggregate_bwd", "sg_read_probe", "sg_hash_probe", "sg_relabel_noalloc", "sg_transpose_workspace",
-           "sg_transpose_blocks", "sg_aggregate_bwd_t", "sg_sampler_workspace_init", "sg_gather_workspace"]
+           "sg_transpose_blocks", "sg_aggregate_bwd_t", "sg_sampler_workspace_init", "sg_gather_workspace",
+           "sg_sage_fwd"]
 
 
 class SgError(RuntimeError):
@@ -107,6 +108,7 @@ def load(build_if_missing: bool = True):
             "sg_cache_info": (i32, [vp, vp, vp, vp, vp, vp]),
             "sg_gather": (i32, [vp, vp, i64, vp, vp, vp, vp, vp, sz, vp]),
             "sg_gather_workspace": (sz, [vp, i64]),
+            "sg_sage_fwd": (i32, [vp, vp, vp, i32, i32, vp, i32, i32, vp, vp, vp]),
             "sg_aggregate_fwd": (i32, [vp, vp, i32, i32, vp, vp, i32, i32, vp, i32, vp]),
             "sg_aggregate_bwd_workspace": (sz, [i32, i32, i64]),
             "sg_aggregate_bwd": (i32, [vp, vp, i32, i32, i64, vp, vp, i32, i32, vp, i32, vp, sz, vp]),
@@ -356,6 +358,13 @@ def sg_gather(cache: Cache, ids: torch.Tensor, n_cap: int, d_n: Optional[torch.T
     _check(load().sg_gather(cache.handle, ids.data_ptr(), int(n_cap), _ptr(d_n), _ptr(d_first), out.data_ptr(),
                             _ptr(stats), _ptr(workspace), 0 if workspace is None else workspace.numel(),
                             _stream(stream)))
+
+
+def sg_sage_fwd(h: torch.Tensor, m: torch.Tensor, W: torch.Tensor, n_cap: int, d_n: Optional[torch.Tensor],
+                out: torch.Tensor, y: Optional[torch.Tensor] = None, stream=None) -> None:
+    """out = ReLU([h | m] W^T) for the first n rows (see sg.h)."""
+    _check(load().sg_sage_fwd(h.data_ptr(), m.data_ptr(), W.data_ptr(), _dtype_code(h), int(n_cap), _ptr(d_n),
+                              int(h.shape[1]), int(W.shape[0]), out.data_ptr(), _ptr(y), _stream(stream)))
 
 
 # --------------------------------------------------------------- aggregate
