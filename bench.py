@@ -53,6 +53,16 @@ def dist_env():
     return rank, world, local
 
 
+def measured_bf16_tflops():
+    """The measured dense bf16 GEMM burst rate (TFLOP/s), or None."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            v = json.load(fh).get("bf16_tflops")
+        return float(v) if v else None
+    return None
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -291,6 +301,19 @@ def run_ours(args, rank, world, local):
         stages.append(("fwd%d" % h, fwd_hop(h)))
     for h in range(1, H + 1):
         stages.append(("bwd%d" % h, bwd_hop(h)))
+    # the SAGE UPDATE (tensor cores) over the largest forward hop's output:
+    # ReLU([H_{H-1} own rows | mean] W^T), W of 128 rows (staged region only;
+    # the headline step is the four-step path)
+    upd = None
+    if (w.row_bytes % 16) == 0 and n_sub == 1:
+        wdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+        upd = {"W": (torch.randn((128, 2 * w.dim), generator=torch.Generator().manual_seed(7)) / (2 * w.dim) ** 0.5)
+               .to(wdt).to(dev),
+               "out": torch.empty((max(1, nb[H - 1]), 128), dtype=torch.float32, device=dev)}
+
+        def update_hop():
+            sg.sg_sage_fwd(pipe.h_feat[H], pipe.h_feat[H - 1], upd["W"], nb[H - 1], pipe.buf.dims(H), upd["out"])
+        stages.append(("update%d" % H, update_hop))
 
     def load_batch(i):
         pipe.seeds[:SB].copy_(seeds_pool[i], non_blocking=True)
@@ -459,6 +482,23 @@ def run_ours(args, rank, world, local):
         t = stage_ms["bwd%d" % h] / 1e3
         stage_roof["bwd%d" % h] = {"bound": "hbm", "bytes_per_launch": byt,
                                    "achieved_gbs": byt / t / 1e9, "frac": byt / t / 1e9 / hbm_peak}
+    if upd is not None:
+        # A = the dst rows' own states and their means (n_{H-1} x 2d), W, and
+        # the fp32 output (n_{H-1} x 128); 2 * n * 2d * 128 flops
+        t = stage_ms["update%d" % H] / 1e3
+        rows = bn[:, H - 1].astype(np.float64)
+        byt = float((rows * 2 * R + 128 * 2 * R + rows * 128 * 4).mean())
+        flops = float((2.0 * rows * 2 * w.dim * 128).mean())
+        # tensor peak for the arithmetic used: tf32 for fp32 rows (the recipe's
+        # nominal tf32 : bf16 ratio, 1.1 : 2.25, times the measured bf16 burst),
+        # bf16 measured burst otherwise
+        bf16_peak = measured_bf16_tflops()
+        tc_peak = bf16_peak * (1.1 / 2.25 if w.dtype == "f32" else 1.0) if bf16_peak else None
+        stage_roof["update%d" % H] = {
+            "bound": "hbm", "bytes_per_launch": byt, "achieved_gbs": byt / t / 1e9, "frac": byt / t / 1e9 / hbm_peak,
+            "flops_per_launch": flops, "achieved_tflops": flops / t / 1e12,
+            "tensor_peak_tflops": tc_peak, "tensor_frac": (flops / t / 1e12) / tc_peak if tc_peak else None,
+            "arithmetic": "tf32 (tcgen05 kind::tf32)" if w.dtype == "f32" else "bf16 (tcgen05 kind::f16)"}
     t_sample = stage_ms["sample"] / 1e3
     calls = float(hashed.sum(axis=1).mean()) / 4.0
     stage_roof["sample"] = {"bound": "alu", "hash_calls_per_step": calls, "hash_calls_per_s": calls / t_sample,
