@@ -381,6 +381,28 @@ sg_status sg_sage_fwd(const void* d_h, const void* d_m, const void* d_W, int32_t
                       const int32_t* d_n, int32_t dim, int32_t d_out, float* d_out_act, float* d_y,
                       sg_stream_t stream);
 
+/* Backward of sg_sage_fwd for the loss gradient d_g = dL/dout (GraphSAGE's
+ * layer as above; ReLU'(0) = 0):
+ *   dY = g * (y > 0)
+ *   dW[o, k]   = sum_{r<n} dY[r, o] z[r, k]         z = [h | m]
+ *   dh[r, k]   = sum_o dY[r, o] W[o, k]             k < dim
+ *   dm[r, k]   = sum_o dY[r, o] W[o, dim + k]
+ * on the tensor cores (operands as in sg_sage_fwd; for bf16 inputs dY is
+ * rounded to bf16).  dW sums over rows in a fixed order of splits, so the
+ * result is deterministic.
+ *   d_y, d_g  device [n_cap x d_out] fp32 (d_y: the forward's pre-activation)
+ *   d_dW      device [d_out x 2 dim] fp32
+ *   d_dh,d_dm device [n_cap x dim] fp32, rows r < n written
+ *   d_workspace  device scratch of sg_sage_bwd_workspace(n_cap, dim, dtype)
+ *             bytes, 256-byte aligned
+ * Other arguments as in sg_sage_fwd. */
+sg_status sg_sage_bwd(const void* d_h, const void* d_m, const void* d_W, int32_t dtype, int32_t n_cap,
+                      const int32_t* d_n, int32_t dim, int32_t d_out, const float* d_y, const float* d_g, float* d_dW,
+                      float* d_dh, float* d_dm, void* d_workspace, size_t workspace_bytes, sg_stream_t stream);
+
+/* Bytes of the workspace of sg_sage_bwd; 0 on bad arguments. */
+size_t sg_sage_bwd_workspace(int32_t n_cap, int32_t dim, int32_t dtype);
+
 /* ------------------------------------------------------------ measurement */
 /* Streams `bytes` of device-accessible memory at d_src with 16-byte loads
  * (a read roofline probe: HBM when d_src is device memory, the host link when

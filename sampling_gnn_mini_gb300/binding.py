@@ -42,7 +42,7 @@ EXPORTS = ["sg_version", "sg_last_error", "sg_stream_check", "sg_graph_load", "s
            "sg_cache_destroy", "sg_cache_info", "sg_gather", "sg_aggregate_fwd", "sg_aggregate_bwd_workspace",
            "sg_aggregate_bwd", "sg_read_probe", "sg_hash_probe", "sg_relabel_noalloc", "sg_transpose_workspace",
            "sg_transpose_blocks", "sg_aggregate_bwd_t", "sg_sampler_workspace_init", "sg_gather_workspace",
-           "sg_sage_fwd"]
+           "sg_sage_fwd", "sg_sage_bwd", "sg_sage_bwd_workspace"]
 
 
 class SgError(RuntimeError):
@@ -109,6 +109,8 @@ def load(build_if_missing: bool = True):
             "sg_gather": (i32, [vp, vp, i64, vp, vp, vp, vp, vp, sz, vp]),
             "sg_gather_workspace": (sz, [vp, i64]),
             "sg_sage_fwd": (i32, [vp, vp, vp, i32, i32, vp, i32, i32, vp, vp, vp]),
+            "sg_sage_bwd": (i32, [vp, vp, vp, i32, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]),
+            "sg_sage_bwd_workspace": (sz, [i32, i32, i32]),
             "sg_aggregate_fwd": (i32, [vp, vp, i32, i32, vp, vp, i32, i32, vp, i32, vp]),
             "sg_aggregate_bwd_workspace": (sz, [i32, i32, i64]),
             "sg_aggregate_bwd": (i32, [vp, vp, i32, i32, i64, vp, vp, i32, i32, vp, i32, vp, sz, vp]),
@@ -365,6 +367,19 @@ def sg_sage_fwd(h: torch.Tensor, m: torch.Tensor, W: torch.Tensor, n_cap: int, d
     """out = ReLU([h | m] W^T) for the first n rows (see sg.h)."""
     _check(load().sg_sage_fwd(h.data_ptr(), m.data_ptr(), W.data_ptr(), _dtype_code(h), int(n_cap), _ptr(d_n),
                               int(h.shape[1]), int(W.shape[0]), out.data_ptr(), _ptr(y), _stream(stream)))
+
+
+def sg_sage_bwd_workspace(n_cap: int, dim: int, dtype: int) -> int:
+    return int(load().sg_sage_bwd_workspace(int(n_cap), int(dim), int(dtype)))
+
+
+def sg_sage_bwd(h: torch.Tensor, m: torch.Tensor, W: torch.Tensor, n_cap: int, d_n: Optional[torch.Tensor],
+                y: torch.Tensor, g: torch.Tensor, dW: torch.Tensor, dh: torch.Tensor, dm: torch.Tensor,
+                workspace: torch.Tensor, stream=None) -> None:
+    """Backward of sg_sage_fwd (see sg.h)."""
+    _check(load().sg_sage_bwd(h.data_ptr(), m.data_ptr(), W.data_ptr(), _dtype_code(h), int(n_cap), _ptr(d_n),
+                              int(h.shape[1]), int(W.shape[0]), y.data_ptr(), g.data_ptr(), dW.data_ptr(),
+                              dh.data_ptr(), dm.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream(stream)))
 
 
 # --------------------------------------------------------------- aggregate
