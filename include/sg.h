@@ -29,6 +29,15 @@
  *    Problems found by a kernel (a node ID out of range, a full hash table,
  *    a repeated seed) set a sticky device error word; sg_stream_check()
  *    synchronises the stream, reads and clears it.
+ *  - Memory the library owns (behind sg_graph and sg_cache) is allocated in
+ *    sg_graph_load and sg_cache_build only; a failed allocation returns
+ *    SG_ERR_OOM and leaves nothing allocated.  With the environment variable
+ *    SG_FAULT_INJECT=alloc:N (read once per process) the N-th such allocation
+ *    fails in that way without reaching the CUDA runtime, so callers can test
+ *    their out-of-memory handling.
+ *  - Every device-side wait (the look-back of the single-pass scans, the
+ *    mbarrier waits of the copy-engine and tensor-core kernels) is bounded;
+ *    a wait that gives up sets SG_ERR_TIMEOUT in the device error word.
  *  - Sizes that depend on the data (|V_h|, E_h) stay on the device.  Calls that
  *    consume them take a host-side CAPACITY plus an optional device pointer to
  *    the actual count (d_n / d_dims), so a whole mini-batch can run, and be
@@ -76,7 +85,8 @@ int32_t sg_last_error(char* buf, size_t n);
 
 /* Synchronises `stream`, then reads and clears the device error word that the
  * library's kernels set.  Returns SG_OK, SG_ERR_INVALID_INDEX, SG_ERR_CAPACITY,
- * SG_ERR_INVALID_ARG (repeated seed in one mini-batch) or SG_ERR_CUDA. */
+ * SG_ERR_INVALID_ARG (repeated seed in one mini-batch), SG_ERR_TIMEOUT (a
+ * bounded device wait gave up) or SG_ERR_CUDA. */
 sg_status sg_stream_check(sg_stream_t stream);
 
 /* ------------------------------------------------------------------ graph */
@@ -414,6 +424,23 @@ sg_status sg_read_probe(const void* d_src, int64_t bytes, uint32_t* d_sink, sg_s
  * 0..n_calls-1 under `seed`) across the whole GPU and folds the outputs into
  * *d_sink (device uint32): the integer-throughput roofline of sampling. */
 sg_status sg_hash_probe(int64_t n_calls, uint64_t seed, uint32_t* d_sink, sg_stream_t stream);
+
+/* Exercises the bounded wait of the library's single-pass scans (decoupled
+ * look-back) so that callers can check their timeout handling: n_tiles
+ * blocks (1..4096) take tiles in order and each computes the exclusive
+ * prefix of the values t + 1 over the tiles before it, written to d_out[t]
+ * (device int32 [n_tiles]; t(t+1)/2 when every tile publishes).  The block
+ * that takes tile `silent_tile` (or none, when it is outside [0, n_tiles))
+ * exits without publishing, so every later tile's look-back that reaches it
+ * polls spin_limit (1..2^22) times, gives up and sets SG_ERR_TIMEOUT in the
+ * device error word, which the next sg_stream_check reports; the stream and
+ * the library stay usable.  d_out[t] for t < silent_tile is exact; later
+ * entries are not defined.  d_workspace: sg_wait_probe_workspace(n_tiles)
+ * bytes, 256-byte aligned, cleared by the call.  No page defines this call:
+ * it is a diagnostic of this library. */
+size_t sg_wait_probe_workspace(int32_t n_tiles);
+sg_status sg_wait_probe(int32_t n_tiles, int32_t silent_tile, int32_t spin_limit, void* d_workspace,
+                        size_t workspace_bytes, int32_t* d_out, sg_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -42,7 +42,7 @@ EXPORTS = ["sg_version", "sg_last_error", "sg_stream_check", "sg_graph_load", "s
            "sg_cache_destroy", "sg_cache_info", "sg_gather", "sg_aggregate_fwd", "sg_aggregate_bwd_workspace",
            "sg_aggregate_bwd", "sg_read_probe", "sg_hash_probe", "sg_relabel_noalloc", "sg_transpose_workspace",
            "sg_transpose_blocks", "sg_aggregate_bwd_t", "sg_sampler_workspace_init", "sg_gather_workspace",
-           "sg_sage_fwd", "sg_sage_bwd", "sg_sage_bwd_workspace"]
+           "sg_sage_fwd", "sg_sage_bwd", "sg_sage_bwd_workspace", "sg_wait_probe", "sg_wait_probe_workspace"]
 
 
 class SgError(RuntimeError):
@@ -122,6 +122,8 @@ def load(build_if_missing: bool = True):
                                           vp]),
             "sg_aggregate_bwd_t": (i32, [vp, vp, vp, i32, i32, vp, vp, i32, i32, vp, i32, vp]),
             "sg_sampler_workspace_init": (i32, [vp, i32, vp, i32, vp, i32, vp, sz, vp]),
+            "sg_wait_probe": (i32, [i32, i32, i32, vp, sz, vp, vp]),
+            "sg_wait_probe_workspace": (sz, [i32]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -421,6 +423,16 @@ def sg_read_probe(src_ptr: int, nbytes: int, sink: torch.Tensor, stream=None) ->
     _check(load().sg_read_probe(int(src_ptr), int(nbytes), sink.data_ptr(), _stream(stream)))
 
 
+def sg_wait_probe(n_tiles: int, silent_tile: int, spin_limit: int, out: torch.Tensor, stream=None) -> None:
+    """Runs the bounded look-back wait over n_tiles tiles with tile
+    silent_tile never publishing (see include/sg.h); out: int32 [n_tiles]."""
+    lib = load()
+    nbytes = int(lib.sg_wait_probe_workspace(int(n_tiles)))
+    ws = _aligned_bytes(max(256, nbytes), out.device)
+    _check(lib.sg_wait_probe(int(n_tiles), int(silent_tile), int(spin_limit), ws.data_ptr(), ws.numel(),
+                             out.data_ptr(), _stream(stream)))
+
+
 def sg_hash_probe(n_calls: int, seed: int, sink: torch.Tensor, stream=None) -> None:
     _check(load().sg_hash_probe(int(n_calls), ctypes.c_uint64(seed), sink.data_ptr(), _stream(stream)))
 
@@ -431,8 +443,21 @@ SG_RELABEL_NOALLOC_MAX_IDS = 262144
 def sg_relabel_noalloc(ids: torch.Tensor, prefix: torch.Tensor, unique: torch.Tensor, local: torch.Tensor,
                        n_unique: torch.Tensor, stream=None) -> None:
     """Relabel into caller-provided outputs with no allocation by the library
-    (its scratch is a static device array; see include/sg.h)."""
+    (its scratch is a static device array; see include/sg.h).  The C entry
+    point cannot see the sizes of the output arrays, so they are checked
+    here: int32, contiguous, on one CUDA device, unique with room for
+    len(prefix) + len(ids) entries, local for len(ids), n_unique for one."""
     n_ids, n_pre = int(ids.numel()), int(prefix.numel())
+    arrays = {"ids": ids, "prefix": prefix, "unique": unique, "local": local, "n_unique": n_unique}
+    dev = unique.device
+    for name, t in arrays.items():
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous() \
+                or t.device != dev:
+            raise SgError(SG_ERR_INVALID_ARG, "sg_relabel_noalloc: %s must be a contiguous int32 tensor on %s"
+                          % (name, dev))
+    if unique.numel() < n_pre + n_ids or local.numel() < n_ids or n_unique.numel() < 1:
+        raise SgError(SG_ERR_INVALID_ARG, "sg_relabel_noalloc: outputs too small (unique needs %d entries, local %d, "
+                      "n_unique 1)" % (n_pre + n_ids, n_ids))
     _check(load().sg_relabel_noalloc(ids.data_ptr() if n_ids else None, n_ids, prefix.data_ptr() if n_pre else None,
                                      n_pre, unique.data_ptr(), local.data_ptr(), n_unique.data_ptr(), _stream(stream)))
 

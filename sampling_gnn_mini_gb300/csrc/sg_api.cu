@@ -1,8 +1,10 @@
 // C ABI entry points for status, graph and cache handles, and the read probe.
 #include <stdarg.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <string>
 
@@ -42,6 +44,29 @@ int num_sms() {
         cache[dev] = n;
     }
     return cache[dev];
+}
+
+// SG_FAULT_INJECT=alloc:N makes the N-th owned allocation fail (N >= 1).
+static long long inject_alloc_at() {
+    static long long at = -1;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        const char* v = getenv("SG_FAULT_INJECT");
+        if (v && strncmp(v, "alloc:", 6) == 0) {
+            char* end = nullptr;
+            const long long n = strtoll(v + 6, &end, 10);
+            if (end != v + 6 && n >= 1) at = n;
+        }
+    });
+    return at;
+}
+
+cudaError_t dev_alloc(void** p, size_t bytes) {
+    static std::atomic<long long> count{0};
+    *p = nullptr;
+    const long long at = inject_alloc_at();
+    if (at > 0 && ++count == at) return cudaErrorMemoryAllocation;
+    return cudaMalloc(p, bytes);
 }
 
 bool is_device_ptr(const void* p) {
@@ -139,6 +164,27 @@ __global__ void k_hash_probe(int64_t n_calls, uint32_t k0, uint32_t k1, uint32_t
     if (acc == 0x9E3779B9u) atomicXor(sink, acc);
 }
 
+// Bounded-wait probe: n_tiles blocks take tiles in order from *counter and
+// run the decoupled look-back of the library's single-pass scans on status,
+// tile t contributing t + 1; out[t] = its exclusive prefix.  The block that
+// takes tile `silent` leaves without publishing, so the look-back of every
+// later tile that reaches it waits spin_limit polls, gives up and reports
+// ERR_TIMEOUT.  Every wait is bounded; nothing else is outstanding.
+__global__ void __launch_bounds__(32) k_wait_probe(unsigned long long* status, unsigned* counter, int32_t silent,
+                                                   int32_t spin_limit, int32_t* out) {
+    __shared__ int tile_sh;
+    if (threadIdx.x == 0) tile_sh = (int)atomicAdd(counter, 1u);
+    __syncwarp();
+    const int t = tile_sh;
+    if (t == silent) return;
+    bool late = false;
+    const int32_t x = chain_lookback(status, t, 0, t + 1, &late, spin_limit);
+    if (threadIdx.x == 0) {
+        out[t] = x;
+        if (late) dev_err(ERR_TIMEOUT);
+    }
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------- status
@@ -157,7 +203,8 @@ extern "C" int32_t sg_last_error(char* buf, size_t n) {
 extern "C" sg_status sg_stream_check(sg_stream_t stream) {
     cudaStream_t s = (cudaStream_t)stream;
     SG_CUDA(cudaStreamSynchronize(s));
-    unsigned w = fetch_err_api(s) | fetch_err_sampler(s) | fetch_err_gather(s) | fetch_err_aggregate(s);
+    unsigned w = fetch_err_api(s) | fetch_err_sampler(s) | fetch_err_gather(s) | fetch_err_aggregate(s) |
+               fetch_err_update(s);
     if (w & 0x80000000u) return fail(SG_ERR_CUDA, "sg_stream_check: could not read the device error word");
     if (w & ERR_INDEX) return fail(SG_ERR_INVALID_INDEX, "a kernel met a node ID or index out of range");
     if (w & ERR_CAPACITY) return fail(SG_ERR_CAPACITY, "a device table or buffer bound was exceeded");
@@ -183,10 +230,10 @@ extern "C" sg_status sg_graph_load(const void* h_indptr, int32_t offset_bits, co
     g->n_edges = n_edges;
     g->offset_bits = offset_bits;
     const size_t ob = offset_bits / 8;
-    cudaError_t e = cudaMalloc(&g->indptr, (size_t)(n_nodes + 1) * ob);
-    if (e == cudaSuccess) e = cudaMalloc((void**)&g->indices, (size_t)(n_edges > 0 ? n_edges : 1) * sizeof(int32_t));
+    cudaError_t e = dev_alloc(&g->indptr, (size_t)(n_nodes + 1) * ob);
+    if (e == cudaSuccess) e = dev_alloc((void**)&g->indices, (size_t)(n_edges > 0 ? n_edges : 1) * sizeof(int32_t));
     void* scratch = nullptr;
-    if (e == cudaSuccess) e = cudaMalloc(&scratch, 64);
+    if (e == cudaSuccess) e = dev_alloc(&scratch, 64);
     if (e == cudaSuccess) e = cudaMemcpy(g->indptr, h_indptr, (size_t)(n_nodes + 1) * ob, cudaMemcpyHostToDevice);
     if (e == cudaSuccess && n_edges > 0)
         e = cudaMemcpy(g->indices, h_indices, (size_t)n_edges * sizeof(int32_t), cudaMemcpyHostToDevice);
@@ -295,10 +342,10 @@ extern "C" sg_status sg_cache_build(const void* h_feat, const void* d_feat, int3
     }
     int32_t* d_ranked = nullptr;
     unsigned* d_bad = nullptr;
-    cudaError_t e = cudaMalloc((void**)&c->slot_of, (size_t)n_nodes * sizeof(int32_t));
-    if (e == cudaSuccess && n_cache > 0) e = cudaMalloc(&c->rows, (size_t)n_cache * (size_t)row_bytes);
-    if (e == cudaSuccess && h_ranked && n_cache > 0) e = cudaMalloc((void**)&d_ranked, (size_t)n_cache * sizeof(int32_t));
-    if (e == cudaSuccess) e = cudaMalloc((void**)&d_bad, sizeof(unsigned));
+    cudaError_t e = dev_alloc((void**)&c->slot_of, (size_t)n_nodes * sizeof(int32_t));
+    if (e == cudaSuccess && n_cache > 0) e = dev_alloc(&c->rows, (size_t)n_cache * (size_t)row_bytes);
+    if (e == cudaSuccess && h_ranked && n_cache > 0) e = dev_alloc((void**)&d_ranked, (size_t)n_cache * sizeof(int32_t));
+    if (e == cudaSuccess) e = dev_alloc((void**)&d_bad, sizeof(unsigned));
     if (e == cudaSuccess) e = cudaMemsetAsync(d_bad, 0, sizeof(unsigned), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(c->slot_of, 0xFF, (size_t)n_nodes * sizeof(int32_t), s);
     if (e == cudaSuccess && d_ranked)
@@ -359,6 +406,28 @@ extern "C" sg_status sg_read_probe(const void* d_src, int64_t bytes, uint32_t* d
     k_read_probe<<<blocks, 256, 0, (cudaStream_t)stream>>>((const uint4*)d_src, bytes / 16, d_sink);
     SG_CHECK_LAUNCH("k_read_probe");
     return SG_OK;
+}
+
+extern "C" sg_status sg_wait_probe(int32_t n_tiles, int32_t silent_tile, int32_t spin_limit, void* d_workspace,
+                                   size_t workspace_bytes, int32_t* d_out, sg_stream_t stream) {
+    if (n_tiles <= 0 || n_tiles > 4096 || spin_limit <= 0 || spin_limit > kLookbackSpins || !d_out || !d_workspace)
+        return fail(SG_ERR_INVALID_ARG, "sg_wait_probe: need 1..4096 tiles, a spin limit in 1..%d and buffers",
+                    kLookbackSpins);
+    const size_t need = sg_wait_probe_workspace(n_tiles);
+    if (workspace_bytes < need || ((uintptr_t)d_workspace) % 256)
+        return fail(SG_ERR_INVALID_ARG, "sg_wait_probe: workspace needs %zu bytes, 256-byte aligned", need);
+    cudaStream_t s = (cudaStream_t)stream;
+    unsigned long long* status = (unsigned long long*)d_workspace;
+    unsigned* counter = (unsigned*)(status + n_tiles);
+    SG_CUDA(cudaMemsetAsync(d_workspace, 0, need, s));
+    k_wait_probe<<<n_tiles, 32, 0, s>>>(status, counter, silent_tile, spin_limit, d_out);
+    SG_CHECK_LAUNCH("k_wait_probe");
+    return SG_OK;
+}
+
+extern "C" size_t sg_wait_probe_workspace(int32_t n_tiles) {
+    if (n_tiles <= 0) return 0;
+    return (size_t)n_tiles * sizeof(unsigned long long) + 256;
 }
 
 extern "C" sg_status sg_hash_probe(int64_t n_calls, uint64_t seed, uint32_t* d_sink, sg_stream_t stream) {

@@ -47,6 +47,14 @@ unsigned fetch_err_sampler(cudaStream_t);
 unsigned fetch_err_gather(cudaStream_t);
 unsigned fetch_err_aggregate(cudaStream_t);
 unsigned fetch_err_api(cudaStream_t);
+unsigned fetch_err_update(cudaStream_t);
+
+// ------------------------------------------------- allocation (owned memory)
+// Every device allocation the library owns goes through dev_alloc.  With the
+// environment variable SG_FAULT_INJECT=alloc:N (read once per process) the
+// N-th such allocation fails as if the device were out of memory, without
+// calling the CUDA runtime, so the OOM paths can be exercised on any host.
+cudaError_t dev_alloc(void** p, size_t bytes);
 
 // ------------------------------------------------------ dependent launches
 // Kernels of the per-batch path are launched with programmatic stream
@@ -165,9 +173,10 @@ __device__ __forceinline__ void st_release(unsigned long long* p, unsigned long 
 // Exclusive prefix of tile t in the chain whose first tile is t0.  Called by
 // all 32 lanes of one warp: the warp reads 32 predecessors at once, adds the
 // aggregates up to the closest inclusive prefix, and moves the window back by
-// 32 only while none is inclusive.
+// 32 only while none is inclusive.  A predecessor still empty after
+// spin_limit polls counts as an inclusive zero and sets *timed_out.
 __device__ __forceinline__ int32_t chain_lookback(unsigned long long* status, int t, int t0, int32_t agg,
-                                                  bool* timed_out) {
+                                                  bool* timed_out, int spin_limit = kLookbackSpins) {
     const int lane = (int)lane_id();
     if (t == t0) {
         if (lane == 0) st_release(status + t, (2ull << 32) | (uint32_t)agg);
@@ -182,7 +191,7 @@ __device__ __forceinline__ int32_t chain_lookback(unsigned long long* status, in
             int spins = 0;
             while (true) {
                 s = ld_acquire(status + p);
-                if ((s >> 32) == 1 || (s >> 32) == 2 || ++spins >= kLookbackSpins) break;
+                if ((s >> 32) == 1 || (s >> 32) == 2 || ++spins >= spin_limit) break;
                 __nanosleep(32);
             }
             if ((s >> 32) != 1 && (s >> 32) != 2) {

@@ -287,6 +287,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t per = (n_kt + (int32_t)gridDim.z - 1) / (int32_t)gridDim.z;
     const int32_t kt0 = min(n_kt, (int32_t)blockIdx.z * per), kt1 = min(n_kt, kt0 + per);
     const int n_k = kt1 - kt0;
+    if (EPI == EPI_SPLIT && n_k == 0) {
+        // a split with no K tiles: its partial tile is zero, and no MMA, copy
+        // or barrier is needed (the same in every thread)
+        float* dst = o0 + (size_t)blockIdx.z * kBM * ld1 + (size_t)(warp * 32 + lane) * ld1 + col0;
+        for (int j = 0; j < kBN && col0 + j < n_cols; ++j) dst[j] = 0.f;
+        return;
+    }
     uint8_t* tiles = dsm + ((1024 - (smem_addr(dsm) & 1023)) & 1023);
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -362,11 +369,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else o1[(size_t)r * ld1 + (c - split_col)] = v[j];
             }
         } else {
-            // the partial tile of split z (zeros when the split has no K tiles)
+            // the partial tile of split z
             float* dst = o0 + (size_t)blockIdx.z * kBM * ld1 + (size_t)r * ld1 + col0 + c0;
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-                if (col0 + c0 + j < n_cols) dst[j] = n_k > 0 ? v[j] : 0.f;
+                if (col0 + c0 + j < n_cols) dst[j] = v[j];
         }
     }
     tmem_fence_before();

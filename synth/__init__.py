@@ -69,6 +69,8 @@ def _load():
         lib.synth_features.argtypes = [i64, i64, i32, i32, u64, vp]
         lib.synth_batch_seeds.restype = i32
         lib.synth_batch_seeds.argtypes = [i64, dbl, u64, i64, i64, i32, vp]
+        lib.synth_epoch_order.restype = i64
+        lib.synth_epoch_order.argtypes = [i64, dbl, u64, i64, vp, i64]
         lib.synth_mask_count.restype = i64
         lib.synth_mask_count.argtypes = [i64, dbl, u64]
         _lib = lib
@@ -158,6 +160,13 @@ def batch_seeds(n: int, p_mask: float, batch: int, bsize: int, seed: int = 0, ep
     return out[:w].copy()
 
 
+def epoch_order(n: int, p_mask: float, seed: int, epoch: int, n_train: int) -> np.ndarray:
+    """Training nodes in the order of one epoch (batch b = entries [bB, (b+1)B))."""
+    out = np.empty(max(1, n_train), dtype=np.int32)
+    w = _load().synth_epoch_order(int(n), float(p_mask), int(seed), int(epoch), out.ctypes.data, int(n_train))
+    return out[:w]
+
+
 def mask_count(n: int, p_mask: float, seed: int = 0) -> int:
     return int(_load().synth_mask_count(int(n), float(p_mask), int(seed)))
 
@@ -170,8 +179,14 @@ class BatchStream:
     def __init__(self, w, epoch0: int = 0):
         self.w = w
         self.epoch0 = epoch0
-        self.per_epoch = max(1, mask_count(w.n_nodes, w.p_mask, w.rng_seed) // w.batch)
+        self.n_train = mask_count(w.n_nodes, w.p_mask, w.rng_seed)
+        self.per_epoch = max(1, self.n_train // w.batch)
+        self._epoch, self._order = None, None
 
     def seeds(self, b: int) -> np.ndarray:
         ep, i = divmod(int(b), self.per_epoch)
-        return batch_seeds(self.w.n_nodes, self.w.p_mask, i, self.w.batch, self.w.rng_seed, self.epoch0 + ep)
+        if self._epoch != ep:  # the epoch's order in one pass, kept for its batches
+            self._order = epoch_order(self.w.n_nodes, self.w.p_mask, self.w.rng_seed, self.epoch0 + ep,
+                                      self.n_train)
+            self._epoch = ep
+        return self._order[i * self.w.batch:(i + 1) * self.w.batch].copy()

@@ -283,6 +283,23 @@ int32_t synth_batch_seeds(int64_t n, double p_mask, uint64_t seed, int64_t epoch
     return w;
 }
 
+/* The whole epoch order of the training nodes (the sequence synth_batch_seeds
+ * slices), in one pass: writes up to cap IDs, returns how many. */
+int64_t synth_epoch_order(int64_t n, double p_mask, uint64_t seed, int64_t epoch, int32_t* out, int64_t cap) {
+    if (n <= 0 || cap < 0) return 0;
+    feistel_t perm = feistel_make(seed ^ (0xE90C0000ull + (uint64_t)epoch), n);
+    uint64_t thr = 0;
+    int all = p_mask >= 1.0;
+    if (!all) thr = (uint64_t)(p_mask * 18446744073709551616.0);
+    int64_t w = 0;
+    for (int64_t i = 0; i < n && w < cap; i++) {
+        int64_t v = feistel_apply(&perm, i);
+        if (!all && draw(seed, 4, (uint64_t)v) >= thr) continue;
+        out[w++] = (int32_t)v;
+    }
+    return w;
+}
+
 /* number of training nodes under the mask above */
 int64_t synth_mask_count(int64_t n, double p_mask, uint64_t seed) {
     if (p_mask >= 1.0) return n;

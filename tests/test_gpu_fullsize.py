@@ -2,9 +2,12 @@
 the launch configuration the benchmark uses (MiniBatchPipeline: sample,
 transpose, gather, forward, backward).
 
-The oracle recomputes what it can one by one: whole mini-batches of the
-sampler (two sub-batches of a super-batch), sampled rows of the gather, and
-sampled dst rows of every aggregation hop (each on the GPU's own input rows).
+The oracle recomputes: whole mini-batches of the sampler (two sub-batches of
+a super-batch), every gathered row, and every aggregation hop forward and
+backward (each on the GPU's own input rows) -- whole where the hop's arrays
+are small enough for the oracle's fp64 sums, else 20,000 sampled dst rows
+(forward) and src rows (backward) through the oracle on a sub-block that
+keeps each named dst row whole.
 """
 import gc
 
@@ -75,61 +78,90 @@ def _check_sampling(pipe, g, seeds_k, k, fanouts, seed):
         assert np.array_equal(blocks[h][1], ref.idx[h]), "idx, hop %d" % (h + 1)
 
 
-def _check_gather(pipe, feat, rng, n_check=3000):
+def _check_gather(pipe, feat):
+    """Every gathered row, byte for byte, against the oracle's gather of the
+    same IDs from the whole table."""
     H = pipe.H
     n = int(pipe.buf.counts[H].item())
-    rows = rng.choice(n, size=min(n, n_check), replace=False)
-    ids = _take(pipe.buf.unique, rows)
-    got = _take(pipe.x, rows)
-    assert np.array_equal(got, feat[ids])
+    ids = pipe.buf.unique[:n].cpu().numpy()
+    got = torch_to_np(pipe.x[:n])
+    assert np.array_equal(got, oracle.gather(feat, ids))
 
 
-def _check_aggregation(pipe, rng, dtype, n_check=600):
+# A hop is checked whole when its arrays fit this many elements (fp64 sums and
+# |term| sums of the oracle over the whole block); larger hops are checked on
+# n_check sampled rows, through the oracle on a sub-block with the same rows.
+FULL_ELEMS = 1 << 26
+
+
+def _row_edges(ip, rows):
+    """Edge positions of the given rows of a CSR, row after row."""
+    lens = ip[rows + 1] - ip[rows]
+    if lens.sum() == 0:
+        return np.zeros(0, np.int64)
+    first = np.repeat(ip[rows] - np.concatenate([[0], np.cumsum(lens)[:-1]]), lens)
+    return first + np.arange(int(lens.sum()))
+
+
+def _sub_block_fwd(ip, idx, rows):
+    """The dst rows `rows` of a block with their whole rows, over the distinct
+    srcs they name (returned for the caller to fetch)."""
+    sub_ip = np.concatenate([[0], np.cumsum(ip[rows + 1] - ip[rows])])
+    uniq, loc = np.unique(idx[_row_edges(ip, rows)], return_inverse=True)
+    return sub_ip, loc.astype(np.int32), uniq
+
+
+def _sub_block_bwd(ip, idx, n_src, srcs):
+    """The dst rows that name a src in `srcs`, each with its whole row (so its
+    count c_v is unchanged); srcs become columns 0..S-1 and every other src
+    the sink column S, whose result is dropped."""
+    col = np.full(n_src, len(srcs), np.int64)
+    col[srcs] = np.arange(len(srcs))
+    dst_of = np.repeat(np.arange(len(ip) - 1), np.diff(ip))
+    rows = np.unique(dst_of[col[idx] < len(srcs)])
+    sub_ip = np.concatenate([[0], np.cumsum(ip[rows + 1] - ip[rows])])
+    return sub_ip, col[idx[_row_edges(ip, rows)]].astype(np.int32), rows
+
+
+def _check_aggregation(pipe, rng, dtype, n_check=20000):
+    """Forward and backward of every hop against the oracle: the whole block
+    where it fits FULL_ELEMS, else n_check sampled dst rows (forward) and
+    src rows (backward), each on the GPU's own input rows."""
     H = pipe.H
     c = pipe.buf.counts.cpu().numpy()
+    dim = pipe.x.shape[1]
     for h in range(1, H + 1):
         n_dst, n_src = int(c[h - 1]), int(c[h])
         ip = pipe.buf.indptr[h - 1][: n_dst + 1].cpu().numpy().astype(np.int64)
         idx = pipe.buf.idx[h - 1][: ip[-1]].cpu().numpy()
-        # forward: sampled dst rows, on the GPU's own H_h
-        rows = rng.choice(n_dst, size=min(n_dst, n_check), replace=False)
-        sub_ip = np.concatenate([[0], np.cumsum(ip[rows + 1] - ip[rows])])
-        sub_idx = np.concatenate([idx[ip[r]:ip[r + 1]] for r in rows]) if len(rows) else np.zeros(0, np.int32)
-        uniq, loc = np.unique(sub_idx, return_inverse=True)
-        hin = _take(pipe.h_feat[h], uniq)
-        want, am = oracle.aggregate_fwd(sub_ip, loc.astype(np.int32), hin)
-        got = as_f64(_take(pipe.h_feat[h - 1], rows))
+        whole = n_src * dim <= FULL_ELEMS
+        # forward: out[v] = mean of H_h over row v
+        if whole:
+            want, am = oracle.aggregate_fwd(ip, idx, torch_to_np(pipe.h_feat[h][:n_src]))
+            got = as_f64(torch_to_np(pipe.h_feat[h - 1][:n_dst]))
+        else:
+            rows = np.sort(rng.choice(n_dst, size=min(n_dst, n_check), replace=False))
+            sub_ip, loc, uniq = _sub_block_fwd(ip, idx, rows)
+            want, am = oracle.aggregate_fwd(sub_ip, loc, _take(pipe.h_feat[h], uniq))
+            got = as_f64(_take(pipe.h_feat[h - 1], rows))
         assert_close(got, want, am, TOL[dtype], "forward hop %d" % h)
-        # backward: sampled src rows u, summing over the dst rows that name u
-        srcs = rng.choice(n_src, size=min(n_src, n_check), replace=False)
-        order = np.argsort(idx, kind="stable")
-        tptr = np.concatenate([[0], np.cumsum(np.bincount(idx, minlength=n_src))])
-        dst_of = np.repeat(np.arange(n_dst), np.diff(ip))
-        cnt = np.diff(ip)
-        gdst_all_rows = np.unique(np.concatenate([dst_of[order[tptr[u]:tptr[u + 1]]] for u in srcs]))
-        gd = _take(pipe.g_feat[h - 1], gdst_all_rows)
-        pos = {int(v): i for i, v in enumerate(gdst_all_rows)}
-        # a small transposed problem: one "dst" row per sampled src
-        b_ip, b_idx, b_w = [0], [], []
-        for u in srcs:
-            for e in order[tptr[u]:tptr[u + 1]]:
-                b_idx.append(pos[int(dst_of[e])])
-                b_w.append(1.0 / cnt[dst_of[e]])
-            b_ip.append(len(b_idx))
-        gdf = as_f64(gd)
-        want = np.zeros((len(srcs), gd.shape[1]))
-        am = np.zeros_like(want)
-        for i in range(len(srcs)):
-            for p in range(b_ip[i], b_ip[i + 1]):
-                want[i] += gdf[b_idx[p]] * b_w[p]
-                am[i] += np.abs(gdf[b_idx[p]]) * b_w[p]
-        got = as_f64(_take(pipe.g_feat[h], srcs))
+        # backward: gsrc[u] = sum over the rows v naming u of gdst[v] / c_v
+        if whole:
+            want, am = oracle.aggregate_bwd(ip, idx, n_src, torch_to_np(pipe.g_feat[h - 1][:n_dst]))
+            got = as_f64(torch_to_np(pipe.g_feat[h][:n_src]))
+        else:
+            srcs = np.sort(rng.choice(n_src, size=min(n_src, n_check), replace=False))
+            sub_ip, sub_idx, rows = _sub_block_bwd(ip, idx, n_src, srcs)
+            want, am = oracle.aggregate_bwd(sub_ip, sub_idx, len(srcs) + 1, _take(pipe.g_feat[h - 1], rows))
+            want, am = want[: len(srcs)], am[: len(srcs)]
+            got = as_f64(_take(pipe.g_feat[h], srcs))
         assert_close(got, want, am, TOL[dtype], "backward hop %d" % h)
 
 
 # ----------------------------------------------------------------- Skew
 SKEW = [("skew_g1.8_b512", (0, 7)), ("skew_g2.0_b512", (0, 7)), ("skew_g2.3_b512", (0, 7)),
-        ("skew_g2.6_b512", (0, 7)), ("skew_g2.0_b4096", (0, 3))]
+        ("skew_g2.6_b512", (0, 7)), ("skew_g1.8_b4096", (0, 5)), ("skew_g2.0_b4096", (0, 3)),
+        ("skew_g2.3_b4096", (2, 7)), ("skew_g2.6_b4096", (1, 6))]
 
 
 @pytest.mark.parametrize("name,check_subs", SKEW)
@@ -152,7 +184,7 @@ def test_skew_super_batch_full_size(name, check_subs):
     for k in check_subs:
         _check_sampling(pipe, g, seed_lists[k], k, w.fanouts, seed)
     rng = np.random.default_rng(1)
-    _check_gather(pipe, feat, rng)
+    _check_gather(pipe, feat)
     _check_aggregation(pipe, rng, w.dtype)
     del pipe, cache, G, feat
     gc.collect()
@@ -183,7 +215,7 @@ def test_host_feature_workloads_full_size(name):
         assert misses > 0 and hits > 0  # both the HBM cache and the host table were read
         _check_sampling(pipe, g, seeds, 0, w.fanouts, w.sampler_seed(0))
         rng = np.random.default_rng(2)
-        _check_gather(pipe, table.arr, rng)
+        _check_gather(pipe, table.arr)
         _check_aggregation(pipe, rng, w.dtype)
         del pipe, cache
     finally:
