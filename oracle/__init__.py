@@ -69,6 +69,12 @@ def _load():
         lib.orc_sage_fwd.argtypes = [vp, vp, i32, vp, i32, i64, i32, i32, vp, vp, vp]
         lib.orc_sage_bwd.restype = None
         lib.orc_sage_bwd.argtypes = [vp, vp, i32, vp, i32, vp, vp, i32, i64, i32, i32, vp, vp, vp, vp, vp]
+        lib.orc_access_stats.restype = None
+        lib.orc_access_stats.argtypes = [vp, vp, i32, vp, ctypes.c_uint32, vp]
+        lib.orc_rank_by_score.restype = None
+        lib.orc_rank_by_score.argtypes = [vp, i64, vp, vp]
+        lib.orc_graph_renumber.restype = None
+        lib.orc_graph_renumber.argtypes = [vp, vp, i64, vp, vp, vp, vp]
         _lib = lib
         return lib
 
@@ -305,6 +311,41 @@ def sage_bwd(h: np.ndarray, m: np.ndarray, W: np.ndarray, y: np.ndarray, g: np.n
     _load().orc_sage_bwd(_p(hh), _p(mm), _dtype_code(hh), _p(ww), _dtype_code(ww), _p(yy), _p(gg), _dtype_code(gg),
                          n, d, d_out, _p(dW), _p(am_w), _p(dh), _p(dm), _p(am_z))
     return dW, am_w, dh, dm, am_z
+
+
+def access_stats(blocks: Blocks, omega, w_in: int, score: np.ndarray) -> None:
+    """Adds the full-link access statistics (Eq. (4)) of one mini-batch to
+    score (uint32 [n_nodes], updated in place)."""
+    assert score.dtype == np.uint32 and score.flags.c_contiguous
+    om = np.ascontiguousarray(omega, dtype=np.uint32)
+    if len(om) != blocks.n_hops:
+        raise ValueError("access_stats: one weight per hop")
+    hop = np.ascontiguousarray(blocks.hop_off, dtype=np.int64)
+    un = np.ascontiguousarray(blocks.unique, dtype=np.int32)
+    _load().orc_access_stats(_p(un), _p(hop), blocks.n_hops, _p(om), int(w_in), _p(score))
+
+
+def rank_by_score(score: np.ndarray):
+    """(order, rank_of): nodes by descending score, ties by ascending ID."""
+    sc = np.ascontiguousarray(score, dtype=np.uint32)
+    n = len(sc)
+    order = np.zeros(max(1, n), np.int32)
+    rank_of = np.zeros(max(1, n), np.int32)
+    _load().orc_rank_by_score(_p(sc), n, _p(order), _p(rank_of))
+    return order[:n], rank_of[:n]
+
+
+def graph_renumber(indptr, indices, order, rank_of):
+    """The CSR with node order[r] renamed r; returns (indptr int64, indices int32)."""
+    ip = np.ascontiguousarray(indptr, dtype=np.int64)
+    ix = np.ascontiguousarray(indices, dtype=np.int32)
+    od = np.ascontiguousarray(order, dtype=np.int32)
+    rk = np.ascontiguousarray(rank_of, dtype=np.int32)
+    n = len(ip) - 1
+    new_ip = np.zeros(n + 1, np.int64)
+    new_ix = np.zeros(max(1, len(ix)), np.int32)
+    _load().orc_graph_renumber(_p(ip), _p(ix), n, _p(od), _p(rk), _p(new_ip), _p(new_ix))
+    return new_ip, new_ix[: len(ix)]
 
 
 def bf16_to_f32(bits: np.ndarray) -> np.ndarray:

@@ -366,3 +366,58 @@ void orc_sage_bwd(const void* h, const void* m, int dtype, const void* W, int wt
         }
     }
 }
+
+/* ------------------------------------------------- cache presampling (NEXT) */
+/* Full-link access statistics of one sampled mini-batch (GARDEN page, Section
+ * IV-B, Eq. (4)): every node v of the batch adds
+ *   W_feat(v) = w_in * 1(v in V_in) + sum_{l=1..L} omega_l * (1(v in V_src^(l)) + 1(v in V_dst^(l)))
+ * to score[v].  Layer l is hop l of the sample: its src nodes are V_l and its
+ * dst nodes V_{l-1}; the input nodes V_in are V_L, the nodes whose features
+ * are gathered.  The nodes of V_h are the first hop_off[h] entries of unique.
+ * Readings: the page gives no values for the layer weights omega_l, so they
+ * are inputs (integers, so that sums are exact and independent of order);
+ * w_in = 1, omega = 0 is the plain count of gathered appearances. */
+void orc_access_stats(const int32_t* unique, const int64_t* hop_off, int32_t n_hops, const uint32_t* omega,
+                      uint32_t w_in, uint32_t* score) {
+    int64_t n_in = hop_off[n_hops];
+    for (int64_t i = 0; i < n_in; i++) {
+        uint32_t w = w_in;  /* every node of the batch is an input node */
+        for (int32_t l = 1; l <= n_hops; l++) {
+            int in_src = i < hop_off[l];      /* v in V_l     */
+            int in_dst = i < hop_off[l - 1];  /* v in V_{l-1} */
+            w += omega[l - 1] * (uint32_t)(in_src + in_dst);
+        }
+        score[unique[i]] += w;
+    }
+}
+
+/* Nodes by descending score, ties by ascending ID: order[r] is the node of
+ * rank r and rank_of[v] the rank of node v (the new ID a node gets when hot
+ * nodes are recoded to the smallest IDs, GARDEN page Section IV-A). */
+static const uint32_t* g_rank_score;
+static int cmp_rank(const void* a, const void* b) {
+    int32_t u = *(const int32_t*)a, v = *(const int32_t*)b;
+    if (g_rank_score[u] != g_rank_score[v]) return g_rank_score[u] > g_rank_score[v] ? -1 : 1;
+    return (u > v) - (u < v);
+}
+
+void orc_rank_by_score(const uint32_t* score, int64_t n, int32_t* order, int32_t* rank_of) {
+    for (int64_t v = 0; v < n; v++) order[v] = (int32_t)v;
+    g_rank_score = score;
+    qsort(order, (size_t)n, sizeof(int32_t), cmp_rank);
+    for (int64_t r = 0; r < n; r++) rank_of[order[r]] = (int32_t)r;
+}
+
+/* The graph with node order[r] renamed r (GARDEN page, Section IV-A: compact
+ * IDs for high-frequency nodes): new row r is old row order[r], position for
+ * position, with every neighbour u written as rank_of[u]. */
+void orc_graph_renumber(const int64_t* indptr, const int32_t* indices, int64_t n, const int32_t* order,
+                        const int32_t* rank_of, int64_t* new_indptr, int32_t* new_indices) {
+    new_indptr[0] = 0;
+    for (int64_t r = 0; r < n; r++) {
+        int64_t v = order[r];
+        int64_t deg = indptr[v + 1] - indptr[v];
+        for (int64_t j = 0; j < deg; j++) new_indices[new_indptr[r] + j] = rank_of[indices[indptr[v] + j]];
+        new_indptr[r + 1] = new_indptr[r] + deg;
+    }
+}

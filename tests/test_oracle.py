@@ -452,3 +452,91 @@ def test_sage_bwd_zero_where_relu_is_off():
     assert dh.tolist() == [[0, 0, 1], [0, 0, 0]] and dm.tolist() == dh.tolist()
     # only (row 0, output 2) is active, with dy = 1: dW's row 2 is z's row 0
     assert dW.tolist() == [[0] * 6, [0] * 6, [1, -2, 3, -1, 1, 1]]
+
+
+# ----------------------------------------------- full-link statistics, recoding
+def _golden_access_stats():
+    rows = {}
+    scores = {}
+    for line in open(os.path.join(GOLDEN, "access_stats_example.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        k, *v = line.split()
+        if k == "score":
+            scores[int(v[0])] = int(v[1])
+        else:
+            rows[k] = [int(x) for x in v]
+    return rows, scores
+
+
+def test_access_stats_worked_example():
+    rows, scores = _golden_access_stats()
+    b = oracle.Blocks(np.array(rows["unique"], np.int32), rows["hop_off"], [None] * 2, [None] * 2, [], [])
+    score = np.zeros(10, np.uint32)
+    oracle.access_stats(b, rows["omega"], rows["w_in"][0], score)
+    for v in range(10):
+        assert score[v] == scores.get(v, 0), v
+
+
+def _sampled_batches(n_batches=6):
+    g = synth.chung_lu(3000, 8.0, 2.1, 200.0, 5)
+    out = []
+    for k in range(n_batches):
+        seeds = synth.batch_seeds(g.n, 1.0, k, 50, 5)
+        out.append(oracle.sampler_run(g.indptr, g.indices, seeds, [6, 4, 3], 77 + k))
+    return g, out
+
+
+def test_access_stats_plain_count_and_closed_form_total():
+    g, runs = _sampled_batches()
+    # w_in = 1, omega = 0: the conventional count of gathered appearances
+    plain = np.zeros(g.n, np.uint32)
+    for r in runs:
+        oracle.access_stats(r, [0, 0, 0], 1, plain)
+    assert np.array_equal(plain, np.bincount(np.concatenate([r.unique for r in runs]), minlength=g.n))
+    # the total over nodes: w_in |V_L| + sum_l omega_l (|V_l| + |V_{l-1}|), per batch
+    om, w_in = [2, 7, 3], 4
+    score = np.zeros(g.n, np.uint32)
+    want = 0
+    for r in runs:
+        oracle.access_stats(r, om, w_in, score)
+        off = r.hop_off
+        want += w_in * off[3] + sum(om[l - 1] * (off[l] + off[l - 1]) for l in (1, 2, 3))
+    assert int(score.astype(np.int64).sum()) == want
+    # linear in the weights
+    a = np.zeros(g.n, np.uint32)
+    b = np.zeros(g.n, np.uint32)
+    for r in runs:
+        oracle.access_stats(r, [1, 0, 2], 0, a)
+        oracle.access_stats(r, [1, 7, 1], 4, b)
+    assert np.array_equal(a + b, score)
+
+
+def test_rank_by_score_matches_lexsort():
+    rng = np.random.default_rng(3)
+    score = rng.integers(0, 6, size=5000).astype(np.uint32)  # many ties
+    order, rank_of = oracle.rank_by_score(score)
+    want = np.lexsort((np.arange(5000), -score.astype(np.int64)))
+    assert np.array_equal(order, want)
+    assert np.array_equal(rank_of[order], np.arange(5000))
+
+
+def test_graph_renumber_is_the_permuted_matrix():
+    import scipy.sparse as sp
+    g = synth.chung_lu(2000, 9.0, 2.1, 150.0, 2)
+    rng = np.random.default_rng(4)
+    order = rng.permutation(g.n).astype(np.int32)
+    rank_of = np.empty_like(order)
+    rank_of[order] = np.arange(g.n, dtype=np.int32)
+    ip, ix = oracle.graph_renumber(g.indptr, g.indices, order, rank_of)
+    A = sp.csr_matrix((np.ones(g.m), g.indices, g.indptr), shape=(g.n, g.n))
+    B = sp.csr_matrix((np.ones(len(ix)), ix, ip), shape=(g.n, g.n))
+    assert (A[order][:, order] != B).nnz == 0  # new (r, c) = old (order[r], order[c])
+    assert np.array_equal(np.diff(ip), np.diff(g.indptr)[order])
+    # renumbering back with the inverse permutation gives the graph back,
+    # position for position
+    ip2, ix2 = oracle.graph_renumber(ip, ix, rank_of, order)
+    assert np.array_equal(ip2, g.indptr) and np.array_equal(ix2, g.indices)
+    ip3, ix3 = oracle.graph_renumber(g.indptr, g.indices, np.arange(g.n, dtype=np.int32),
+                                     np.arange(g.n, dtype=np.int32))
+    assert np.array_equal(ip3, g.indptr) and np.array_equal(ix3, g.indices)
