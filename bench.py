@@ -33,6 +33,15 @@ import synth  # noqa: E402
 METRIC = "sampled edges/s, gathered feature GB/s, batch latency; % of memory roofline"
 
 
+def log(msg: str) -> None:
+    """Progress on stderr (the JSON line alone goes to stdout)."""
+    sys.stderr.write("[bench %.1fs] %s\n" % (time.time() - _T0, msg))
+    sys.stderr.flush()
+
+
+_T0 = time.time()
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -40,6 +49,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="billion")
+    ap.add_argument("--no-recode", action="store_true",
+                    help="keep the original node IDs and a slot-map cache of the ranked rows")
+    ap.add_argument("--omega", default="", help="layer weights of the access statistics, comma-separated (default 1s)")
+    ap.add_argument("--w-in", type=int, default=1, help="input-node weight of the access statistics")
     ap.add_argument("--min-seconds", type=float, default=2.0,
                     help="the timed region of --steps steps is repeated (new batches each time) until this long")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="bound on the CPU-baseline sample")
@@ -162,9 +175,12 @@ class Clocks:
 
 # ------------------------------------------------------------------ workload
 class Workload:
-    """Graph, features and batches of one config, built once per process."""
+    """Graph, features and batches of one config, built once per process.
+    With recode=True (the HBM cache holds part of the table) the feature
+    table is not filled here: run_ours recodes the graph first (hot nodes to
+    the smallest IDs) and fills the table in the new order."""
 
-    def __init__(self, name: str, pinned_features: bool):
+    def __init__(self, name: str, pinned_features: bool, recode: bool = False):
         import torch
         self.w = synth.workload(name)
         w = self.w
@@ -178,13 +194,25 @@ class Workload:
             self.feat = pinned_table(w.n_nodes, w.dim, dt)
         else:
             self.feat = torch.empty((w.n_nodes, w.dim), dtype=dt)
-        synth.features_into(self.feat.data_ptr(), 0, w.n_nodes, w.dim, w.dtype, w.rng_seed)
+        self.rank_of = None  # new ID of each node once recoded
+        if not recode:
+            synth.features_into(self.feat.data_ptr(), 0, w.n_nodes, w.dim, w.dtype, w.rng_seed)
         self.t_feat = time.time() - t0
         self.batches = synth.BatchStream(w, epoch0=0)
         self.presample = synth.BatchStream(w, epoch0=1000)  # a separate series of epochs
 
+    def recoded(self, order: np.ndarray, rank_of: np.ndarray, indptr: np.ndarray, indices: np.ndarray) -> None:
+        """Switches to the recoded graph: row r of the feature table becomes
+        node order[r]'s row, and seeds are mapped through rank_of."""
+        t0 = time.time()
+        synth.features_rows_into(self.feat.data_ptr(), order, self.w.dim, self.w.dtype, self.w.rng_seed)
+        self.t_feat += time.time() - t0
+        self.rank_of = rank_of
+        self.g = synth.csr_graph(np.asarray(indptr, dtype=np.int64), indices)
+
     def seeds(self, batch: int) -> np.ndarray:
-        return self.batches.seeds(batch)
+        s = self.batches.seeds(batch)
+        return s if self.rank_of is None else self.rank_of[s]
 
 
 def replica_batches(rank: int, world: int, n: int):
@@ -233,7 +261,7 @@ def kernels_per_step(H: int, n_sub: int, by_region: bool = False) -> int:
 def run_ours(args, rank, world, local):
     import torch
     from sampling_gnn_mini_gb300 import binding as sg
-    from sampling_gnn_mini_gb300.pipeline import MiniBatchPipeline, OverlappedPipeline
+    from sampling_gnn_mini_gb300.pipeline import MiniBatchPipeline, OverlappedPipeline, rank_by_access
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -241,29 +269,47 @@ def run_ours(args, rank, world, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     sg.load(build_if_missing=True)
-    W = Workload(args.config, pinned_features=True)
+    w0 = synth.workload(args.config)
+    recode = w0.cache_rows < w0.n_nodes and not args.no_recode
+    W = Workload(args.config, pinned_features=True, recode=recode)
     w, g = W.w, W.g
     H = w.n_hops
     R = w.row_bytes
     hbm_peak, peak_kind = peaks()
+    log("workload %s: graph %.1fs, feature table %.1fs" % (w.name, W.t_graph, W.t_feat))
 
     # graph into HBM; int64 offsets where the config calls for them
     G = sg.sg_graph_load(g.indptr if w.offset_bits == 64 else g.indptr.astype(np.int32), g.indices, w.offset_bits)
     cache_rows = w.cache_rows
-    # rank nodes by presampled frequency in V_H: batches disjoint from the measured ones
+    omega = [int(x) for x in args.omega.split(",")] if args.omega else [1] * H
+    presample = None
+    # rank nodes by their full-link access statistics (Eq. (4)) over presampled
+    # batches disjoint from the measured ones, all on the GPU; then recode the
+    # graph so that the hot nodes hold the smallest IDs (ID-range cache)
     if cache_rows < w.n_nodes:
-        full = sg.sg_cache_build(W.feat, None, sg.SG_F32 if w.dtype == "f32" else sg.SG_BF16, w.n_nodes, w.dim,
-                                 np.zeros(0, np.int32), 0)
-        pre = MiniBatchPipeline(G, full, w.fanouts, w.batch, backward=False, device=dev)
-        freq = np.zeros(w.n_nodes, np.int64)
-        for b in range(w.presample_batches):
-            s = W.presample.seeds(b)
-            pre.set_batch(torch.from_numpy(s).to(dev), w.presample_seed(b))
-            pre.sample()
-            n_h = int(pre.counts[H].item())
-            np.add.at(freq, pre.buf.unique[:n_h].cpu().numpy(), 1)
-        ranked = np.lexsort((np.arange(w.n_nodes), -freq))[:cache_rows].astype(np.int32)
-        del pre, full
+        t0 = time.time()
+        pre_batches = ((torch.from_numpy(W.presample.seeds(b)).to(dev), w.presample_seed(b))
+                       for b in range(w.presample_batches))
+        order, rank_of = rank_by_access(G, pre_batches, w.fanouts, omega, args.w_in, device=dev)
+        torch.cuda.synchronize(dev)
+        sg.sg_stream_check()
+        presample = {"batches": w.presample_batches, "omega": omega, "w_in": args.w_in,
+                     "statistics_and_rank_s": time.time() - t0}
+        if recode:
+            t0 = time.time()
+            G2 = sg.sg_graph_renumber(G, order, rank_of)
+            del G
+            G = G2
+            presample["recode_graph_s"] = time.time() - t0
+            ip, ix = sg.sg_graph_copy_out(G)  # the recoded CSR, for the host-side bookkeeping and oracle
+            W.recoded(order.cpu().numpy(), rank_of.cpu().numpy(), ip, ix)
+            del ip, ix
+            g = W.g
+            ranked = None  # ID-range cache: nodes [0, cache_rows)
+        else:
+            ranked = order[:cache_rows].cpu().numpy()
+        del order, rank_of
+        log("presample %s" % presample)
     else:
         ranked = None
     dtype_code = sg.SG_F32 if w.dtype == "f32" else sg.SG_BF16
@@ -431,6 +477,7 @@ def run_ours(args, rank, world, local):
     # a first region on the warm-up pool's last K batches sizes the repeats
     calib_ms = timed_region(seeds_pool, hseed_pool, args.warmup, counts_log)
     repeats = max(1, int(np.ceil(args.min_seconds * 1e3 / max(calib_ms, 1e-3))))
+    log("calibration region %.2f ms for %d steps: %d timed regions" % (calib_ms, args.steps, repeats))
     if world > 1:  # every rank runs the same number of regions
         r_t = torch.tensor([repeats], dtype=torch.int64, device=dev)
         torch.distributed.all_reduce(r_t, op=torch.distributed.ReduceOp.MAX)
@@ -444,6 +491,7 @@ def run_ours(args, rank, world, local):
     region_ms = [timed_region(rep_seeds, rep_hseed, r * args.steps, rep_log) for r in range(repeats)]
     torch.cuda.nvtx.range_pop()
     clk = clocks.stop()
+    log("timed regions done: %s ms" % ", ".join("%.2f" % x for x in region_ms[:8]))
     rep_counts = rep_log.cpu().numpy().astype(np.int64)
     region_edges = [int(rep_counts[r * args.steps:(r + 1) * args.steps, H + 1: 2 * H + 1].sum())
                     for r in range(repeats)]
@@ -560,7 +608,7 @@ def run_ours(args, rank, world, local):
     if dom == "gather":
         ach_bytes = (gather_host if stage_roof["gather"]["bound"] == "host_link" else gather_hbm) / args.steps
         peak = link_gbs if stage_roof["gather"]["bound"] == "host_link" else hbm_peak
-        roof = {"kernel": "gather stage (%s a step)" % ("k_gather" if not pipe.gather_ws[0] else
+        roof = {"kernel": "gather stage (%s a step)" % ("k_gather" if pipe.gather_ws[0] is None else
                                                          "k_gather, k_region_scan, k_region_scatter, k_gather_list"),
                 "bound": stage_roof["gather"]["bound"],
                 "achieved": ach_bytes / (stage_ms["gather"] / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
@@ -608,6 +656,8 @@ def run_ours(args, rank, world, local):
                     "none: one batch at a time, a step graph each (misses come from a host table read by region, "
                     "which concurrent gathers would interleave)") +
                    ". batch_latency_ms is one batch alone (a step graph per batch, batches back to back)",
+        "presample": presample,
+        "recoded": W.rank_of is not None,
         "host_table": None if not w.host_features else {
             "bytes": w.n_nodes * R,
             "huge_page_bytes": getattr(getattr(W.feat, "_sg_owner", None), "huge", 0),

@@ -111,6 +111,11 @@ sg_status sg_graph_destroy(sg_graph* g);
 sg_status sg_graph_info(const sg_graph* g, int64_t* n_nodes, int64_t* n_edges, int32_t* offset_bits,
                         int64_t* max_degree);
 
+/* Copies a loaded graph's CSR back to host memory (synchronous): h_indptr
+ * gets n_nodes + 1 offsets of the graph's offset width, h_indices n_edges
+ * int32 IDs; for example to keep a recoded graph (sg_graph_renumber). */
+sg_status sg_graph_copy_out(const sg_graph* g, void* h_indptr, int32_t* h_indices);
+
 /* ---------------------------------------------------------------- sampling */
 /* Worst-case sizes of one sampler_run, so the caller can preallocate.
  * Counts are totals over the n_sub mini-batches of a super-batch. */
@@ -254,16 +259,21 @@ sg_status sg_relabel_noalloc(const int32_t* d_ids, int64_t n_ids, const int32_t*
  *   d_feat        optional device copy of the whole table to fill the cache
  *                 from (NULL: read the rows from h_feat).
  *   h_ranked      host, n_cache distinct node IDs; h_ranked[s] goes to cache
- *                 slot s.  NULL with n_cache = n_nodes caches every node with
- *                 slot = ID.
- * The library allocates n_cache rows plus an n_nodes int32 slot map in HBM. */
+ *                 slot s, and a map of n_nodes int32 slots says where each
+ *                 node is.  NULL caches the ID range [0, n_cache) with slot =
+ *                 ID and no map: the hit test is ID < n_cache (GARDEN page
+ *                 Section IV-A, hot nodes recoded to the smallest IDs; see
+ *                 sg_graph_renumber).  That is also the form for a whole
+ *                 table (n_cache = n_nodes).
+ * The library allocates n_cache rows (plus the slot map with h_ranked) in HBM. */
 sg_status sg_cache_build(const void* h_feat, const void* d_feat, int32_t dtype, int64_t n_nodes, int32_t dim,
                          const int32_t* h_ranked, int64_t n_cache, sg_cache** out, sg_stream_t stream);
 
 /* Frees the cache's device memory (synchronous).  NULL is a no-op. */
 sg_status sg_cache_destroy(sg_cache* c);
 
-/* Device view of a cache (for callers that want to inspect it). */
+/* Device view of a cache (for callers that want to inspect it); *d_slot_of
+ * is NULL for an ID-range cache (built without h_ranked). */
 sg_status sg_cache_info(const sg_cache* c, int64_t* n_nodes, int32_t* dim, int32_t* dtype, int64_t* n_cache,
                         const int32_t** d_slot_of);
 
@@ -365,6 +375,52 @@ sg_status sg_transpose_blocks(const sg_blocks* blocks, const int64_t* max_nodes,
 sg_status sg_aggregate_bwd_t(const int32_t* d_tptr, const int32_t* d_tdst, const float* d_tw, int32_t n_src_cap,
                              int32_t n_dst_cap, const int32_t* d_dims, const void* d_gdst, int32_t dtype_in,
                              int32_t dim, void* d_gsrc, int32_t dtype_out, sg_stream_t stream);
+
+/* ------------------------------------- cache presampling and node recoding */
+/* Full-link access statistics (GARDEN page Section IV-B, Eq. (4)) of one
+ * sampler_run output, for ranking nodes before the cache is built: every node
+ * v of every mini-batch adds
+ *   W_feat(v) = w_in + sum_{l=1..H} omega[l-1] * (1(v in V_l) + 1(v in V_{l-1}))
+ * to d_score[v] (layer l's src nodes are V_l, its dst nodes V_{l-1}; every
+ * node of the output is an input node, V_in = V_H).  The page leaves the
+ * layer weights open; they are integers here, so the sums are exact and
+ * do not depend on the order of the atomic adds.  w_in = 1, omega = 0 counts
+ * gathered appearances.  Sums wrap modulo 2^32.
+ *   blocks, unique_cap  the sampler output and the capacity of its unique
+ *                       array (bounds.max_nodes[H]); counts are read on the
+ *                       device
+ *   h_omega      host, n_hops weights
+ *   d_score      device uint32 [n_nodes], accumulated (+=)
+ * A node ID outside [0, n_nodes) sets the device error word. */
+sg_status sg_access_stats(const sg_blocks* blocks, int64_t unique_cap, int32_t n_hops, int32_t n_sub,
+                          const uint32_t* h_omega, uint32_t w_in, uint32_t* d_score, int64_t n_nodes,
+                          sg_stream_t stream);
+
+/* Nodes ordered by descending score, ties by ascending ID: d_order[r]
+ * (device int32 [n_nodes]) is the node of rank r and, when d_rank_of is not
+ * NULL, d_rank_of[v] (device int32 [n_nodes]) the rank of node v.  A stable
+ * radix sort; the result is deterministic.  Workspace:
+ * sg_rank_workspace(n_nodes) bytes, 256-byte aligned (0 on bad sizes). */
+size_t sg_rank_workspace(int64_t n_nodes);
+sg_status sg_rank_by_score(const uint32_t* d_score, int64_t n_nodes, int32_t* d_order, int32_t* d_rank_of,
+                           void* d_workspace, size_t workspace_bytes, sg_stream_t stream);
+
+/* Recodes a graph's nodes (GARDEN page Section IV-A: the allocator gives the
+ * high-frequency nodes compact IDs): the new graph's row r is the old row
+ * d_order[r], position for position, with every neighbour u written as
+ * d_rank_of[u].  With the order of sg_rank_by_score the hot nodes take the
+ * smallest IDs, so an ID-range cache (sg_cache_build without h_ranked) of
+ * the top C rows is hit exactly when ID < C, and the rows a batch misses
+ * sit in a compact, rank-ordered part of the host table.  The caller lays the
+ * feature table out in the new order (new row r = old row d_order[r]) and
+ * maps seed IDs through d_rank_of.  Sampling the new graph is sampling a
+ * graph like any other: the hash takes the new IDs.
+ *   d_order, d_rank_of  device int32 [n_nodes], inverse permutations of
+ *               [0, n_nodes) (checked: SG_ERR_INVALID_ARG otherwise)
+ * One-time and synchronous on `stream`; *out receives a new handle (same
+ * offset width) freed by sg_graph_destroy. */
+sg_status sg_graph_renumber(const sg_graph* g, const int32_t* d_order, const int32_t* d_rank_of, sg_graph** out,
+                            sg_stream_t stream);
 
 /* ----------------------------------------------------- SAGE UPDATE (GEMM) */
 /* The UPDATE of one GraphSAGE layer (GARDEN page Section II-A, Eq. (2); the

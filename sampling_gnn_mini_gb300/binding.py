@@ -42,7 +42,8 @@ EXPORTS = ["sg_version", "sg_last_error", "sg_stream_check", "sg_graph_load", "s
            "sg_cache_destroy", "sg_cache_info", "sg_gather", "sg_aggregate_fwd", "sg_aggregate_bwd_workspace",
            "sg_aggregate_bwd", "sg_read_probe", "sg_hash_probe", "sg_relabel_noalloc", "sg_transpose_workspace",
            "sg_transpose_blocks", "sg_aggregate_bwd_t", "sg_sampler_workspace_init", "sg_gather_workspace",
-           "sg_sage_fwd", "sg_sage_bwd", "sg_sage_bwd_workspace", "sg_wait_probe", "sg_wait_probe_workspace"]
+           "sg_sage_fwd", "sg_sage_bwd", "sg_sage_bwd_workspace", "sg_wait_probe", "sg_wait_probe_workspace",
+           "sg_access_stats", "sg_rank_workspace", "sg_rank_by_score", "sg_graph_renumber", "sg_graph_copy_out"]
 
 
 class SgError(RuntimeError):
@@ -124,6 +125,11 @@ def load(build_if_missing: bool = True):
             "sg_sampler_workspace_init": (i32, [vp, i32, vp, i32, vp, i32, vp, sz, vp]),
             "sg_wait_probe": (i32, [i32, i32, i32, vp, sz, vp, vp]),
             "sg_wait_probe_workspace": (sz, [i32]),
+            "sg_access_stats": (i32, [ctypes.POINTER(_Blocks), i64, i32, i32, vp, ctypes.c_uint32, vp, i64, vp]),
+            "sg_rank_workspace": (sz, [i64]),
+            "sg_rank_by_score": (i32, [vp, i64, vp, vp, vp, sz, vp]),
+            "sg_graph_renumber": (i32, [vp, vp, vp, ctypes.POINTER(vp), vp]),
+            "sg_graph_copy_out": (i32, [vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -212,6 +218,27 @@ def sg_graph_load(indptr: np.ndarray, indices: np.ndarray, offset_bits: Optional
     return Graph(out.value)
 
 
+def sg_graph_renumber(graph: Graph, order: torch.Tensor, rank_of: torch.Tensor, stream=None) -> Graph:
+    """The graph with node order[r] renamed r (device int32 permutations;
+    see include/sg.h)."""
+    for t in (order, rank_of):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous() or t.numel() != graph.n_nodes:
+            raise SgError(SG_ERR_INVALID_ARG, "sg_graph_renumber: order and rank_of must be contiguous int32 "
+                                              "device tensors of n_nodes entries")
+    out = ctypes.c_void_p()
+    _check(load().sg_graph_renumber(graph.handle, order.data_ptr(), rank_of.data_ptr(), ctypes.byref(out),
+                                    _stream(stream)))
+    return Graph(out.value)
+
+
+def sg_graph_copy_out(graph: Graph):
+    """(indptr, indices) of a loaded graph as host numpy arrays."""
+    ip = np.empty(graph.n_nodes + 1, dtype=np.int64 if graph.offset_bits == 64 else np.int32)
+    ix = np.empty(max(1, graph.n_edges), dtype=np.int32)
+    _check(load().sg_graph_copy_out(graph.handle, ip.ctypes.data, ix.ctypes.data))
+    return ip, ix[: graph.n_edges]
+
+
 # ---------------------------------------------------------------- sampling
 @dataclass
 class Bounds:
@@ -291,6 +318,35 @@ def sg_sampler_run(graph: Graph, seeds: torch.Tensor, fanouts: Sequence[int], se
                                  fo.ctypes.data, len(fo), ctypes.c_uint64(seed & 0xFFFFFFFFFFFFFFFF), _ptr(d_seed),
                                  buffers.workspace.data_ptr(), buffers.workspace.numel(),
                                  ctypes.byref(buffers._blocks), evs, _stream(stream)))
+
+
+def sg_access_stats(buffers: "SampleBuffers", omega: Sequence[int], w_in: int, score: torch.Tensor, n_sub: int = 1,
+                    stream=None) -> None:
+    """Adds the full-link access statistics (Eq. (4)) of the sampler output in
+    buffers to score (device uint32 / int32 [n_nodes]); see include/sg.h."""
+    om = np.ascontiguousarray(omega, dtype=np.uint32)
+    if len(om) != buffers.n_hops:
+        raise SgError(SG_ERR_INVALID_ARG, "sg_access_stats: one weight per hop")
+    if score.element_size() != 4 or score.is_floating_point() or not score.is_cuda or not score.is_contiguous():
+        raise SgError(SG_ERR_INVALID_ARG, "sg_access_stats: score must be a 32-bit device tensor")
+    _check(load().sg_access_stats(ctypes.byref(buffers._blocks), buffers.unique.numel(), buffers.n_hops, int(n_sub),
+                                  om.ctypes.data, int(w_in), score.data_ptr(), int(score.numel()), _stream(stream)))
+
+
+def sg_rank_by_score(score: torch.Tensor, stream=None):
+    """(order, rank_of) device int32 tensors: nodes by descending score (the
+    32-bit unsigned contents of score), ties by ascending ID."""
+    lib = load()
+    n = int(score.numel())
+    nbytes = int(lib.sg_rank_workspace(n))
+    if nbytes == 0:
+        raise SgError(SG_ERR_INVALID_ARG, "sg_rank_by_score: bad size")
+    order = torch.empty(n, dtype=torch.int32, device=score.device)
+    rank_of = torch.empty(n, dtype=torch.int32, device=score.device)
+    ws = _aligned_bytes(nbytes, score.device)
+    _check(lib.sg_rank_by_score(score.data_ptr(), n, order.data_ptr(), rank_of.data_ptr(), ws.data_ptr(), ws.numel(),
+                                _stream(stream)))
+    return order, rank_of
 
 
 def sg_relabel(ids: torch.Tensor, prefix: torch.Tensor, stream=None):

@@ -114,7 +114,8 @@ __global__ void k_validate_indices(const int32_t* idx, int64_t m, int64_t n, uns
 }
 
 // Fill cache slot s with feature row ranked[s] (or row s when ranked is NULL)
-// and record slot_of[node] = s.  One 16-byte vector per thread step.
+// and record slot_of[node] = s (when there is a slot map).  One 16-byte
+// vector per thread step.
 __global__ void k_cache_fill(const int32_t* ranked, int64_t n_cache, int64_t n_nodes, const uint4* src,
                              int64_t row_vecs, uint4* cache, int32_t* slot_of) {
     const int64_t total = n_cache * row_vecs;
@@ -126,7 +127,7 @@ __global__ void k_cache_fill(const int32_t* ranked, int64_t n_cache, int64_t n_n
             continue;
         }
         cache[s * row_vecs + c] = src[g * row_vecs + c];
-        if (c == 0) slot_of[g] = (int32_t)s;
+        if (c == 0 && slot_of) slot_of[g] = (int32_t)s;
     }
 }
 
@@ -204,7 +205,7 @@ extern "C" sg_status sg_stream_check(sg_stream_t stream) {
     cudaStream_t s = (cudaStream_t)stream;
     SG_CUDA(cudaStreamSynchronize(s));
     unsigned w = fetch_err_api(s) | fetch_err_sampler(s) | fetch_err_gather(s) | fetch_err_aggregate(s) |
-               fetch_err_update(s);
+               fetch_err_update(s) | fetch_err_recode(s);
     if (w & 0x80000000u) return fail(SG_ERR_CUDA, "sg_stream_check: could not read the device error word");
     if (w & ERR_INDEX) return fail(SG_ERR_INVALID_INDEX, "a kernel met a node ID or index out of range");
     if (w & ERR_CAPACITY) return fail(SG_ERR_CAPACITY, "a device table or buffer bound was exceeded");
@@ -287,6 +288,14 @@ extern "C" sg_status sg_graph_info(const sg_graph* g, int64_t* n_nodes, int64_t*
     return SG_OK;
 }
 
+extern "C" sg_status sg_graph_copy_out(const sg_graph* g, void* h_indptr, int32_t* h_indices) {
+    if (!g || !h_indptr || (g->n_edges > 0 && !h_indices)) return fail(SG_ERR_INVALID_ARG, "sg_graph_copy_out: NULL argument");
+    SG_CUDA(cudaMemcpy(h_indptr, g->indptr, (size_t)(g->n_nodes + 1) * (g->offset_bits / 8), cudaMemcpyDeviceToHost));
+    if (g->n_edges > 0)
+        SG_CUDA(cudaMemcpy(h_indices, g->indices, (size_t)g->n_edges * sizeof(int32_t), cudaMemcpyDeviceToHost));
+    return SG_OK;
+}
+
 // -------------------------------------------------------------------- cache
 extern "C" sg_status sg_cache_build(const void* h_feat, const void* d_feat, int32_t dtype, int64_t n_nodes, int32_t dim,
                                     const int32_t* h_ranked, int64_t n_cache, sg_cache** out, sg_stream_t stream) {
@@ -295,8 +304,6 @@ extern "C" sg_status sg_cache_build(const void* h_feat, const void* d_feat, int3
     if (dtype != SG_F32 && dtype != SG_BF16) return fail(SG_ERR_INVALID_ARG, "sg_cache_build: dtype");
     if (n_nodes <= 0 || n_nodes > 2147483647LL || dim <= 0) return fail(SG_ERR_INVALID_ARG, "sg_cache_build: shape");
     if (n_cache < 0 || n_cache > n_nodes) return fail(SG_ERR_INVALID_ARG, "sg_cache_build: n_cache outside [0, n_nodes]");
-    if (!h_ranked && n_cache != n_nodes && n_cache != 0)
-        return fail(SG_ERR_INVALID_ARG, "sg_cache_build: h_ranked may be NULL only when every node is cached");
     const int64_t row_bytes = (int64_t)dim * (dtype == SG_F32 ? 4 : 2);
     if (row_bytes % 16) return fail(SG_ERR_UNSUPPORTED, "sg_cache_build: row bytes (%lld) must be a multiple of 16", (long long)row_bytes);
     if (!h_feat && !d_feat) return fail(SG_ERR_INVALID_ARG, "sg_cache_build: no feature table");
@@ -342,12 +349,13 @@ extern "C" sg_status sg_cache_build(const void* h_feat, const void* d_feat, int3
     }
     int32_t* d_ranked = nullptr;
     unsigned* d_bad = nullptr;
-    cudaError_t e = dev_alloc((void**)&c->slot_of, (size_t)n_nodes * sizeof(int32_t));
+    // with a ranked list, a slot map; without, the ID range [0, n_cache)
+    cudaError_t e = h_ranked ? dev_alloc((void**)&c->slot_of, (size_t)n_nodes * sizeof(int32_t)) : cudaSuccess;
     if (e == cudaSuccess && n_cache > 0) e = dev_alloc(&c->rows, (size_t)n_cache * (size_t)row_bytes);
     if (e == cudaSuccess && h_ranked && n_cache > 0) e = dev_alloc((void**)&d_ranked, (size_t)n_cache * sizeof(int32_t));
     if (e == cudaSuccess) e = dev_alloc((void**)&d_bad, sizeof(unsigned));
     if (e == cudaSuccess) e = cudaMemsetAsync(d_bad, 0, sizeof(unsigned), s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(c->slot_of, 0xFF, (size_t)n_nodes * sizeof(int32_t), s);
+    if (e == cudaSuccess && c->slot_of) e = cudaMemsetAsync(c->slot_of, 0xFF, (size_t)n_nodes * sizeof(int32_t), s);
     if (e == cudaSuccess && d_ranked)
         e = cudaMemcpyAsync(d_ranked, h_ranked, (size_t)n_cache * sizeof(int32_t), cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess && n_cache > 0) {

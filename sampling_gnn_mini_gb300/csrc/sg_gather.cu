@@ -13,6 +13,10 @@
 // with the default policy, so that the first aggregation hop, which reads it
 // next, finds part of it in L2.
 //
+// Hit test: with a slot map (a cache built from a ranked list), slot_of[g];
+// without one (an ID-range cache, hot nodes recoded to the smallest IDs),
+// node g is cached in slot g exactly when g < n_cache, and no map is read.
+//
 // Large host tables (32 GiB and more) with a workspace: random zero-copy
 // reads there lose most of their rate to address translation (measured on
 // GB300, 512-byte rows: ~208 GB/s from a 16 GB pinned table in any order,
@@ -33,9 +37,16 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kUnroll = 8;
 
+// cache slot of node g, or -1 when it is read from the host table
+__device__ __forceinline__ int64_t slot_for(const int32_t* __restrict__ slot_of, int64_t n_cache, int32_t g) {
+    if (slot_of) return __ldg(slot_of + g);
+    return (int64_t)g < n_cache ? (int64_t)g : -1;
+}
+
 __global__ void __launch_bounds__(kThreads) k_gather(const int32_t* __restrict__ ids, const int32_t* __restrict__ d_n,
                                                      const int32_t* __restrict__ d_first,
-                                                     int64_t n_cap, const int32_t* __restrict__ slot_of, int64_t n_nodes,
+                                                     int64_t n_cap, const int32_t* __restrict__ slot_of, int64_t n_cache,
+                                                     int64_t n_nodes,
                                                      const uint4* __restrict__ cache, const uint4* __restrict__ host,
                                                      int32_t row_vecs, int64_t step_rows, int32_t step_rem,
                                                      uint4* __restrict__ out, sg_gather_stats* __restrict__ stats,
@@ -72,7 +83,7 @@ __global__ void __launch_bounds__(kThreads) k_gather(const int32_t* __restrict__
                     if (c == 0) dev_err(ERR_INDEX);
                     v[u] = make_uint4(0, 0, 0, 0);
                 } else {
-                    const int32_t s = __ldg(slot_of + g);
+                    const int64_t s = slot_for(slot_of, n_cache, g);
                     if (s >= 0) {
                         v[u] = __ldcs(cache + (int64_t)s * row_vecs + c);
                         hits += (c == 0);
@@ -155,7 +166,8 @@ __global__ void __launch_bounds__(kScanThreads) k_region_scan(uint32_t* __restri
 __global__ void __launch_bounds__(kThreads) k_region_scatter(const int32_t* __restrict__ ids,
                                                              const int32_t* __restrict__ d_n,
                                                              const int32_t* __restrict__ d_first, int64_t n_cap,
-                                                             const int32_t* __restrict__ slot_of, int64_t n_nodes,
+                                                             const int32_t* __restrict__ slot_of, int64_t n_cache,
+                                                             int64_t n_nodes,
                                                              uint32_t* __restrict__ cnt, int32_t region_shift,
                                                              int32_t* __restrict__ list) {
     pdl_start();
@@ -164,7 +176,7 @@ __global__ void __launch_bounds__(kThreads) k_region_scatter(const int32_t* __re
     for (int64_t i = first + blockIdx.x * (int64_t)kThreads + threadIdx.x; i < n; i += (int64_t)gridDim.x * kThreads) {
         const int32_t g = __ldg(ids + i);
         if (g < 0 || (int64_t)g >= n_nodes) continue;
-        if (__ldg(slot_of + g) >= 0) continue;
+        if (slot_for(slot_of, n_cache, g) >= 0) continue;
         const uint32_t pos = atomicAdd(cnt + (g >> region_shift), 1u);
         if ((int64_t)pos < n_cap) list[pos] = (int32_t)i;
         else dev_err(ERR_CAPACITY);
@@ -252,7 +264,7 @@ extern "C" sg_status sg_gather(const sg_cache* c, const int32_t* d_ids, int64_t 
                               : nullptr;
     if (by_region) SG_CUDA(cudaMemsetAsync(cnt, 0, (size_t)(c->n_regions + 1) * sizeof(uint32_t), s));
     SG_CUDA(launch_pdl(k_gather, dim3((unsigned)blocks), dim3(kThreads), 0, s, d_ids, d_n, d_first,
-                       n_cap, c->slot_of, c->n_nodes, (const uint4*)c->rows, (const uint4*)c->host_rows,
+                       n_cap, c->slot_of, c->n_cache, c->n_nodes, (const uint4*)c->rows, (const uint4*)c->host_rows,
                        (int32_t)row_vecs, stride / row_vecs, (int32_t)(stride % row_vecs), (uint4*)d_out, d_stats,
                        cnt, c->region_shift));
     if (!by_region) return SG_OK;
@@ -260,7 +272,7 @@ extern "C" sg_status sg_gather(const sg_cache* c, const int32_t* d_ids, int64_t 
     int64_t sblocks = cdiv(n_cap, (int64_t)kThreads);
     if (sblocks > cap) sblocks = cap;
     SG_CUDA(launch_pdl(k_region_scatter, dim3((unsigned)sblocks), dim3(kThreads), 0, s, d_ids, d_n, d_first, n_cap,
-                       c->slot_of, c->n_nodes, cnt, c->region_shift, list));
+                       c->slot_of, c->n_cache, c->n_nodes, cnt, c->region_shift, list));
     SG_CUDA(launch_pdl(k_gather_list, dim3((unsigned)blocks), dim3(kThreads), 0, s, (const int32_t*)list,
                        (const uint32_t*)(cnt + c->n_regions), d_ids, (const uint4*)c->host_rows, (int32_t)row_vecs,
                        n_cap, stride / row_vecs, (int32_t)(stride % row_vecs), (uint4*)d_out));

@@ -48,6 +48,7 @@ unsigned fetch_err_gather(cudaStream_t);
 unsigned fetch_err_aggregate(cudaStream_t);
 unsigned fetch_err_api(cudaStream_t);
 unsigned fetch_err_update(cudaStream_t);
+unsigned fetch_err_recode(cudaStream_t);
 
 // ------------------------------------------------- allocation (owned memory)
 // Every device allocation the library owns goes through dev_alloc.  With the

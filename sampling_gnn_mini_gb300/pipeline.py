@@ -23,11 +23,41 @@ the calls.
 """
 from __future__ import annotations
 
-from typing import Optional, Sequence
+from typing import Iterable, Optional, Sequence, Tuple
 
 import torch
 
 from . import binding as sg
+
+
+def rank_by_access(graph: sg.Graph, batches: Iterable[Tuple[torch.Tensor, int]], fanouts: Sequence[int],
+                   omega: Sequence[int], w_in: int = 1, device="cuda"):
+    """Presampling statistics and ranking (GARDEN page, Section IV-B): each
+    (seeds, hash seed) batch is sampled and its full-link access statistics
+    (Eq. (4), weights omega per layer and w_in for input nodes) are added to a
+    per-node score on the device; returns (order, rank_of), nodes by
+    descending score.  All sizes of a batch must be equal."""
+    score = torch.zeros(graph.n_nodes, dtype=torch.int32, device=device)
+    buf, n_seeds = None, None
+    for seeds, hseed in batches:
+        if buf is None:
+            n_seeds = int(seeds.numel())
+            bounds = sg.sg_sampler_bounds(graph, n_seeds, fanouts)
+            buf = sg.SampleBuffers(bounds, device, graph, n_seeds, fanouts)
+        elif int(seeds.numel()) != n_seeds:
+            raise ValueError("rank_by_access: every presampled batch must have %d seeds" % n_seeds)
+        sg.sg_sampler_run(graph, seeds, fanouts, hseed, buf)
+        sg.sg_access_stats(buf, omega, w_in, score)
+    return sg.sg_rank_by_score(score)
+
+
+def recode_by_access(graph: sg.Graph, batches, fanouts, omega, w_in: int = 1, device="cuda"):
+    """rank_by_access, then the graph recoded so that the node of rank r has
+    ID r (Section IV-A): returns (new graph, order, rank_of).  The feature
+    table must then be laid out in the new order (new row r = old row
+    order[r]) for an ID-range cache, and seeds mapped through rank_of."""
+    order, rank_of = rank_by_access(graph, batches, fanouts, omega, w_in, device)
+    return sg.sg_graph_renumber(graph, order, rank_of), order, rank_of
 
 
 class MiniBatchPipeline:

@@ -67,6 +67,8 @@ def _load():
         lib.synth_graph_free.argtypes = [vp]
         lib.synth_features.restype = ctypes.c_int
         lib.synth_features.argtypes = [i64, i64, i32, i32, u64, vp]
+        lib.synth_features_rows.restype = ctypes.c_int
+        lib.synth_features_rows.argtypes = [vp, i64, i32, i32, u64, vp]
         lib.synth_batch_seeds.restype = i32
         lib.synth_batch_seeds.argtypes = [i64, dbl, u64, i64, i64, i32, vp]
         lib.synth_epoch_order.restype = i64
@@ -143,6 +145,15 @@ def features_into(out_ptr: int, row0: int, nrows: int, dim: int, dtype: str, see
     code = {"f32": 0, "bf16": 1}[dtype]
     if _load().synth_features(int(row0), int(nrows), int(dim), code, int(seed), ctypes.c_void_p(out_ptr)):
         raise ValueError("features_into: bad arguments")
+
+
+def features_rows_into(out_ptr: int, ids: np.ndarray, dim: int, dtype: str, seed: int = 0) -> None:
+    """Write the feature rows of nodes ids[0], ids[1], ... as consecutive rows
+    at ``out_ptr`` (the table laid out for recoded node IDs)."""
+    code = {"f32": 0, "bf16": 1}[dtype]
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    if _load().synth_features_rows(ids.ctypes.data, len(ids), int(dim), code, int(seed), ctypes.c_void_p(out_ptr)):
+        raise ValueError("features_rows_into: bad arguments")
 
 
 def features(n: int, dim: int, dtype: str = "f32", seed: int = 0, row0: int = 0) -> np.ndarray:

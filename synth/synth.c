@@ -235,28 +235,40 @@ static inline uint16_t f32_to_bf16_rne(float f) {
 /* Rows [row0, row0+nrows) of the N x dim feature table: N(0,1) by Box-Muller
  * on a pair of 24-bit uniforms drawn for (row, column pair).
  * dtype 0 = fp32, 1 = bf16 (fp32 value rounded to nearest even). */
-int synth_features(int64_t row0, int64_t nrows, int32_t dim, int32_t dtype, uint64_t seed, void* out) {
-    if (dim <= 0 || nrows < 0 || (dtype != 0 && dtype != 1)) return -1;
+static void feature_row(int64_t v, int32_t dim, int32_t dtype, uint64_t seed, void* out_row) {
     int64_t pairs = (dim + 1) / 2;
-    #pragma omp parallel for schedule(static)
-    for (int64_t r = 0; r < nrows; r++) {
-        int64_t v = row0 + r;
-        for (int64_t p = 0; p < pairs; p++) {
-            uint64_t x = draw(seed, 3, (uint64_t)(v * pairs + p));
-            float u1 = (float)((x >> 40) + 1) * (1.0f / 16777216.0f);
-            float u2 = (float)(x & 0xFFFFFFull) * (1.0f / 16777216.0f);
-            float rad = sqrtf(-2.0f * logf(u1));
-            float z[2];
-            z[0] = rad * cosf(6.28318530717958647692f * u2);
-            z[1] = rad * sinf(6.28318530717958647692f * u2);
-            for (int t = 0; t < 2; t++) {
-                int64_t col = 2 * p + t;
-                if (col >= dim) break;
-                if (dtype == 0) ((float*)out)[r * dim + col] = z[t];
-                else ((uint16_t*)out)[r * dim + col] = f32_to_bf16_rne(z[t]);
-            }
+    for (int64_t p = 0; p < pairs; p++) {
+        uint64_t x = draw(seed, 3, (uint64_t)(v * pairs + p));
+        float u1 = (float)((x >> 40) + 1) * (1.0f / 16777216.0f);
+        float u2 = (float)(x & 0xFFFFFFull) * (1.0f / 16777216.0f);
+        float rad = sqrtf(-2.0f * logf(u1));
+        float z[2];
+        z[0] = rad * cosf(6.28318530717958647692f * u2);
+        z[1] = rad * sinf(6.28318530717958647692f * u2);
+        for (int t = 0; t < 2; t++) {
+            int64_t col = 2 * p + t;
+            if (col >= dim) break;
+            if (dtype == 0) ((float*)out_row)[col] = z[t];
+            else ((uint16_t*)out_row)[col] = f32_to_bf16_rne(z[t]);
         }
     }
+}
+
+int synth_features(int64_t row0, int64_t nrows, int32_t dim, int32_t dtype, uint64_t seed, void* out) {
+    if (dim <= 0 || nrows < 0 || (dtype != 0 && dtype != 1)) return -1;
+    size_t rb = (size_t)dim * (dtype == 0 ? 4 : 2);
+    #pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < nrows; r++) feature_row(row0 + r, dim, dtype, seed, (char*)out + (size_t)r * rb);
+    return 0;
+}
+
+/* Rows of the table in a given order: output row r is node ids[r]'s row (a
+ * table laid out for recoded node IDs). */
+int synth_features_rows(const int32_t* ids, int64_t nrows, int32_t dim, int32_t dtype, uint64_t seed, void* out) {
+    if (dim <= 0 || nrows < 0 || (dtype != 0 && dtype != 1)) return -1;
+    size_t rb = (size_t)dim * (dtype == 0 ? 4 : 2);
+    #pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < nrows; r++) feature_row(ids[r], dim, dtype, seed, (char*)out + (size_t)r * rb);
     return 0;
 }
 

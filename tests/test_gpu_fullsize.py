@@ -20,7 +20,7 @@ import synth
 from helpers import as_f64, assert_close, dev_i32, torch_to_np
 from sampling_gnn_mini_gb300 import binding as sg
 from sampling_gnn_mini_gb300.hostmem import pinned_table
-from sampling_gnn_mini_gb300.pipeline import MiniBatchPipeline
+from sampling_gnn_mini_gb300.pipeline import MiniBatchPipeline, recode_by_access
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -38,11 +38,15 @@ def _cuda():
 
 class PinnedTable:
     """The whole feature table in page-locked host memory (as the benchmark
-    holds it), with a numpy view for the checks (bf16 as uint16 bits)."""
+    holds it), with a numpy view for the checks (bf16 as uint16 bits); with
+    `order`, row r holds node order[r]'s features (a recoded table)."""
 
-    def __init__(self, n, dim, dtype, seed):
+    def __init__(self, n, dim, dtype, seed, order=None):
         self.t = pinned_table(n, dim, torch.float32 if dtype == "f32" else torch.bfloat16)
-        synth.features_into(self.t.data_ptr(), 0, n, dim, dtype, seed)
+        if order is None:
+            synth.features_into(self.t.data_ptr(), 0, n, dim, dtype, seed)
+        else:
+            synth.features_rows_into(self.t.data_ptr(), order, dim, dtype, seed)
         self.arr = self.t.numpy() if dtype == "f32" else self.t.view(torch.int16).numpy().view(np.uint16)
 
 
@@ -194,33 +198,45 @@ def test_skew_super_batch_full_size(name, check_subs):
 # ------------------------------------------------- Billion-edge and Wide
 @pytest.mark.parametrize("name", ["billion", "wide"])
 def test_host_feature_workloads_full_size(name):
+    """The benchmark's launch configuration: presampled full-link statistics,
+    ranking and recoding on the GPU, the host table laid out in the new order,
+    an ID-range cache of the budget's rows, then one mini-batch through every
+    stage, checked against the oracle on the recoded graph."""
     w = synth.workload(name)
     g = synth.chung_lu(w.n_nodes, w.mean_deg, w.gamma, w.wmax, w.rng_seed)
     indptr = g.indptr if w.offset_bits == 64 else g.indptr.astype(np.int32)
-    G = sg.sg_graph_load(indptr, g.indices, w.offset_bits)
+    G0 = sg.sg_graph_load(indptr, g.indices, w.offset_bits)
+    del g, indptr
+    pre = synth.BatchStream(w, epoch0=1000)
+    batches = ((dev_i32(pre.seeds(b)), w.presample_seed(b)) for b in range(8))
+    G, order, rank_of = recode_by_access(G0, batches, w.fanouts, [1] * w.n_hops)
+    del G0
     assert G.offset_bits == w.offset_bits
-    table = PinnedTable(w.n_nodes, w.dim, w.dtype, w.rng_seed)
+    ip, ix = sg.sg_graph_copy_out(G)
+    order_h, rank_h = order.cpu().numpy(), rank_of.cpu().numpy()
+    table = PinnedTable(w.n_nodes, w.dim, w.dtype, w.rng_seed, order=order_h)
     try:
-        deg = np.diff(g.indptr)
-        ranked = np.argpartition(-deg, w.cache_rows - 1)[: w.cache_rows].astype(np.int32)  # the hubs: speed only
         cache = sg.sg_cache_build(table.t, None, sg.SG_F32 if w.dtype == "f32" else sg.SG_BF16, w.n_nodes, w.dim,
-                                  ranked, w.cache_rows)
+                                  None, w.cache_rows)
+        assert cache.slot_of_ptr() in (None, 0)  # the ID-range hit test
         pipe = MiniBatchPipeline(G, cache, w.fanouts, w.batch)
-        bs = synth.BatchStream(w)
-        seeds = bs.seeds(0)
+        seeds = rank_h[synth.BatchStream(w).seeds(0)]
         pipe.set_batch(dev_i32(seeds), w.sampler_seed(0))
         pipe.step()
         sg.sg_stream_check()
         hits, misses = pipe.stats.cpu().tolist()
         assert misses > 0 and hits > 0  # both the HBM cache and the host table were read
-        _check_sampling(pipe, g, seeds, 0, w.fanouts, w.sampler_seed(0))
+        n = int(pipe.buf.counts[w.n_hops].item())
+        assert hits == int((pipe.buf.unique[:n] < w.cache_rows).sum().item())
+        rg = synth.csr_graph(ip.astype(np.int64), ix)
+        _check_sampling(pipe, rg, seeds, 0, w.fanouts, w.sampler_seed(0))
         rng = np.random.default_rng(2)
         _check_gather(pipe, table.arr)
         _check_aggregation(pipe, rng, w.dtype)
         del pipe, cache
     finally:
         torch.cuda.synchronize()
-    del table, G, g
+    del table, G
     gc.collect()
     torch.cuda.empty_cache()
 

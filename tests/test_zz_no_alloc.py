@@ -67,7 +67,7 @@ def test_noalloc_matches_oracle_on_calls_in_a_row():
     # larger then smaller then larger again: each call clears what it uses of
     # the shared scratch, so the previous call's contents never show
     for prefix, ids in (_case(1, 3000, 120000, 500000), _case(2, 17, 250000, 40000), _case(3, 500, 900, 2000),
-                        _case(4, 40, 200000, 1 << 30)):
+                        _case(4, 40, 200000, 1 << 24)):
         _check(prefix, ids)
 
 
