@@ -75,6 +75,19 @@ def _load():
         lib.orc_rank_by_score.argtypes = [vp, i64, vp, vp]
         lib.orc_graph_renumber.restype = None
         lib.orc_graph_renumber.argtypes = [vp, vp, i64, vp, vp, vp, vp]
+        u32 = ctypes.c_uint32
+        lib.orc_dyn_weights.restype = u32
+        lib.orc_dyn_weights.argtypes = [u32, i32, vp]
+        lib.orc_dyn_accumulate.restype = None
+        lib.orc_dyn_accumulate.argtypes = [vp, i64, vp, u32, vp]
+        lib.orc_dyn_update.restype = i64
+        lib.orc_dyn_update.argtypes = [vp, vp, i64, u32, i64, vp]
+        lib.orc_match.restype = i64
+        lib.orc_match.argtypes = [vp, i64, vp, i64, i64, vp]
+        lib.orc_overlap.restype = ctypes.c_int
+        lib.orc_overlap.argtypes = [vp, vp, i32, i64, vp]
+        lib.orc_greedy_order.restype = None
+        lib.orc_greedy_order.argtypes = [vp, i32, i32, vp]
         _lib = lib
         return lib
 
@@ -346,6 +359,68 @@ def graph_renumber(indptr, indices, order, rank_of):
     new_ix = np.zeros(max(1, len(ix)), np.int32)
     _load().orc_graph_renumber(_p(ip), _p(ix), n, _p(od), _p(rk), _p(new_ip), _p(new_ix))
     return new_ip, new_ix[: len(ix)]
+
+
+class DynCache:
+    """The dynamic cache's scores (Eq. (5)-(6), windowed fixed-point reading;
+    see oracle.c): gamma = g / 2^16, windows of T batches, k_dyn nodes."""
+
+    def __init__(self, n_nodes: int, g: int, T: int, k_dyn: int, static_cached: np.ndarray):
+        self.n, self.T, self.k = int(n_nodes), int(T), int(k_dyn)
+        self.W = np.zeros(self.T, np.uint32)
+        self.G = int(_load().orc_dyn_weights(int(g), self.T, _p(self.W)))
+        self.S = np.zeros(self.n, np.uint32)
+        self.A = np.zeros(self.n, np.uint32)
+        self.cached = np.ascontiguousarray(static_cached, dtype=np.uint8)
+        self.j = 0  # batch within the window
+
+    def batch(self, unique) -> None:
+        """Adds one batch's nodes (its V_H); closes the window after T."""
+        u = np.ascontiguousarray(unique, dtype=np.int32)
+        _load().orc_dyn_accumulate(_p(u), len(u), _p(self.cached), int(self.W[self.j]), _p(self.A))
+        self.j += 1
+
+    def update(self) -> np.ndarray:
+        """End of a window: the new dynamic set (Eq. (6))."""
+        dyn = np.zeros(max(1, self.k), np.int32)
+        c = _load().orc_dyn_update(_p(self.S), _p(self.A), self.n, self.G, self.k, _p(dyn))
+        if c < 0:
+            raise MemoryError("oracle dyn update")
+        self.j = 0
+        return dyn[:c].copy()
+
+
+def match(prev, cur, n_nodes: int):
+    """Position of each cur ID in prev, or -1 (prev: distinct IDs)."""
+    p = np.ascontiguousarray(prev, dtype=np.int32)
+    c = np.ascontiguousarray(cur, dtype=np.int32)
+    pos = np.zeros(max(1, len(c)), np.int32)
+    m = _load().orc_match(_p(p), len(p), _p(c), len(c), int(n_nodes), _p(pos))
+    if m < 0:
+        raise MemoryError("oracle match")
+    return pos[: len(c)]
+
+
+def overlap(lists, n_nodes: int) -> np.ndarray:
+    """G x G matrix of |list a intersect list b| (lists of distinct IDs)."""
+    off = np.concatenate([[0], np.cumsum([len(x) for x in lists])]).astype(np.int64)
+    ids = np.ascontiguousarray(np.concatenate(lists) if len(lists) else np.zeros(0), dtype=np.int32)
+    G = len(lists)
+    O = np.zeros((G, G), np.int64)
+    if _load().orc_overlap(_p(ids), _p(off), G, int(n_nodes), _p(O)) != 0:
+        raise MemoryError("oracle overlap")
+    return O
+
+
+def greedy_order(O: np.ndarray, first: int = 0) -> np.ndarray:
+    """Nearest-overlap-first order of G batches from `first` (ties: lowest)."""
+    OO = np.ascontiguousarray(O, dtype=np.int64)
+    G = OO.shape[0]
+    if G > 1024:
+        raise ValueError("greedy_order: at most 1024 batches")
+    order = np.zeros(G, np.int32)
+    _load().orc_greedy_order(_p(OO), G, int(first), _p(order))
+    return order
 
 
 def bf16_to_f32(bits: np.ndarray) -> np.ndarray:

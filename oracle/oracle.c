@@ -421,3 +421,119 @@ void orc_graph_renumber(const int64_t* indptr, const int32_t* indices, int64_t n
         new_indptr[r + 1] = new_indptr[r] + deg;
     }
 }
+
+/* ------------------------------------------------ dynamic cache (NEXT) */
+/* Adaptive dynamic feature caching (GARDEN page, Section IV-B, Eq. (5)-(6)).
+ * Eq. (5): Score(v, t) = gamma * Score(v, t-1) + (occurrences of v among the
+ * batch-t nodes B_t).  Readings:
+ *   - B_t are the nodes of batch t that the static cache does not hold (the
+ *     page's Dynamic-Cache serves only accesses the static cache misses);
+ *   - the score is kept in fixed point and evaluated at the end of each
+ *     update window of T batches (Eq. (6) reads it only there): with
+ *     gamma = g / 2^16 and 8 fractional bits,
+ *       W_{T-1} = 2^8,  W_{j-1} = (W_j * g) >> 16      (gamma^{T-1-j} in Q8)
+ *       G_1 = g,        G_{i+1} = (G_i * g) >> 16       (gamma^T in Q16)
+ *     batch j of the window (0 <= j < T) adds W_j to A[v] for each of its
+ *     occurrences of v in B_j, and at the window's end
+ *       S[v] = ((S[v] * G_T) >> 16) + A[v],  A[v] = 0,
+ *     which is Eq. (5) applied T times, rounded down to the fixed point;
+ *     every sum is an integer, so the result is exact and order-free.
+ * orc_dyn_weights fills W[0..T) and returns G_T. */
+uint32_t orc_dyn_weights(uint32_t g, int32_t T, uint32_t* W) {
+    W[T - 1] = 256;
+    for (int32_t j = T - 1; j > 0; j--) W[j - 1] = (uint32_t)(((uint64_t)W[j] * g) >> 16);
+    uint64_t G = g;
+    for (int32_t i = 1; i < T; i++) G = (G * g) >> 16;
+    return (uint32_t)G;
+}
+
+/* batch j of the window: A[v] += w for every node v of the batch (local
+ * order, n entries of unique) that the static cache does not hold */
+void orc_dyn_accumulate(const int32_t* unique, int64_t n, const uint8_t* static_cached, uint32_t w, uint32_t* A) {
+    for (int64_t i = 0; i < n; i++) {
+        int32_t v = unique[i];
+        if (!static_cached[v]) A[v] += w;
+    }
+}
+
+/* end of a window: S = (S * G_T >> 16) + A, A = 0; then Eq. (6): the k_dyn
+ * nodes of largest S (ties by ascending ID), only nodes with S > 0, into
+ * dyn[]; returns how many were chosen */
+int64_t orc_dyn_update(uint32_t* S, uint32_t* A, int64_t n_nodes, uint32_t G_T, int64_t k_dyn, int32_t* dyn) {
+    for (int64_t v = 0; v < n_nodes; v++) {
+        S[v] = (uint32_t)(((uint64_t)S[v] * G_T) >> 16) + A[v];
+        A[v] = 0;
+    }
+    int32_t* order = (int32_t*)malloc((size_t)(n_nodes > 0 ? n_nodes : 1) * sizeof(int32_t));
+    int32_t* rank = (int32_t*)malloc((size_t)(n_nodes > 0 ? n_nodes : 1) * sizeof(int32_t));
+    if (!order || !rank) { free(order); free(rank); return -1; }
+    orc_rank_by_score(S, n_nodes, order, rank);
+    int64_t c = 0;
+    for (int64_t r = 0; r < n_nodes && c < k_dyn; r++) {
+        if (S[order[r]] == 0) break;
+        dyn[c++] = order[r];
+    }
+    free(order);
+    free(rank);
+    return c;
+}
+
+/* -------------------------------------------- match and reorder (NEXT) */
+/* FastGL explainer page ("Match-Reorder"): consecutive sampled subgraphs
+ * share many nodes, so a batch reuses the features of the previous batch
+ * still resident on the GPU, and a group of batches is ordered so that each
+ * follows the one it overlaps most.
+ * Match: pos[j] = the position of cur[j] in prev (prev holds distinct IDs),
+ * or -1 when cur[j] is not there; returns the number matched. */
+int64_t orc_match(const int32_t* prev, int64_t n_prev, const int32_t* cur, int64_t n_cur, int64_t n_nodes,
+                  int32_t* pos) {
+    int32_t* at = (int32_t*)malloc((size_t)(n_nodes > 0 ? n_nodes : 1) * sizeof(int32_t));
+    if (!at) return -1;
+    for (int64_t v = 0; v < n_nodes; v++) at[v] = -1;
+    for (int64_t i = 0; i < n_prev; i++) at[prev[i]] = (int32_t)i;
+    int64_t m = 0;
+    for (int64_t j = 0; j < n_cur; j++) {
+        pos[j] = at[cur[j]];
+        m += pos[j] >= 0;
+    }
+    free(at);
+    return m;
+}
+
+/* Overlap matrix of G node lists (list a = ids[off[a] .. off[a+1]), each with
+ * distinct IDs): O[a*G + b] = |list a intersect list b| (the diagonal is the
+ * list's size). */
+int orc_overlap(const int32_t* ids, const int64_t* off, int32_t G, int64_t n_nodes, int64_t* O) {
+    uint8_t* in = (uint8_t*)malloc((size_t)(n_nodes > 0 ? n_nodes : 1));
+    if (!in) return -1;
+    for (int32_t a = 0; a < G; a++) {
+        memset(in, 0, (size_t)n_nodes);
+        for (int64_t i = off[a]; i < off[a + 1]; i++) in[ids[i]] = 1;
+        for (int32_t b = 0; b < G; b++) {
+            int64_t c = 0;
+            for (int64_t i = off[b]; i < off[b + 1]; i++) c += in[ids[i]];
+            O[(int64_t)a * G + b] = c;
+        }
+    }
+    free(in);
+    return 0;
+}
+
+/* Greedy order (nearest overlap first): start at batch `first`, then
+ * repeatedly take the batch not yet taken that overlaps most with the last
+ * one taken (ties: the lowest index). */
+void orc_greedy_order(const int64_t* O, int32_t G, int32_t first, int32_t* order) {
+    uint8_t taken[1024];
+    memset(taken, 0, sizeof(taken));
+    order[0] = first;
+    taken[first] = 1;
+    for (int32_t k = 1; k < G; k++) {
+        int32_t last = order[k - 1], best = -1;
+        for (int32_t b = 0; b < G; b++) {
+            if (taken[b]) continue;
+            if (best < 0 || O[(int64_t)last * G + b] > O[(int64_t)last * G + best]) best = b;
+        }
+        order[k] = best;
+        taken[best] = 1;
+    }
+}

@@ -540,3 +540,92 @@ def test_graph_renumber_is_the_permuted_matrix():
     ip3, ix3 = oracle.graph_renumber(g.indptr, g.indices, np.arange(g.n, dtype=np.int32),
                                      np.arange(g.n, dtype=np.int32))
     assert np.array_equal(ip3, g.indptr) and np.array_equal(ix3, g.indices)
+
+
+# ------------------------------------------- dynamic cache, match and reorder
+def test_dyn_cache_without_decay_counts_residual_appearances():
+    # gamma = 1 (g = 2^16): no decay, every batch weighs 2^8, so the window's
+    # score is 256 x the number of batches a node appeared in, static misses only
+    rng = np.random.default_rng(0)
+    n = 500
+    cached = np.zeros(n, np.uint8)
+    cached[:100] = 1
+    dc = oracle.DynCache(n, 1 << 16, 4, 50, cached)
+    lists = [rng.choice(n, 120, replace=False).astype(np.int32) for _ in range(4)]
+    for u in lists:
+        dc.batch(u)
+    dyn = dc.update()
+    cnt = np.bincount(np.concatenate(lists), minlength=n) * (1 - cached.astype(np.int64))
+    assert np.array_equal(dc.S.astype(np.int64), 256 * cnt)
+    assert not dc.A.any()
+    want = np.lexsort((np.arange(n), -cnt))[:50]
+    want = want[cnt[want] > 0]
+    assert np.array_equal(dyn, want)
+    assert not cached[dyn].any()
+
+
+def test_dyn_cache_half_decay_worked_example():
+    # gamma = 1/2, T = 3: W = (64, 128, 256), gamma^3 = 2^13 / 2^16.  Node 7
+    # appears in batches 0 and 2 of the first window and batch 1 of the
+    # second.  Eq. (5) in reals, in units of one occurrence: 1, 0.5, 1.25,
+    # then 0.625, 1.3125, 0.65625; in Q8 that is 320 and then 168.
+    dc = oracle.DynCache(10, 1 << 15, 3, 2, np.zeros(10, np.uint8))
+    assert list(dc.W) == [64, 128, 256] and dc.G == 1 << 13
+    for u in ([7, 1], [2], [7]):
+        dc.batch(np.array(u, np.int32))
+    dyn = dc.update()
+    assert dc.S[7] == 320 and dc.S[1] == 64 and dc.S[2] == 128
+    assert list(dyn) == [7, 2]
+    for u in ([3], [7], [3]):
+        dc.batch(np.array(u, np.int32))
+    dc.update()
+    assert dc.S[7] == 168
+
+
+def test_dyn_cache_tracks_the_real_valued_recursion():
+    # any gamma: the fixed-point window scores stay within rounding of Eq. (5)
+    # run batch by batch in double precision
+    rng = np.random.default_rng(2)
+    n, T = 300, 5
+    g = 52000
+    gamma = g / 65536.0
+    dc = oracle.DynCache(n, g, T, 10, np.zeros(n, np.uint8))
+    real = np.zeros(n)
+    for w in range(4):
+        for j in range(T):
+            u = rng.choice(n, 80, replace=False).astype(np.int32)
+            dc.batch(u)
+            real *= gamma
+            real[u] += 1.0
+        dc.update()
+        # each rounding down loses at most one unit of 2^-8 per batch, and
+        # earlier losses only shrink under the decay
+        err = real * 256 - dc.S
+        assert np.all(err >= -1e-9) and np.all(err <= T * (w + 1) + 1e-9)
+
+
+def test_match_positions():
+    rng = np.random.default_rng(3)
+    prev = rng.choice(10000, 3000, replace=False).astype(np.int32)
+    cur = rng.choice(10000, 4000, replace=False).astype(np.int32)
+    pos = oracle.match(prev, cur, 10000)
+    where = {int(v): i for i, v in enumerate(prev)}
+    assert list(pos) == [where.get(int(v), -1) for v in cur]
+
+
+def test_overlap_and_greedy_order():
+    rng = np.random.default_rng(4)
+    lists = [rng.choice(2000, int(rng.integers(100, 900)), replace=False).astype(np.int32) for _ in range(7)]
+    O = oracle.overlap(lists, 2000)
+    for a in range(7):
+        for b in range(7):
+            assert O[a, b] == len(np.intersect1d(lists[a], lists[b]))
+    order = oracle.greedy_order(O, 2)
+    assert sorted(order) == list(range(7)) and order[0] == 2
+    for k in range(1, 7):  # each step takes the untaken batch overlapping most with the last
+        rest = [b for b in range(7) if b not in order[:k]]
+        best = max(rest, key=lambda b: (O[order[k - 1], b], -b))
+        assert order[k] == best
+    # a worked example: from batch 0, 0-2 overlap most, then 2-1 (1 beats 3 on the tie)
+    O2 = np.array([[9, 1, 5, 0], [1, 9, 4, 2], [5, 4, 9, 4], [0, 2, 4, 9]])
+    assert list(oracle.greedy_order(O2, 0)) == [0, 2, 1, 3]
