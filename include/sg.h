@@ -308,10 +308,90 @@ sg_status sg_gather(const sg_cache* c, const int32_t* d_ids, int64_t n_cap, cons
                     const int32_t* d_first, void* d_out, sg_gather_stats* d_stats, void* d_workspace,
                     size_t workspace_bytes, sg_stream_t stream);
 
+/* sg_gather with reuse of the previous batch's rows (FastGL explainer page,
+ * "Match-Reorder": consecutive sampled subgraphs share many nodes, so the
+ * features a batch shares with the previous one are copied from that
+ * batch's gathered rows, still in HBM, and only the rest is shipped):
+ *   d_pos        device int32 [n_cap]: for row i, the row of d_prev_rows that
+ *                holds node d_ids[i] (sg_match), or -1
+ *   d_prev_rows  device, the previous batch's gathered rows (same row size),
+ *                16-byte aligned; it must not overlap d_out
+ *   d_reused     device, accumulated (+=) count of rows copied from it, or
+ *                NULL; d_stats counts the other rows as with sg_gather
+ * Other arguments and the result as sg_gather: out row i = feature row
+ * d_ids[i], byte for byte. */
+sg_status sg_gather_reuse(const sg_cache* c, const int32_t* d_ids, int64_t n_cap, const int32_t* d_n,
+                          const int32_t* d_first, const int32_t* d_pos, const void* d_prev_rows, void* d_out,
+                          sg_gather_stats* d_stats, unsigned long long* d_reused, void* d_workspace,
+                          size_t workspace_bytes, sg_stream_t stream);
+
+/* Match (FastGL explainer page, "Match-Reorder"): d_pos[j] = the position of
+ * node d_cur[j] in d_prev (whose IDs are distinct), or -1.  Counts: the
+ * lists hold prev_cap / cur_cap entries, *d_prev_n / *d_cur_n of them when
+ * those device pointers are not NULL.  d_map: device int32 [n_nodes],
+ * caller-owned scratch that must be all -1 (bytes 0xFF) on entry and is all
+ * -1 again when the call's work is done.  d_matched: device int32,
+ * accumulated (+=) number of matches, or NULL.  IDs outside [0, n_nodes) set
+ * the device error word.  Asynchronous on `stream`. */
+sg_status sg_match(const int32_t* d_prev, int64_t prev_cap, const int32_t* d_prev_n, const int32_t* d_cur,
+                   int64_t cur_cap, const int32_t* d_cur_n, int32_t* d_map, int64_t n_nodes, int32_t* d_pos,
+                   int32_t* d_matched, sg_stream_t stream);
+
+/* Overlap matrix of a group of node lists (the Reorder step): list a is
+ * d_ids[h_off[a] .. h_off[a+1]) (distinct IDs within a list), 1..32 lists;
+ * d_overlap (device uint64 [n_lists x n_lists]) gets |list a ^ list b| at
+ * [a * n_lists + b] (the diagonal is a list's size).  d_mask: device uint32
+ * [n_nodes] scratch, all zero on entry and again after the call's work.
+ * Asynchronous on `stream`. */
+sg_status sg_overlap(const int32_t* d_ids, const int64_t* h_off, int32_t n_lists, uint32_t* d_mask, int64_t n_nodes,
+                     unsigned long long* d_overlap, sg_stream_t stream);
+
+/* Greedy order of a group (nearest overlap first; host only): h_order[0] =
+ * first, then each next list is the one not yet taken that overlaps most
+ * with the last one taken (ties: the lowest index).  h_overlap: host
+ * n_lists x n_lists as from sg_overlap; 1..1024 lists. */
+sg_status sg_greedy_order(const unsigned long long* h_overlap, int32_t n_lists, int32_t first, int32_t* h_order);
+
 /* Bytes of the workspace sg_gather uses to read the misses of up to n_cap
  * rows grouped by host-table region; 0 when the cache has no host table or
  * the table is small enough (under 32 GiB) that row order reads as fast. */
 size_t sg_gather_workspace(const sg_cache* c, int64_t n_cap);
+
+/* Bounded dynamic cache beside the static one (GARDEN page, Section IV-B,
+ * "Adaptive Dynamic Feature Caching", Eq. (5)-(6)).  It holds k_dyn more rows
+ * in HBM, chosen among the nodes the static cache misses by a decayed count
+ * of their recent accesses, and sg_gather serves a static miss from it when
+ * it can (counted as a hit).  Rows are byte-identical to the table's, so a
+ * gather's output does not depend on it.
+ * Scores (Eq. (5), read in windows of t_update batches and in fixed point):
+ * with gamma = gamma_q16 / 2^16 in (0, 1], batch j of a window (0-based)
+ * adds W_j = gamma^(t_update-1-j) (8 fractional bits, computed as
+ * W_{T-1} = 256, W_{j-1} = W_j * gamma_q16 >> 16) to A[v] for each of its
+ * nodes v that the static cache misses; after the window's last batch
+ *   S[v] = (S[v] * gamma^T >> 16) + A[v],  A[v] = 0
+ * (gamma^T in Q16 by repeated multiplication, rounded down each time), and
+ * the dynamic set becomes the k_dyn nodes of largest S > 0, ties by
+ * ascending ID (Eq. (6)).  Nodes that stay keep their slot; only entering
+ * nodes' rows are copied from the host table.  All sums are integers: the
+ * scores and the set are deterministic.
+ *   sg_dyn_cache_create  attaches the dynamic cache to c (which must leave
+ *                 rows to the host table); freed with the cache.  Synchronous.
+ *   sg_dyn_cache_batch   adds one batch's nodes (device IDs, n_cap entries,
+ *                 *d_n of them when d_n is not NULL; e.g. the sampler's unique
+ *                 array and its count of V_H) and, after every t_update-th
+ *                 call, updates the set.  Asynchronous on `stream`; order it
+ *                 after the gathers of the batch and before the next batch's
+ *                 gathers (the update changes the slots they read).  It
+ *                 keeps the window position on the host, so a captured CUDA
+ *                 graph would replay one position only.
+ *   sg_dyn_cache_info    k_dyn, the position in the window and, into host
+ *                 arrays when not NULL, the scores S [n_nodes] and the node in
+ *                 each slot [k_dyn] (-1: free); synchronises `stream`. */
+sg_status sg_dyn_cache_create(sg_cache* c, int64_t k_dyn, uint32_t gamma_q16, int32_t t_update, sg_stream_t stream);
+sg_status sg_dyn_cache_batch(sg_cache* c, const int32_t* d_ids, int64_t n_cap, const int32_t* d_n,
+                             sg_stream_t stream);
+sg_status sg_dyn_cache_info(const sg_cache* c, int64_t* k_dyn, int32_t* window_pos, uint32_t* h_score,
+                            int32_t* h_nodes, sg_stream_t stream);
 
 /* -------------------------------------------------------------- aggregate */
 /* Mean aggregation over one block (GARDEN page Section II-A Eq. (1) with

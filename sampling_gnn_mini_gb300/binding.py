@@ -43,7 +43,9 @@ EXPORTS = ["sg_version", "sg_last_error", "sg_stream_check", "sg_graph_load", "s
            "sg_aggregate_bwd", "sg_read_probe", "sg_hash_probe", "sg_relabel_noalloc", "sg_transpose_workspace",
            "sg_transpose_blocks", "sg_aggregate_bwd_t", "sg_sampler_workspace_init", "sg_gather_workspace",
            "sg_sage_fwd", "sg_sage_bwd", "sg_sage_bwd_workspace", "sg_wait_probe", "sg_wait_probe_workspace",
-           "sg_access_stats", "sg_rank_workspace", "sg_rank_by_score", "sg_graph_renumber", "sg_graph_copy_out"]
+           "sg_access_stats", "sg_rank_workspace", "sg_rank_by_score", "sg_graph_renumber", "sg_graph_copy_out",
+           "sg_dyn_cache_create", "sg_dyn_cache_batch", "sg_dyn_cache_info", "sg_gather_reuse", "sg_match",
+           "sg_overlap", "sg_greedy_order"]
 
 
 class SgError(RuntimeError):
@@ -130,6 +132,13 @@ def load(build_if_missing: bool = True):
             "sg_rank_by_score": (i32, [vp, i64, vp, vp, vp, sz, vp]),
             "sg_graph_renumber": (i32, [vp, vp, vp, ctypes.POINTER(vp), vp]),
             "sg_graph_copy_out": (i32, [vp, vp, vp]),
+            "sg_dyn_cache_create": (i32, [vp, i64, ctypes.c_uint32, i32, vp]),
+            "sg_dyn_cache_batch": (i32, [vp, vp, i64, vp, vp]),
+            "sg_dyn_cache_info": (i32, [vp, vp, vp, vp, vp, vp]),
+            "sg_gather_reuse": (i32, [vp, vp, i64, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+            "sg_match": (i32, [vp, i64, vp, vp, i64, vp, vp, i64, vp, vp, vp]),
+            "sg_overlap": (i32, [vp, vp, i32, vp, i64, vp, vp]),
+            "sg_greedy_order": (i32, [vp, i32, i32, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -408,6 +417,31 @@ def sg_cache_build(h_feat: Optional[torch.Tensor], d_feat: Optional[torch.Tensor
     return Cache(out.value, h_feat)
 
 
+def sg_dyn_cache_create(cache: Cache, k_dyn: int, gamma_q16: int, t_update: int, stream=None) -> None:
+    """Attaches the bounded dynamic cache (Eq. (5)-(6)) to cache; see sg.h."""
+    _check(load().sg_dyn_cache_create(cache.handle, int(k_dyn), int(gamma_q16), int(t_update), _stream(stream)))
+
+
+def sg_dyn_cache_batch(cache: Cache, ids: torch.Tensor, n_cap: int, d_n: Optional[torch.Tensor] = None,
+                       stream=None) -> None:
+    """Adds one batch's nodes to the dynamic cache's scores (and updates the
+    set at the end of a window)."""
+    _check(load().sg_dyn_cache_batch(cache.handle, ids.data_ptr() if n_cap else None, int(n_cap), _ptr(d_n),
+                                     _stream(stream)))
+
+
+def sg_dyn_cache_state(cache: Cache, stream=None):
+    """(k_dyn, window position, scores, node per slot), the last two as host
+    numpy copies (synchronises the stream)."""
+    lib = load()
+    k, j = ctypes.c_int64(), ctypes.c_int32()
+    _check(lib.sg_dyn_cache_info(cache.handle, ctypes.byref(k), ctypes.byref(j), None, None, _stream(stream)))
+    S = np.empty(cache.n_nodes, np.uint32)
+    nodes = np.empty(max(1, k.value), np.int32)
+    _check(lib.sg_dyn_cache_info(cache.handle, None, None, S.ctypes.data, nodes.ctypes.data, _stream(stream)))
+    return k.value, j.value, S, nodes[: k.value]
+
+
 def sg_gather_workspace(cache: Cache, n_cap: int) -> int:
     return int(load().sg_gather_workspace(cache.handle, int(n_cap)))
 
@@ -418,6 +452,48 @@ def sg_gather(cache: Cache, ids: torch.Tensor, n_cap: int, d_n: Optional[torch.T
     _check(load().sg_gather(cache.handle, ids.data_ptr(), int(n_cap), _ptr(d_n), _ptr(d_first), out.data_ptr(),
                             _ptr(stats), _ptr(workspace), 0 if workspace is None else workspace.numel(),
                             _stream(stream)))
+
+
+def sg_gather_reuse(cache: Cache, ids: torch.Tensor, n_cap: int, d_n: Optional[torch.Tensor], pos: torch.Tensor,
+                    prev_rows: torch.Tensor, out: torch.Tensor, stats: Optional[torch.Tensor] = None,
+                    reused: Optional[torch.Tensor] = None, stream=None, d_first: Optional[torch.Tensor] = None,
+                    workspace: Optional[torch.Tensor] = None) -> None:
+    """sg_gather that copies matched rows (pos >= 0) from the previous
+    batch's rows (see sg.h)."""
+    _check(load().sg_gather_reuse(cache.handle, ids.data_ptr(), int(n_cap), _ptr(d_n), _ptr(d_first), pos.data_ptr(),
+                                  prev_rows.data_ptr(), out.data_ptr(), _ptr(stats), _ptr(reused), _ptr(workspace),
+                                  0 if workspace is None else workspace.numel(), _stream(stream)))
+
+
+def sg_match(prev: torch.Tensor, prev_cap: int, prev_n: Optional[torch.Tensor], cur: torch.Tensor, cur_cap: int,
+             cur_n: Optional[torch.Tensor], match_map: torch.Tensor, pos: torch.Tensor,
+             matched: Optional[torch.Tensor] = None, stream=None) -> None:
+    """pos[j] = position of cur[j] in prev or -1; match_map: int32 [n_nodes]
+    all -1 (left so); see sg.h."""
+    _check(load().sg_match(prev.data_ptr() if prev_cap else None, int(prev_cap), _ptr(prev_n),
+                           cur.data_ptr() if cur_cap else None, int(cur_cap), _ptr(cur_n), match_map.data_ptr(),
+                           int(match_map.numel()), pos.data_ptr() if cur_cap else None, _ptr(matched),
+                           _stream(stream)))
+
+
+def sg_overlap(ids: torch.Tensor, offsets: Sequence[int], mask: torch.Tensor, stream=None) -> torch.Tensor:
+    """G x G overlap matrix (device int64) of the lists ids[off[a]:off[a+1]];
+    mask: int32/uint32 [n_nodes] all zero (left so)."""
+    off = np.ascontiguousarray(offsets, dtype=np.int64)
+    G = len(off) - 1
+    out = torch.empty((G, G), dtype=torch.int64, device=mask.device)
+    _check(load().sg_overlap(ids.data_ptr() if off[-1] else None, off.ctypes.data, G, mask.data_ptr(),
+                             int(mask.numel()), out.data_ptr(), _stream(stream)))
+    return out
+
+
+def sg_greedy_order(overlap: np.ndarray, first: int = 0) -> np.ndarray:
+    """Nearest-overlap-first order of a group (host)."""
+    O = np.ascontiguousarray(overlap, dtype=np.uint64)
+    G = O.shape[0]
+    order = np.empty(G, np.int32)
+    _check(load().sg_greedy_order(O.ctypes.data, G, int(first), order.ctypes.data))
+    return order
 
 
 def sg_sage_fwd(h: torch.Tensor, m: torch.Tensor, W: torch.Tensor, n_cap: int, d_n: Optional[torch.Tensor],

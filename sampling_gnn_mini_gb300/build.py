@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libsg.so")
-SOURCES = ["sg_api.cu", "sg_sampler.cu", "sg_gather.cu", "sg_aggregate.cu", "sg_update.cu", "sg_recode.cu"]
+SOURCES = ["sg_api.cu", "sg_sampler.cu", "sg_gather.cu", "sg_aggregate.cu", "sg_update.cu", "sg_recode.cu", "sg_dyncache.cu", "sg_match.cu"]
 HEADERS = ["sg_internal.cuh", "sg_objects.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -205,7 +205,8 @@ extern "C" sg_status sg_stream_check(sg_stream_t stream) {
     cudaStream_t s = (cudaStream_t)stream;
     SG_CUDA(cudaStreamSynchronize(s));
     unsigned w = fetch_err_api(s) | fetch_err_sampler(s) | fetch_err_gather(s) | fetch_err_aggregate(s) |
-               fetch_err_update(s) | fetch_err_recode(s);
+               fetch_err_update(s) | fetch_err_recode(s) |
+               fetch_err_dyncache(s) | fetch_err_match(s);
     if (w & 0x80000000u) return fail(SG_ERR_CUDA, "sg_stream_check: could not read the device error word");
     if (w & ERR_INDEX) return fail(SG_ERR_INVALID_INDEX, "a kernel met a node ID or index out of range");
     if (w & ERR_CAPACITY) return fail(SG_ERR_CAPACITY, "a device table or buffer bound was exceeded");
@@ -389,6 +390,7 @@ extern "C" sg_status sg_cache_build(const void* h_feat, const void* d_feat, int3
 
 extern "C" sg_status sg_cache_destroy(sg_cache* c) {
     if (!c) return SG_OK;
+    dyn_cache_free(c);
     if (c->rows) cudaFree(c->rows);
     if (c->slot_of) cudaFree(c->slot_of);
     delete c;

@@ -16,6 +16,8 @@
 // Hit test: with a slot map (a cache built from a ranked list), slot_of[g];
 // without one (an ID-range cache, hot nodes recoded to the smallest IDs),
 // node g is cached in slot g exactly when g < n_cache, and no map is read.
+// A static miss is then looked up in the dynamic cache, when there is one
+// (counted as a hit when found there).
 //
 // Large host tables (32 GiB and more) with a workspace: random zero-copy
 // reads there lose most of their rate to address translation (measured on
@@ -43,6 +45,23 @@ __device__ __forceinline__ int64_t slot_for(const int32_t* __restrict__ slot_of,
     return (int64_t)g < n_cache ? (int64_t)g : -1;
 }
 
+// The optional dynamic cache beside the static one: a static miss g is read
+// from dyn_rows[dyn_slot[g]] when that slot is not -1.
+struct DynView {
+    const int32_t* slot;
+    const uint4* rows;
+};
+
+// Optional reuse of the previous batch's rows (FastGL explainer page,
+// "Match-Reorder"): row i with pos[i] >= 0 is copied from prev[pos[i]], the
+// previous batch's gathered features still resident in HBM, and counted in
+// *reused instead of hits or misses.
+struct ReuseView {
+    const int32_t* pos;
+    const uint4* prev;
+    unsigned long long* reused;
+};
+
 __global__ void __launch_bounds__(kThreads) k_gather(const int32_t* __restrict__ ids, const int32_t* __restrict__ d_n,
                                                      const int32_t* __restrict__ d_first,
                                                      int64_t n_cap, const int32_t* __restrict__ slot_of, int64_t n_cache,
@@ -50,7 +69,8 @@ __global__ void __launch_bounds__(kThreads) k_gather(const int32_t* __restrict__
                                                      const uint4* __restrict__ cache, const uint4* __restrict__ host,
                                                      int32_t row_vecs, int64_t step_rows, int32_t step_rem,
                                                      uint4* __restrict__ out, sg_gather_stats* __restrict__ stats,
-                                                     uint32_t* __restrict__ region_cnt, int32_t region_shift) {
+                                                     uint32_t* __restrict__ region_cnt, int32_t region_shift,
+                                                     DynView dyn, ReuseView reuse) {
     pdl_start();
     int64_t n = n_cap;
     if (d_n) {
@@ -69,7 +89,7 @@ __global__ void __launch_bounds__(kThreads) k_gather(const int32_t* __restrict__
     int64_t t = first * row_vecs + blockIdx.x * (int64_t)kThreads + threadIdx.x;
     int64_t i = t / row_vecs;
     int32_t c = (int32_t)(t - i * row_vecs);
-    unsigned long long hits = 0, misses = 0;
+    unsigned long long hits = 0, misses = 0, reused = 0;
     while (t < total) {
         uint4 v[kUnroll];
         int64_t dst[kUnroll];
@@ -78,14 +98,22 @@ __global__ void __launch_bounds__(kThreads) k_gather(const int32_t* __restrict__
             dst[u] = -1;
             if (t < total) {
                 const int32_t g = __ldg(ids + i);
+                const int32_t rp = reuse.pos ? __ldg(reuse.pos + i) : -1;
                 dst[u] = t;
-                if (g < 0 || (int64_t)g >= n_nodes) {
+                if (rp >= 0) {
+                    v[u] = __ldcs(reuse.prev + (int64_t)rp * row_vecs + c);
+                    reused += (c == 0);
+                } else if (g < 0 || (int64_t)g >= n_nodes) {
                     if (c == 0) dev_err(ERR_INDEX);
                     v[u] = make_uint4(0, 0, 0, 0);
                 } else {
                     const int64_t s = slot_for(slot_of, n_cache, g);
+                    const int32_t ds = (s < 0 && dyn.slot) ? __ldg(dyn.slot + g) : -1;
                     if (s >= 0) {
                         v[u] = __ldcs(cache + (int64_t)s * row_vecs + c);
+                        hits += (c == 0);
+                    } else if (ds >= 0) {
+                        v[u] = __ldcs(dyn.rows + (int64_t)ds * row_vecs + c);
                         hits += (c == 0);
                     } else if (region_cnt) {  // left for k_gather_list
                         if (c == 0) atomicAdd(region_cnt + (g >> region_shift), 1u);
@@ -116,6 +144,10 @@ __global__ void __launch_bounds__(kThreads) k_gather(const int32_t* __restrict__
             atomicAdd(&stats->hits, hits);
             atomicAdd(&stats->misses, misses);
         }
+    }
+    if (reuse.reused) {
+        reused = warp_sum(reused);
+        if (lane_id() == 0 && reused) atomicAdd(reuse.reused, reused);
     }
 }
 
@@ -169,14 +201,17 @@ __global__ void __launch_bounds__(kThreads) k_region_scatter(const int32_t* __re
                                                              const int32_t* __restrict__ slot_of, int64_t n_cache,
                                                              int64_t n_nodes,
                                                              uint32_t* __restrict__ cnt, int32_t region_shift,
-                                                             int32_t* __restrict__ list) {
+                                                             int32_t* __restrict__ list, DynView dyn,
+                                                             const int32_t* __restrict__ reuse_pos) {
     pdl_start();
     int64_t first, n;
     gather_range(d_n, d_first, n_cap, first, n);
     for (int64_t i = first + blockIdx.x * (int64_t)kThreads + threadIdx.x; i < n; i += (int64_t)gridDim.x * kThreads) {
         const int32_t g = __ldg(ids + i);
         if (g < 0 || (int64_t)g >= n_nodes) continue;
+        if (reuse_pos && __ldg(reuse_pos + i) >= 0) continue;
         if (slot_for(slot_of, n_cache, g) >= 0) continue;
+        if (dyn.slot && __ldg(dyn.slot + g) >= 0) continue;
         const uint32_t pos = atomicAdd(cnt + (g >> region_shift), 1u);
         if ((int64_t)pos < n_cap) list[pos] = (int32_t)i;
         else dev_err(ERR_CAPACITY);
@@ -234,9 +269,10 @@ extern "C" size_t sg_gather_workspace(const sg_cache* c, int64_t n_cap) {
     return a256((size_t)(c->n_regions + 1) * sizeof(uint32_t)) + a256((size_t)n_cap * sizeof(int32_t));
 }
 
-extern "C" sg_status sg_gather(const sg_cache* c, const int32_t* d_ids, int64_t n_cap, const int32_t* d_n,
-                               const int32_t* d_first, void* d_out, sg_gather_stats* d_stats, void* d_workspace,
-                               size_t workspace_bytes, sg_stream_t stream) {
+namespace {
+sg_status gather_impl(const sg_cache* c, const int32_t* d_ids, int64_t n_cap, const int32_t* d_n,
+                      const int32_t* d_first, void* d_out, sg_gather_stats* d_stats, void* d_workspace,
+                      size_t workspace_bytes, ReuseView reuse, sg_stream_t stream) {
     if (!c) return fail(SG_ERR_INVALID_ARG, "sg_gather: NULL cache");
     if (n_cap < 0) return fail(SG_ERR_INVALID_ARG, "sg_gather: n_cap < 0");
     if (n_cap == 0) return SG_OK;
@@ -263,18 +299,39 @@ extern "C" sg_status sg_gather(const sg_cache* c, const int32_t* d_ids, int64_t 
     int32_t* list = by_region ? (int32_t*)((char*)d_workspace + a256((size_t)(c->n_regions + 1) * sizeof(uint32_t)))
                               : nullptr;
     if (by_region) SG_CUDA(cudaMemsetAsync(cnt, 0, (size_t)(c->n_regions + 1) * sizeof(uint32_t), s));
+    DynView dyn;
+    dyn.slot = c->dyn ? c->dyn->slot : nullptr;
+    dyn.rows = c->dyn ? (const uint4*)c->dyn->rows : nullptr;
     SG_CUDA(launch_pdl(k_gather, dim3((unsigned)blocks), dim3(kThreads), 0, s, d_ids, d_n, d_first,
                        n_cap, c->slot_of, c->n_cache, c->n_nodes, (const uint4*)c->rows, (const uint4*)c->host_rows,
                        (int32_t)row_vecs, stride / row_vecs, (int32_t)(stride % row_vecs), (uint4*)d_out, d_stats,
-                       cnt, c->region_shift));
+                       cnt, c->region_shift, dyn, reuse));
     if (!by_region) return SG_OK;
     SG_CUDA(launch_pdl(k_region_scan, dim3(1), dim3(kScanThreads), 0, s, cnt, c->n_regions));
     int64_t sblocks = cdiv(n_cap, (int64_t)kThreads);
     if (sblocks > cap) sblocks = cap;
     SG_CUDA(launch_pdl(k_region_scatter, dim3((unsigned)sblocks), dim3(kThreads), 0, s, d_ids, d_n, d_first, n_cap,
-                       c->slot_of, c->n_cache, c->n_nodes, cnt, c->region_shift, list));
+                       c->slot_of, c->n_cache, c->n_nodes, cnt, c->region_shift, list, dyn, reuse.pos));
     SG_CUDA(launch_pdl(k_gather_list, dim3((unsigned)blocks), dim3(kThreads), 0, s, (const int32_t*)list,
                        (const uint32_t*)(cnt + c->n_regions), d_ids, (const uint4*)c->host_rows, (int32_t)row_vecs,
                        n_cap, stride / row_vecs, (int32_t)(stride % row_vecs), (uint4*)d_out));
     return SG_OK;
+}
+}  // namespace
+
+extern "C" sg_status sg_gather(const sg_cache* c, const int32_t* d_ids, int64_t n_cap, const int32_t* d_n,
+                               const int32_t* d_first, void* d_out, sg_gather_stats* d_stats, void* d_workspace,
+                               size_t workspace_bytes, sg_stream_t stream) {
+    ReuseView none = {nullptr, nullptr, nullptr};
+    return gather_impl(c, d_ids, n_cap, d_n, d_first, d_out, d_stats, d_workspace, workspace_bytes, none, stream);
+}
+
+extern "C" sg_status sg_gather_reuse(const sg_cache* c, const int32_t* d_ids, int64_t n_cap, const int32_t* d_n,
+                                     const int32_t* d_first, const int32_t* d_pos, const void* d_prev_rows,
+                                     void* d_out, sg_gather_stats* d_stats, unsigned long long* d_reused,
+                                     void* d_workspace, size_t workspace_bytes, sg_stream_t stream) {
+    if (!d_pos || !d_prev_rows) return fail(SG_ERR_INVALID_ARG, "sg_gather_reuse: NULL match positions or rows");
+    if (((uintptr_t)d_prev_rows) % 16) return fail(SG_ERR_INVALID_ARG, "sg_gather_reuse: rows must be 16-byte aligned");
+    ReuseView r = {d_pos, (const uint4*)d_prev_rows, d_reused};
+    return gather_impl(c, d_ids, n_cap, d_n, d_first, d_out, d_stats, d_workspace, workspace_bytes, r, stream);
 }

@@ -49,6 +49,18 @@ unsigned fetch_err_aggregate(cudaStream_t);
 unsigned fetch_err_api(cudaStream_t);
 unsigned fetch_err_update(cudaStream_t);
 unsigned fetch_err_recode(cudaStream_t);
+unsigned fetch_err_dyncache(cudaStream_t);
+unsigned fetch_err_match(cudaStream_t);
+
+// ------------------------------------------------------------- ranking
+// Nodes by descending 32-bit score, ties by ascending ID, into order[n]
+// (sg_rank_by_score without argument checks); workspace of rank_ws_bytes(n)
+// bytes, 256-byte aligned.
+size_t rank_ws_bytes(int64_t n);
+sg_status rank_scores(const uint32_t* score, int64_t n, int32_t* order, void* ws, cudaStream_t s);
+
+// Frees a cache's dynamic cache, if any (sg_cache_destroy).
+void dyn_cache_free(::sg_cache* c);
 
 // ------------------------------------------------- allocation (owned memory)
 // Every device allocation the library owns goes through dev_alloc.  With the

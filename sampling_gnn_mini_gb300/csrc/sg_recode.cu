@@ -361,17 +361,14 @@ extern "C" sg_status sg_access_stats(const sg_blocks* blocks, int64_t unique_cap
 
 extern "C" size_t sg_rank_workspace(int64_t n_nodes) {
     if (n_nodes <= 0 || n_nodes > 2147483647LL) return 0;
-    return rank_layout(n_nodes).total;
+    return rank_ws_bytes(n_nodes);
 }
 
-extern "C" sg_status sg_rank_by_score(const uint32_t* d_score, int64_t n_nodes, int32_t* d_order, int32_t* d_rank_of,
-                                      void* d_workspace, size_t workspace_bytes, sg_stream_t stream) {
-    if (n_nodes <= 0 || n_nodes > 2147483647LL) return fail(SG_ERR_INVALID_ARG, "sg_rank_by_score: n_nodes out of range");
-    if (!d_score || !d_order || !d_workspace) return fail(SG_ERR_INVALID_ARG, "sg_rank_by_score: NULL argument");
+namespace sgi {
+size_t rank_ws_bytes(int64_t n) { return rank_layout(n).total; }
+
+sg_status rank_scores(const uint32_t* d_score, int64_t n_nodes, int32_t* d_order, void* d_workspace, cudaStream_t s) {
     const RankLayout L = rank_layout(n_nodes);
-    if (workspace_bytes < L.total || ((uintptr_t)d_workspace) % 256)
-        return fail(SG_ERR_INVALID_ARG, "sg_rank_by_score: workspace needs %zu bytes, 256-byte aligned", L.total);
-    cudaStream_t s = (cudaStream_t)stream;
     char* ws = (char*)d_workspace;
     uint32_t* keys[2] = {(uint32_t*)(ws + L.keys0), (uint32_t*)(ws + L.keys1)};
     int32_t* vals[2] = {(int32_t*)(ws + L.vals), d_order};
@@ -394,6 +391,20 @@ extern "C" sg_status sg_rank_by_score(const uint32_t* d_score, int64_t n_nodes, 
                                                        L.nb, kout, vout);
         SG_CHECK_LAUNCH("k_radix_scatter");
     }
+    return SG_OK;
+}
+}  // namespace sgi
+
+extern "C" sg_status sg_rank_by_score(const uint32_t* d_score, int64_t n_nodes, int32_t* d_order, int32_t* d_rank_of,
+                                      void* d_workspace, size_t workspace_bytes, sg_stream_t stream) {
+    if (n_nodes <= 0 || n_nodes > 2147483647LL) return fail(SG_ERR_INVALID_ARG, "sg_rank_by_score: n_nodes out of range");
+    if (!d_score || !d_order || !d_workspace) return fail(SG_ERR_INVALID_ARG, "sg_rank_by_score: NULL argument");
+    const size_t need = rank_ws_bytes(n_nodes);
+    if (workspace_bytes < need || ((uintptr_t)d_workspace) % 256)
+        return fail(SG_ERR_INVALID_ARG, "sg_rank_by_score: workspace needs %zu bytes, 256-byte aligned", need);
+    cudaStream_t s = (cudaStream_t)stream;
+    sg_status st = rank_scores(d_score, n_nodes, d_order, d_workspace, s);
+    if (st != SG_OK) return st;
     if (d_rank_of) {
         k_rank_scatter<<<num_sms() * 8, kNT, 0, s>>>(d_order, n_nodes, d_rank_of);
         SG_CHECK_LAUNCH("k_rank_scatter");
