@@ -75,6 +75,10 @@ def _load():
         lib.orc_rank_by_score.argtypes = [vp, i64, vp, vp]
         lib.orc_graph_renumber.restype = None
         lib.orc_graph_renumber.argtypes = [vp, vp, i64, vp, vp, vp, vp]
+        lib.orc_in_degree.restype = None
+        lib.orc_in_degree.argtypes = [vp, i64, i64, vp]
+        lib.orc_rank_by_score_tie.restype = None
+        lib.orc_rank_by_score_tie.argtypes = [vp, vp, i64, vp, vp]
         u32 = ctypes.c_uint32
         lib.orc_dyn_weights.restype = u32
         lib.orc_dyn_weights.argtypes = [u32, i32, vp]
@@ -338,14 +342,27 @@ def access_stats(blocks: Blocks, omega, w_in: int, score: np.ndarray) -> None:
     _load().orc_access_stats(_p(un), _p(hop), blocks.n_hops, _p(om), int(w_in), _p(score))
 
 
-def rank_by_score(score: np.ndarray):
-    """(order, rank_of): nodes by descending score, ties by ascending ID."""
+def rank_by_score(score: np.ndarray, tie: np.ndarray = None):
+    """(order, rank_of): nodes by descending score, then (when given)
+    descending tie key, then ascending ID."""
     sc = np.ascontiguousarray(score, dtype=np.uint32)
     n = len(sc)
     order = np.zeros(max(1, n), np.int32)
     rank_of = np.zeros(max(1, n), np.int32)
-    _load().orc_rank_by_score(_p(sc), n, _p(order), _p(rank_of))
+    if tie is None:
+        _load().orc_rank_by_score(_p(sc), n, _p(order), _p(rank_of))
+    else:
+        tk = np.ascontiguousarray(tie, dtype=np.uint32)
+        _load().orc_rank_by_score_tie(_p(sc), _p(tk), n, _p(order), _p(rank_of))
     return order[:n], rank_of[:n]
+
+
+def in_degree(indices, n_nodes: int) -> np.ndarray:
+    """uint32 [n_nodes]: how many CSR positions name each node."""
+    ix = np.ascontiguousarray(indices, dtype=np.int32)
+    deg = np.zeros(max(1, n_nodes), np.uint32)
+    _load().orc_in_degree(_p(ix), len(ix), int(n_nodes), _p(deg))
+    return deg[:n_nodes]
 
 
 def graph_renumber(indptr, indices, order, rank_of):

@@ -537,3 +537,31 @@ void orc_greedy_order(const int64_t* O, int32_t G, int32_t first, int32_t* order
         taken[best] = 1;
     }
 }
+
+/* In-degree of every node: the number of CSR positions that name it (how
+ * often uniform neighbour sampling can reach it). */
+void orc_in_degree(const int32_t* indices, int64_t m, int64_t n, uint32_t* deg) {
+    for (int64_t v = 0; v < n; v++) deg[v] = 0;
+    for (int64_t e = 0; e < m; e++) deg[indices[e]]++;
+}
+
+/* Ranking with a second key: descending score, then descending tie key,
+ * then ascending ID.  Reading: Eq. (4) gives no score to the nodes the
+ * presampled batches never reach (and equal scores to many others); their
+ * in-degree, the chance uniform neighbour sampling reaches them, orders
+ * them (GARDEN page, Section IV-A: hot nodes first). */
+static const uint32_t* g_rank_tie;
+static int cmp_rank2(const void* a, const void* b) {
+    int32_t u = *(const int32_t*)a, v = *(const int32_t*)b;
+    if (g_rank_score[u] != g_rank_score[v]) return g_rank_score[u] > g_rank_score[v] ? -1 : 1;
+    if (g_rank_tie[u] != g_rank_tie[v]) return g_rank_tie[u] > g_rank_tie[v] ? -1 : 1;
+    return (u > v) - (u < v);
+}
+
+void orc_rank_by_score_tie(const uint32_t* score, const uint32_t* tie, int64_t n, int32_t* order, int32_t* rank_of) {
+    for (int64_t v = 0; v < n; v++) order[v] = (int32_t)v;
+    g_rank_score = score;
+    g_rank_tie = tie;
+    qsort(order, (size_t)n, sizeof(int32_t), cmp_rank2);
+    for (int64_t r = 0; r < n; r++) rank_of[order[r]] = (int32_t)r;
+}

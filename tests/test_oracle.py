@@ -629,3 +629,15 @@ def test_overlap_and_greedy_order():
     # a worked example: from batch 0, 0-2 overlap most, then 2-1 (1 beats 3 on the tie)
     O2 = np.array([[9, 1, 5, 0], [1, 9, 4, 2], [5, 4, 9, 4], [0, 2, 4, 9]])
     assert list(oracle.greedy_order(O2, 0)) == [0, 2, 1, 3]
+
+
+def test_in_degree_and_ranking_with_a_tie_key():
+    g = synth.chung_lu(3000, 8.0, 2.1, 200.0, 9)
+    deg = oracle.in_degree(g.indices, g.n)
+    assert np.array_equal(deg, np.bincount(g.indices, minlength=g.n))
+    rng = np.random.default_rng(6)
+    score = rng.integers(0, 3, size=g.n).astype(np.uint32)  # mostly ties
+    order, rank_of = oracle.rank_by_score(score, deg)
+    want = np.lexsort((np.arange(g.n), -deg.astype(np.int64), -score.astype(np.int64)))
+    assert np.array_equal(order, want)
+    assert np.array_equal(rank_of[order], np.arange(g.n))
