@@ -465,17 +465,29 @@ def run_ours(args, rank, world, local):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         ov.start_after(stream)
+        marks = []
         for s_ in range(args.steps):
-            ov.step(inputs(first + s_), after(first + s_))
+            p = ov.step(inputs(first + s_), after(first + s_))
+            if ov.depth == 1:  # one batch at a time: an event per step gives its duration
+                e = torch.cuda.Event(enable_timing=True)
+                e.record(ov.streams[0])
+                marks.append(e)
         ov.wait_all(stream)
         b.record(stream)
         torch.cuda.synchronize(dev)
         for s_ in ov.streams:
             sg.sg_stream_check(s_)
+        if marks:
+            prev = a
+            for e in marks:
+                step_ms.append(prev.elapsed_time(e))
+                prev = e
         return a.elapsed_time(b)
 
     # a first region on the warm-up pool's last K batches sizes the repeats
+    step_ms = []
     calib_ms = timed_region(seeds_pool, hseed_pool, args.warmup, counts_log)
+    step_ms.clear()
     repeats = max(1, int(np.ceil(args.min_seconds * 1e3 / max(calib_ms, 1e-3))))
     log("calibration region %.2f ms for %d steps: %d timed regions" % (calib_ms, args.steps, repeats))
     if world > 1:  # every rank runs the same number of regions
@@ -637,6 +649,8 @@ def run_ours(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
         "timed_regions": {"repeats": repeats, "median_ms": elapsed_ms, "min_ms": min(region_ms),
                           "max_ms": max(region_ms), "seconds": sum(region_ms) / 1e3,
+                          "step_ms_percentiles": None if not step_ms else
+                          {q: float(np.percentile(step_ms, q)) for q in (10, 50, 90, 99, 100)},
                           "note": "the timed region of `steps` steps runs `repeats` times on new batches until "
                                   "%.1f s have elapsed; the line reports the median region by throughput"
                                   % args.min_seconds},

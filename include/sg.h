@@ -476,14 +476,22 @@ sg_status sg_access_stats(const sg_blocks* blocks, int64_t unique_cap, int32_t n
                           const uint32_t* h_omega, uint32_t w_in, uint32_t* d_score, int64_t n_nodes,
                           sg_stream_t stream);
 
-/* Nodes ordered by descending score, ties by ascending ID: d_order[r]
- * (device int32 [n_nodes]) is the node of rank r and, when d_rank_of is not
- * NULL, d_rank_of[v] (device int32 [n_nodes]) the rank of node v.  A stable
- * radix sort; the result is deterministic.  Workspace:
+/* Nodes ordered by descending score, then (when d_tie is not NULL) by
+ * descending tie key, then by ascending ID: d_order[r] (device int32
+ * [n_nodes]) is the node of rank r and, when d_rank_of is not NULL,
+ * d_rank_of[v] (device int32 [n_nodes]) the rank of node v.  d_score and
+ * d_tie: device uint32 [n_nodes].  Presampled statistics leave most nodes of
+ * a large graph without a score; their in-degree (sg_graph_in_degree), the
+ * chance that uniform neighbour sampling reaches them, is the natural tie
+ * key.  Stable radix sorts; the result is deterministic.  Workspace:
  * sg_rank_workspace(n_nodes) bytes, 256-byte aligned (0 on bad sizes). */
 size_t sg_rank_workspace(int64_t n_nodes);
-sg_status sg_rank_by_score(const uint32_t* d_score, int64_t n_nodes, int32_t* d_order, int32_t* d_rank_of,
-                           void* d_workspace, size_t workspace_bytes, sg_stream_t stream);
+sg_status sg_rank_by_score(const uint32_t* d_score, const uint32_t* d_tie, int64_t n_nodes, int32_t* d_order,
+                           int32_t* d_rank_of, void* d_workspace, size_t workspace_bytes, sg_stream_t stream);
+
+/* In-degree of every node of a graph: d_deg[u] (device uint32 [n_nodes]) =
+ * the number of CSR positions naming u.  Asynchronous on `stream`. */
+sg_status sg_graph_in_degree(const sg_graph* g, uint32_t* d_deg, sg_stream_t stream);
 
 /* Recodes a graph's nodes (GARDEN page Section IV-A: the allocator gives the
  * high-frequency nodes compact IDs): the new graph's row r is the old row

@@ -45,7 +45,7 @@ EXPORTS = ["sg_version", "sg_last_error", "sg_stream_check", "sg_graph_load", "s
            "sg_sage_fwd", "sg_sage_bwd", "sg_sage_bwd_workspace", "sg_wait_probe", "sg_wait_probe_workspace",
            "sg_access_stats", "sg_rank_workspace", "sg_rank_by_score", "sg_graph_renumber", "sg_graph_copy_out",
            "sg_dyn_cache_create", "sg_dyn_cache_batch", "sg_dyn_cache_info", "sg_gather_reuse", "sg_match",
-           "sg_overlap", "sg_greedy_order"]
+           "sg_overlap", "sg_greedy_order", "sg_graph_in_degree"]
 
 
 class SgError(RuntimeError):
@@ -129,7 +129,8 @@ def load(build_if_missing: bool = True):
             "sg_wait_probe_workspace": (sz, [i32]),
             "sg_access_stats": (i32, [ctypes.POINTER(_Blocks), i64, i32, i32, vp, ctypes.c_uint32, vp, i64, vp]),
             "sg_rank_workspace": (sz, [i64]),
-            "sg_rank_by_score": (i32, [vp, i64, vp, vp, vp, sz, vp]),
+            "sg_rank_by_score": (i32, [vp, vp, i64, vp, vp, vp, sz, vp]),
+            "sg_graph_in_degree": (i32, [vp, vp, vp]),
             "sg_graph_renumber": (i32, [vp, vp, vp, ctypes.POINTER(vp), vp]),
             "sg_graph_copy_out": (i32, [vp, vp, vp]),
             "sg_dyn_cache_create": (i32, [vp, i64, ctypes.c_uint32, i32, vp]),
@@ -342,9 +343,10 @@ def sg_access_stats(buffers: "SampleBuffers", omega: Sequence[int], w_in: int, s
                                   om.ctypes.data, int(w_in), score.data_ptr(), int(score.numel()), _stream(stream)))
 
 
-def sg_rank_by_score(score: torch.Tensor, stream=None):
+def sg_rank_by_score(score: torch.Tensor, tie: Optional[torch.Tensor] = None, stream=None):
     """(order, rank_of) device int32 tensors: nodes by descending score (the
-    32-bit unsigned contents of score), ties by ascending ID."""
+    32-bit unsigned contents of score), then descending tie key (when
+    given), then ascending ID."""
     lib = load()
     n = int(score.numel())
     nbytes = int(lib.sg_rank_workspace(n))
@@ -353,9 +355,18 @@ def sg_rank_by_score(score: torch.Tensor, stream=None):
     order = torch.empty(n, dtype=torch.int32, device=score.device)
     rank_of = torch.empty(n, dtype=torch.int32, device=score.device)
     ws = _aligned_bytes(nbytes, score.device)
-    _check(lib.sg_rank_by_score(score.data_ptr(), n, order.data_ptr(), rank_of.data_ptr(), ws.data_ptr(), ws.numel(),
-                                _stream(stream)))
+    if tie is not None and (tie.numel() != n or tie.element_size() != 4 or not tie.is_cuda):
+        raise SgError(SG_ERR_INVALID_ARG, "sg_rank_by_score: tie must be a 32-bit device tensor like score")
+    _check(lib.sg_rank_by_score(score.data_ptr(), _ptr(tie), n, order.data_ptr(), rank_of.data_ptr(), ws.data_ptr(),
+                                ws.numel(), _stream(stream)))
     return order, rank_of
+
+
+def sg_graph_in_degree(graph: Graph, stream=None) -> torch.Tensor:
+    """Device int32 [n_nodes] (uint32 contents): the in-degree of each node."""
+    deg = torch.empty(graph.n_nodes, dtype=torch.int32, device="cuda")
+    _check(load().sg_graph_in_degree(graph.handle, deg.data_ptr(), _stream(stream)))
+    return deg
 
 
 def sg_relabel(ids: torch.Tensor, prefix: torch.Tensor, stream=None):

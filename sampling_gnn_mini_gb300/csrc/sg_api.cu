@@ -138,6 +138,18 @@ __global__ void k_cache_check_distinct(const int32_t* ranked, int64_t n_cache, c
     }
 }
 
+// Reads one 16-byte vector of every 64 KB of the host table (its base
+// pages), so that the device's first-touch translation work for the table
+// happens here, once, and not inside the first gathers.
+__global__ void k_host_touch(const uint4* __restrict__ host, int64_t n_pages, int64_t page_vecs, unsigned* sink) {
+    uint32_t acc = 0;
+    for (int64_t p = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; p < n_pages; p += (int64_t)gridDim.x * blockDim.x) {
+        const uint4 v = __ldcs(host + p * page_vecs);
+        acc ^= v.x ^ v.y ^ v.z ^ v.w;
+    }
+    if (acc == 0x9E3779B9u) atomicXor(sink, acc);  // keeps the loads live; almost never taken
+}
+
 // Streams bytes with 16-byte loads and folds them into one word (read probe).
 __global__ void k_read_probe(const uint4* __restrict__ src, int64_t nvec, uint32_t* sink) {
     uint32_t acc = 0;
@@ -354,7 +366,7 @@ extern "C" sg_status sg_cache_build(const void* h_feat, const void* d_feat, int3
     cudaError_t e = h_ranked ? dev_alloc((void**)&c->slot_of, (size_t)n_nodes * sizeof(int32_t)) : cudaSuccess;
     if (e == cudaSuccess && n_cache > 0) e = dev_alloc(&c->rows, (size_t)n_cache * (size_t)row_bytes);
     if (e == cudaSuccess && h_ranked && n_cache > 0) e = dev_alloc((void**)&d_ranked, (size_t)n_cache * sizeof(int32_t));
-    if (e == cudaSuccess) e = dev_alloc((void**)&d_bad, sizeof(unsigned));
+    if (e == cudaSuccess) e = dev_alloc((void**)&d_bad, 2 * sizeof(unsigned));  // flag, touch sink
     if (e == cudaSuccess) e = cudaMemsetAsync(d_bad, 0, sizeof(unsigned), s);
     if (e == cudaSuccess && c->slot_of) e = cudaMemsetAsync(c->slot_of, 0xFF, (size_t)n_nodes * sizeof(int32_t), s);
     if (e == cudaSuccess && d_ranked)
@@ -368,6 +380,12 @@ extern "C" sg_status sg_cache_build(const void* h_feat, const void* d_feat, int3
             k_cache_check_distinct<<<blocks, 256, 0, s>>>(d_ranked, n_cache, c->slot_of, d_bad);
             e = cudaGetLastError();
         }
+    }
+    if (e == cudaSuccess && host_dev && n_cache < n_nodes) {
+        const int64_t table_bytes = n_nodes * row_bytes, page = 64 << 10;
+        k_host_touch<<<num_sms() * 8, 256, 0, s>>>((const uint4*)host_dev, table_bytes / page, page / 16,
+                                                   d_bad + 1);
+        e = cudaGetLastError();
     }
     unsigned bad = 0;
     if (e == cudaSuccess) e = cudaMemcpyAsync(&bad, d_bad, sizeof(unsigned), cudaMemcpyDeviceToHost, s);

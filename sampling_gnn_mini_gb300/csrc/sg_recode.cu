@@ -81,10 +81,21 @@ __global__ void __launch_bounds__(kNT) k_access_stats(StatsArgs a) {
     }
 }
 
+// in-degree: deg[u] += 1 for every CSR position naming u
+__global__ void k_in_degree(const int32_t* __restrict__ indices, int64_t m, int64_t n, uint32_t* __restrict__ deg) {
+    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < m; e += (int64_t)gridDim.x * blockDim.x) {
+        const int32_t u = indices[e];
+        if (u >= 0 && (int64_t)u < n) atomicAdd(deg + u, 1u);
+        else dev_err(ERR_INDEX);
+    }
+}
+
 // ------------------------------------------------------------ radix sort
-// Digit histogram of block b's tile.  Pass 0 reads the keys as ~score[i].
+// Digit histogram of block b's tile.  A first pass reads the keys as
+// ~score[v] with v = init[i] (or i without an initial order).
 __global__ void __launch_bounds__(kNT) k_radix_hist(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ score,
-                                                    int64_t n, int shift, uint32_t* __restrict__ hist, int64_t nb) {
+                                                    const int32_t* __restrict__ init, int64_t n, int shift,
+                                                    uint32_t* __restrict__ hist, int64_t nb) {
     __shared__ uint32_t h[kDigits];
     h[threadIdx.x] = 0;
     __syncthreads();
@@ -93,7 +104,7 @@ __global__ void __launch_bounds__(kNT) k_radix_hist(const uint32_t* __restrict__
     for (int r = 0; r < kItems; ++r) {
         const int64_t i = i0 + r * kNT + threadIdx.x;
         if (i < n) {
-            const uint32_t key = score ? ~score[i] : keys[i];
+            const uint32_t key = score ? ~score[init ? init[i] : i] : keys[i];
             atomicAdd(&h[(key >> shift) & 0xFF], 1u);
         }
     }
@@ -121,8 +132,8 @@ __global__ void __launch_bounds__(kNT) k_radix_scatter(const uint32_t* __restric
         uint32_t key = 0;
         int32_t val = 0;
         if (valid) {
-            key = score ? ~score[i] : keys_in[i];
             val = vals_in ? vals_in[i] : (int32_t)i;
+            key = score ? ~score[val] : keys_in[i];
         }
         const uint32_t d = valid ? (key >> shift) & 0xFF : 0x100u + (uint32_t)lane;  // invalid lanes match none
 #pragma unroll
@@ -238,7 +249,7 @@ sg_status scan_excl(const T* in, T* out, int64_t n, T* total, void* scratch, cud
 
 struct RankLayout {
     int64_t nb;
-    size_t keys0, keys1, vals, hist, scan, total;
+    size_t keys0, keys1, vals, order1, hist, scan, total;
 };
 
 RankLayout rank_layout(int64_t n) {
@@ -250,6 +261,8 @@ RankLayout rank_layout(int64_t n) {
     L.keys1 = o;
     o += a256((size_t)n * 4);
     L.vals = o;
+    o += a256((size_t)n * 4);
+    L.order1 = o;  // the order by the tie key, when there is one
     o += a256((size_t)n * 4);
     L.hist = o;
     o += a256((size_t)kDigits * L.nb * 4);
@@ -367,47 +380,77 @@ extern "C" size_t sg_rank_workspace(int64_t n_nodes) {
 namespace sgi {
 size_t rank_ws_bytes(int64_t n) { return rank_layout(n).total; }
 
-sg_status rank_scores(const uint32_t* d_score, int64_t n_nodes, int32_t* d_order, void* d_workspace, cudaStream_t s) {
-    const RankLayout L = rank_layout(n_nodes);
-    char* ws = (char*)d_workspace;
+// Four LSD passes of 8 bits over the complemented keys of `score` (ascending
+// key = descending score), stable, starting from the order `init` (or the
+// IDs); the values end in d_order.  Pass 0 gathers the keys through the
+// values and writes keys0 / tmp, pass 1 keys1 / order, pass 2 keys0 / tmp,
+// pass 3 the values alone into order.
+sg_status radix_by(const uint32_t* score, const int32_t* init, int64_t n_nodes, int32_t* d_order, char* ws,
+                   const RankLayout& L, cudaStream_t s) {
     uint32_t* keys[2] = {(uint32_t*)(ws + L.keys0), (uint32_t*)(ws + L.keys1)};
     int32_t* vals[2] = {(int32_t*)(ws + L.vals), d_order};
     uint32_t* hist = (uint32_t*)(ws + L.hist);
-    // four passes of 8 bits over the complemented scores (ascending key =
-    // descending score); LSD passes are stable, so ties keep the initial
-    // ascending-ID order.  Pass 0 reads the scores (values: the IDs) and
-    // writes keys0 / tmp, pass 1 keys1 / order, pass 2 keys0 / tmp, and
-    // pass 3 the values alone into order.
     for (int p = 0; p < 4; ++p) {
         const int shift = 8 * p;
         const uint32_t* kin = p == 0 ? nullptr : keys[(p + 1) & 1];
-        const int32_t* vin = p == 0 ? nullptr : vals[(p + 1) & 1];
+        const int32_t* vin = p == 0 ? init : vals[(p + 1) & 1];
         uint32_t* kout = p == 3 ? nullptr : keys[p & 1];
         int32_t* vout = vals[p & 1];
-        k_radix_hist<<<(unsigned)L.nb, kNT, 0, s>>>(kin, p == 0 ? d_score : nullptr, n_nodes, shift, hist, L.nb);
+        k_radix_hist<<<(unsigned)L.nb, kNT, 0, s>>>(kin, p == 0 ? score : nullptr, p == 0 ? init : nullptr, n_nodes,
+                                                    shift, hist, L.nb);
         sg_status st = scan_excl<uint32_t>(hist, hist, (int64_t)kDigits * L.nb, (uint32_t*)nullptr, ws + L.scan, s);
         if (st != SG_OK) return st;
-        k_radix_scatter<<<(unsigned)L.nb, kNT, 0, s>>>(kin, p == 0 ? d_score : nullptr, vin, n_nodes, shift, hist,
+        k_radix_scatter<<<(unsigned)L.nb, kNT, 0, s>>>(kin, p == 0 ? score : nullptr, vin, n_nodes, shift, hist,
                                                        L.nb, kout, vout);
         SG_CHECK_LAUNCH("k_radix_scatter");
     }
     return SG_OK;
 }
+
+// Nodes by descending score, then descending tie key (when given), then
+// ascending ID: a stable sort by the tie key, then a stable sort of that
+// order by the score.
+sg_status rank_scores2(const uint32_t* d_score, const uint32_t* d_tie, int64_t n_nodes, int32_t* d_order,
+                       void* d_workspace, cudaStream_t s) {
+    const RankLayout L = rank_layout(n_nodes);
+    char* ws = (char*)d_workspace;
+    if (!d_tie) return radix_by(d_score, nullptr, n_nodes, d_order, ws, L, s);
+    int32_t* first = (int32_t*)(ws + L.order1);
+    sg_status st = radix_by(d_tie, nullptr, n_nodes, first, ws, L, s);
+    if (st != SG_OK) return st;
+    return radix_by(d_score, first, n_nodes, d_order, ws, L, s);
+}
+
+sg_status rank_scores(const uint32_t* d_score, int64_t n_nodes, int32_t* d_order, void* d_workspace, cudaStream_t s) {
+    return rank_scores2(d_score, nullptr, n_nodes, d_order, d_workspace, s);
+}
 }  // namespace sgi
 
-extern "C" sg_status sg_rank_by_score(const uint32_t* d_score, int64_t n_nodes, int32_t* d_order, int32_t* d_rank_of,
-                                      void* d_workspace, size_t workspace_bytes, sg_stream_t stream) {
+extern "C" sg_status sg_rank_by_score(const uint32_t* d_score, const uint32_t* d_tie, int64_t n_nodes, int32_t* d_order,
+                                      int32_t* d_rank_of, void* d_workspace, size_t workspace_bytes,
+                                      sg_stream_t stream) {
     if (n_nodes <= 0 || n_nodes > 2147483647LL) return fail(SG_ERR_INVALID_ARG, "sg_rank_by_score: n_nodes out of range");
     if (!d_score || !d_order || !d_workspace) return fail(SG_ERR_INVALID_ARG, "sg_rank_by_score: NULL argument");
     const size_t need = rank_ws_bytes(n_nodes);
     if (workspace_bytes < need || ((uintptr_t)d_workspace) % 256)
         return fail(SG_ERR_INVALID_ARG, "sg_rank_by_score: workspace needs %zu bytes, 256-byte aligned", need);
     cudaStream_t s = (cudaStream_t)stream;
-    sg_status st = rank_scores(d_score, n_nodes, d_order, d_workspace, s);
+    sg_status st = rank_scores2(d_score, d_tie, n_nodes, d_order, d_workspace, s);
     if (st != SG_OK) return st;
     if (d_rank_of) {
         k_rank_scatter<<<num_sms() * 8, kNT, 0, s>>>(d_order, n_nodes, d_rank_of);
         SG_CHECK_LAUNCH("k_rank_scatter");
+    }
+    return SG_OK;
+}
+
+extern "C" sg_status sg_graph_in_degree(const sg_graph* g, uint32_t* d_deg, sg_stream_t stream) {
+    if (!g || !d_deg) return fail(SG_ERR_INVALID_ARG, "sg_graph_in_degree: NULL argument");
+    cudaStream_t s = (cudaStream_t)stream;
+    SG_CUDA(cudaMemsetAsync(d_deg, 0, (size_t)g->n_nodes * sizeof(uint32_t), s));
+    if (g->n_edges > 0) {
+        k_in_degree<<<num_sms() * 8, kNT, 0, s>>>(g->indices, g->n_edges, g->n_nodes, d_deg);
+        SG_CHECK_LAUNCH("k_in_degree");
     }
     return SG_OK;
 }

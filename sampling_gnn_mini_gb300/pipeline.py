@@ -31,12 +31,14 @@ from . import binding as sg
 
 
 def rank_by_access(graph: sg.Graph, batches: Iterable[Tuple[torch.Tensor, int]], fanouts: Sequence[int],
-                   omega: Sequence[int], w_in: int = 1, device="cuda"):
+                   omega: Sequence[int], w_in: int = 1, device="cuda", tie_by_in_degree: bool = True):
     """Presampling statistics and ranking (GARDEN page, Section IV-B): each
     (seeds, hash seed) batch is sampled and its full-link access statistics
     (Eq. (4), weights omega per layer and w_in for input nodes) are added to a
     per-node score on the device; returns (order, rank_of), nodes by
-    descending score.  All sizes of a batch must be equal."""
+    descending score, equal scores (among them every node the presampled
+    batches never reached) by descending in-degree, then by ID.  All sizes of
+    a batch must be equal."""
     score = torch.zeros(graph.n_nodes, dtype=torch.int32, device=device)
     buf, n_seeds = None, None
     for seeds, hseed in batches:
@@ -48,15 +50,17 @@ def rank_by_access(graph: sg.Graph, batches: Iterable[Tuple[torch.Tensor, int]],
             raise ValueError("rank_by_access: every presampled batch must have %d seeds" % n_seeds)
         sg.sg_sampler_run(graph, seeds, fanouts, hseed, buf)
         sg.sg_access_stats(buf, omega, w_in, score)
-    return sg.sg_rank_by_score(score)
+    tie = sg.sg_graph_in_degree(graph) if tie_by_in_degree else None
+    return sg.sg_rank_by_score(score, tie)
 
 
-def recode_by_access(graph: sg.Graph, batches, fanouts, omega, w_in: int = 1, device="cuda"):
+def recode_by_access(graph: sg.Graph, batches, fanouts, omega, w_in: int = 1, device="cuda",
+                     tie_by_in_degree: bool = True):
     """rank_by_access, then the graph recoded so that the node of rank r has
     ID r (Section IV-A): returns (new graph, order, rank_of).  The feature
     table must then be laid out in the new order (new row r = old row
     order[r]) for an ID-range cache, and seeds mapped through rank_of."""
-    order, rank_of = rank_by_access(graph, batches, fanouts, omega, w_in, device)
+    order, rank_of = rank_by_access(graph, batches, fanouts, omega, w_in, device, tie_by_in_degree)
     return sg.sg_graph_renumber(graph, order, rank_of), order, rank_of
 
 

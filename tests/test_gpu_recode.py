@@ -72,15 +72,29 @@ def test_access_stats_super_batch():
 
 
 @pytest.mark.parametrize("n,hi", [(1, 5), (4095, 3), (4097, 1 << 20), (100_000, 7), (1_000_003, 1 << 31)])
-def test_rank_by_score_matches_oracle(n, hi):
+@pytest.mark.parametrize("with_tie", [False, True])
+def test_rank_by_score_matches_oracle(n, hi, with_tie):
     rng = np.random.default_rng(n)
     score = rng.integers(0, hi, size=n, dtype=np.uint64).astype(np.uint32)
     score[: n // 7] = score[0]  # a long run of ties
-    order, rank_of = sg.sg_rank_by_score(torch.from_numpy(score.view(np.int32)).cuda())
+    tie = rng.integers(0, 1 << 32, size=n, dtype=np.uint64).astype(np.uint32) if with_tie else None
+    if with_tie:
+        tie[n // 3: n // 2] = 5  # ties of both keys, decided by ID
+    order, rank_of = sg.sg_rank_by_score(torch.from_numpy(score.view(np.int32)).cuda(),
+                                         None if tie is None else torch.from_numpy(tie.view(np.int32)).cuda())
     sg.sg_stream_check()
-    w_order, w_rank = oracle.rank_by_score(score)
+    w_order, w_rank = oracle.rank_by_score(score, tie)
     assert np.array_equal(order.cpu().numpy(), w_order)
     assert np.array_equal(rank_of.cpu().numpy(), w_rank)
+
+
+@pytest.mark.parametrize("offset_bits", [32, 64])
+def test_in_degree_matches_oracle(offset_bits):
+    g = synth.chung_lu(40000, 12.0, 2.0, 3000.0, 12)
+    G = sg.sg_graph_load(g.indptr if offset_bits == 64 else g.indptr.astype(np.int32), g.indices, offset_bits)
+    deg = sg.sg_graph_in_degree(G)
+    sg.sg_stream_check()
+    assert np.array_equal(deg.cpu().numpy().view(np.uint32), oracle.in_degree(g.indices, g.n))
 
 
 @pytest.mark.parametrize("offset_bits", [32, 64])
@@ -157,10 +171,12 @@ def test_recoded_pipeline_matches_oracle():
     for b in range(8):
         sg.sg_sampler_run(G, dev_i32(synth.batch_seeds(n, 1.0, b, B, 0, 1000)), fan, 5000 + b, buf)
         sg.sg_access_stats(buf, [1, 1, 1], 1, score)
-    order, rank_of = sg.sg_rank_by_score(score)
+    order, rank_of = sg.sg_rank_by_score(score, sg.sg_graph_in_degree(G))
     G2 = sg.sg_graph_renumber(G, order, rank_of)
     sg.sg_stream_check()
     order_h, rank_h = order.cpu().numpy(), rank_of.cpu().numpy()
+    want_order, _ = oracle.rank_by_score(score.cpu().numpy().view(np.uint32), oracle.in_degree(g.indices, n))
+    assert np.array_equal(order_h, want_order)
     ip2, ix2 = oracle.graph_renumber(g.indptr, g.indices, order_h, rank_h)
     feat = synth.features(n, dim, "f32", 0)[order_h]  # new row r = old row order[r]
     host = torch.from_numpy(np.ascontiguousarray(feat)).pin_memory()
