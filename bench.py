@@ -249,12 +249,12 @@ def frontier_ids(counts, unique, H: int, n_sub: int, h: int) -> np.ndarray:
     return np.unique(np.concatenate(parts))
 
 
-def kernels_per_step(H: int, n_sub: int, by_region: bool = False) -> int:
+def kernels_per_step(H: int, n_sub: int, by_region: bool = False, split: bool = True) -> int:
     """Kernels one step launches: sampler 3 per hop (+1 per hop for a
     super-batch) + 2, transposes 5, gather 1 a call (4 when misses are read
     grouped by host-table region) and 2 calls when one mini-batch of two hops
     or more is gathered in two parts, forward 1 per hop, backward 1 per hop."""
-    gathers = (2 if (n_sub == 1 and H >= 2) else 1) * (4 if by_region else 1)
+    gathers = (2 if (split and n_sub == 1 and H >= 2) else 1) * (4 if by_region else 1)
     return (2 + 3 * H + (H if n_sub > 1 else 0)) + 5 + gathers + H + H
 
 
@@ -421,7 +421,8 @@ def run_ours(args, rank, world, local):
     # i+1 is sampled and gathered while batch i's forward and backward run;
     # batch i+1's forward still waits for batch i's backward)
     depth = args.depth if args.depth > 0 else OverlappedPipeline.suggested_depth(cache)
-    ov = OverlappedPipeline(G, cache, w.fanouts, SB, depth=depth, batch_ptr=bptr, device=dev)
+    serial = OverlappedPipeline.suggested_serial_gathers(cache)
+    ov = OverlappedPipeline(G, cache, w.fanouts, SB, depth=depth, batch_ptr=bptr, device=dev, serial_gathers=serial)
     with torch.cuda.stream(stream):
         load_batch(0)
     for p in ov.pipes:
@@ -467,11 +468,14 @@ def run_ours(args, rank, world, local):
         ov.start_after(stream)
         marks = []
         for s_ in range(args.steps):
-            p = ov.step(inputs(first + s_), after(first + s_))
-            if ov.depth == 1:  # one batch at a time: an event per step gives its duration
-                e = torch.cuda.Event(enable_timing=True)
-                e.record(ov.streams[0])
-                marks.append(e)
+            k = ov.next_slot()
+            ov.step(inputs(first + s_), after(first + s_))
+            # an event when each step ends; batches end in order (each step's
+            # training waits for the previous one), so the gaps between them
+            # are the steps' durations in the steady state
+            e = torch.cuda.Event(enable_timing=True)
+            e.record(ov.streams[k])
+            marks.append(e)
         ov.wait_all(stream)
         b.record(stream)
         torch.cuda.synchronize(dev)
@@ -536,10 +540,14 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize(dev)
     sg.sg_stream_check(stream)
     hits, misses = [int(x) for x in pipe.stats.cpu().tolist()]
-    stage_ms = {name: 0.0 for name, _ in graphs}
+    stage_runs = {name: [] for name, _ in graphs}
     for s_ in range(args.steps):
         for j, (name, _) in enumerate(graphs):
-            stage_ms[name] += ev[s_][j].elapsed_time(ev[s_][j + 1]) / args.steps
+            stage_runs[name].append(ev[s_][j].elapsed_time(ev[s_][j + 1]))
+    # the median over the steps: a zero-copy stall of the host link in one
+    # step (seen on this host, independent of the kernels) does not move it
+    stage_ms = {name: float(np.median(v)) for name, v in stage_runs.items()}
+    stage_mean_ms = {name: float(np.mean(v)) for name, v in stage_runs.items()}
     counts = counts_log[args.warmup:].cpu().numpy()
     counts_all = counts.astype(np.int64)
     nodes = counts[:, : H + 1].astype(np.int64)
@@ -665,10 +673,12 @@ def run_ours(args, rank, world, local):
                    "l2": "inputs larger than L2 (CSR %.0f MB, features %.0f MB); a new batch every step"
                          % ((g.indptr.nbytes + g.indices.nbytes) / 1e6, w.n_nodes * R / 1e6)},
         "batch_latency_ms": latency_ms,
-        "overlap": ("%d pipelines in turn: batch i+1 is sampled, transposed and gathered while batch i's forward "
-                    "and backward run; batch i+1's forward waits for batch i's backward" % depth if depth > 1 else
-                    "none: one batch at a time, a step graph each (misses come from a host table read by region, "
-                    "which concurrent gathers would interleave)") +
+        "overlap": (("%d pipelines in turn, gathers one after another (misses come from a host table read by "
+                     "region, which concurrent gathers would interleave): batch i+1 is sampled and transposed while "
+                     "batch i gathers; batch i+1's forward waits for batch i's backward" % depth) if ov.serial_gathers
+                    else ("%d pipelines in turn: batch i+1 is sampled, transposed and gathered while batch i's forward "
+                          "and backward run; batch i+1's forward waits for batch i's backward" % depth) if depth > 1
+                    else "none: one batch at a time, a step graph each") +
                    ". batch_latency_ms is one batch alone (a step graph per batch, batches back to back)",
         "presample": presample,
         "recoded": W.rank_of is not None,
@@ -681,16 +691,18 @@ def run_ours(args, rank, world, local):
         "memory_roofline_frac": {k: v["frac"] for k, v in stage_roof.items()},
         "hit_rate": hits / max(1, hits + misses),
         "stage_ms": stage_ms,
-        "stage_note": "per-stage times from a third timed region replaying per-stage graphs in sequence, one "
-                      "batch at a time (the headline overlaps batches; within a batch the transposes overlap "
-                      "gather and forward)",
+        "stage_mean_ms": stage_mean_ms,
+        "stage_note": "per-stage times (median over the steps; stage_mean_ms: the means) from a third timed region "
+                      "replaying per-stage graphs in sequence, one batch at a time (the headline overlaps batches; "
+                      "within a batch the transposes overlap gather and forward)",
         "stages": stage_roof,
         "update_note": update_note,
         "roofline": roof,
         "host_link_gbs": link_gbs,
         "host_link": None if not link else dict(link, roofline=max(link, key=link.get)),
         "per_step": {"nodes": nodes.mean(axis=0).tolist(), "edges": edges.mean(axis=0).tolist()},
-        "gpu_launches": kernels_per_step(H, n_sub, pipe.gather_ws[0] is not None) * args.steps,
+        "gpu_launches": kernels_per_step(H, n_sub, pipe.gather_ws[0] is not None, ov.pipes[0].split_gather)
+                        * args.steps,
         "clocks": clk,
     }
     if rank == 0 and not args.no_e2e:
@@ -748,11 +760,12 @@ def measure_e2e(sg, torch, ov, seeds_host, hseeds, dev, args, H, w):
     seeds go host -> device from pinned memory and the step's result (the
     seed rows H_0 and the counts) comes back device -> host, with batches
     overlapped as in the headline (OverlappedPipeline, its CUDA graphs).  The
-    host reads step j's result after enqueuing step j + depth - 1: step j +
-    depth reuses step j's pipeline and could not start earlier anyway.  The
-    pinned result buffers form a ring of depth + 1 sets."""
+    host reads step j's result after enqueuing step j + depth, so the device
+    always has the next step queued (step j's result was copied out on its
+    pipeline's stream before that pipeline is reused).  The pinned result
+    buffers form a ring of depth + 2 sets."""
     B = ov.pipes[0].n_seeds
-    lag = ov.depth
+    lag = ov.depth + 1
     ring = lag + 1
     p0 = ov.pipes[0]
     h_seeds = torch.from_numpy(seeds_host).pin_memory()

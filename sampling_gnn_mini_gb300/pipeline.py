@@ -66,7 +66,8 @@ def recode_by_access(graph: sg.Graph, batches, fanouts, omega, w_in: int = 1, de
 
 class MiniBatchPipeline:
     def __init__(self, graph: sg.Graph, cache: sg.Cache, fanouts: Sequence[int], n_seeds: int,
-                 batch_ptr: Optional[Sequence[int]] = None, backward: bool = True, device="cuda"):
+                 batch_ptr: Optional[Sequence[int]] = None, backward: bool = True, device="cuda",
+                 split_gather: Optional[bool] = None):
         self.graph, self.cache = graph, cache
         self.fanouts = [int(f) for f in fanouts]
         self.H = len(self.fanouts)
@@ -97,7 +98,8 @@ class MiniBatchPipeline:
             self.ev_transposed = torch.cuda.Event()
         # split gather (one mini-batch, two hops or more): the rows of V_{H-1}
         # go first, on their own stream
-        self.split_gather = (self.batch_ptr is None or len(self.batch_ptr) == 2) and self.H >= 2
+        can_split = (self.batch_ptr is None or len(self.batch_ptr) == 2) and self.H >= 2
+        self.split_gather = can_split if split_gather is None else (bool(split_gather) and can_split)
         if self.split_gather:
             H = self.H
             self.gather_stream = torch.cuda.Stream(device=device)
@@ -176,6 +178,13 @@ class MiniBatchPipeline:
         backward pass.  With the split gather, V_{H-1}'s rows are gathered on a
         third stream during hop H."""
         main = torch.cuda.current_stream() if stream is None else stream
+        self.load_sample(main)
+        self.load_gather(main, join)
+
+    def load_sample(self, stream=None) -> None:
+        """The first part of load(): sampling (with the split gather's first
+        part on its own stream) and the transposes forked to a side stream."""
+        main = torch.cuda.current_stream() if stream is None else stream
         if self.split_gather:
             events = [None] * self.H
             events[self.H - 2] = self.ev_prefix
@@ -190,6 +199,11 @@ class MiniBatchPipeline:
             self.side.wait_event(self.ev_sampled)
             self.transpose(self.side)
             self.ev_transposed.record(self.side)
+
+    def load_gather(self, stream=None, join: bool = False) -> None:
+        """The second part of load(): the gather (the rest of it, with the
+        split gather); with join, the side streams are joined back."""
+        main = torch.cuda.current_stream() if stream is None else stream
         if self.split_gather:
             self.gather_rest(main)
             main.wait_event(self.ev_gathered)
@@ -236,25 +250,39 @@ class OverlappedPipeline:
     reaches them.  capture() records each pipeline's two parts as CUDA graphs
     (depth 1: the whole step as one graph), which step() then replays.
 
-    suggested_depth() picks the depth: 4, or 1 when misses are read from a
-    host table large enough that the gather reads them grouped by region
-    there, concurrent gathers of several batches interleave their regions and
-    lose that grouping (measured on the 61 GB Wide table: 3.6 ms a step with
-    four pipelines against 2.8 ms one batch at a time)."""
+    With serial_gathers (for host tables large enough that the gather reads
+    misses grouped by region), batches still overlap, but their gathers run
+    one after another: concurrent gathers of several batches would interleave
+    their regions and lose the grouping (measured on the 61 GB Wide table:
+    3.6 ms a step with four pipelines gathering at once against 2.8 ms one
+    batch at a time).  Each batch's gather is then a single call, after its
+    sampling, and batch i+1 is sampled and transposed while batch i gathers.
+
+    suggested_depth() picks the depth (4, or 2 with serial gathers when
+    misses are read by region) and suggested_serial_gathers() the mode."""
 
     @staticmethod
     def suggested_depth(cache: sg.Cache) -> int:
-        return 1 if sg.sg_gather_workspace(cache, 1) > 0 else 4
+        return 2 if sg.sg_gather_workspace(cache, 1) > 0 else 4
+
+    @staticmethod
+    def suggested_serial_gathers(cache: sg.Cache) -> bool:
+        return sg.sg_gather_workspace(cache, 1) > 0
 
     def __init__(self, graph: sg.Graph, cache: sg.Cache, fanouts: Sequence[int], n_seeds: int, depth: int = 2,
-                 batch_ptr: Optional[Sequence[int]] = None, backward: bool = True, device="cuda"):
+                 batch_ptr: Optional[Sequence[int]] = None, backward: bool = True, device="cuda",
+                 serial_gathers: bool = False):
         if depth < 1:
             raise ValueError("OverlappedPipeline: depth must be at least 1")
+        self.serial_gathers = bool(serial_gathers) and depth > 1
         self.pipes = [MiniBatchPipeline(graph, cache, fanouts, n_seeds, batch_ptr=batch_ptr, backward=backward,
-                                        device=device) for _ in range(depth)]
+                                        device=device, split_gather=False if self.serial_gathers else None)
+                      for _ in range(depth)]
         self.streams = [torch.cuda.Stream(device=device) for _ in range(depth)]
         self.ev_trained = torch.cuda.Event()
         self.ev_trained.record()  # nothing is training yet
+        self.ev_gathered = torch.cuda.Event()
+        self.ev_gathered.record()  # nothing is gathering yet
         self.graphs = None
         self.i = 0
 
@@ -284,9 +312,20 @@ class OverlappedPipeline:
                 p.load(s, join=True)
                 p.train(s, joined=True)
             s.synchronize()
-            gl, gt = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gl, stream=s):
-                p.load(s, join=True)
+            gt = torch.cuda.CUDAGraph()
+            if self.serial_gathers:  # sampling + transposes, and the gather, as two graphs
+                gs, gg = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gs, stream=s):
+                    p.load_sample(s)
+                    if p.backward:
+                        s.wait_event(p.ev_transposed)
+                with torch.cuda.graph(gg, stream=s):
+                    p.load_gather(s)
+                gl = (gs, gg)
+            else:
+                gl = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gl, stream=s):
+                    p.load(s, join=True)
             with torch.cuda.graph(gt, stream=s):
                 p.train(s, joined=True)
             graphs.append((gl, gt))
@@ -313,7 +352,22 @@ class OverlappedPipeline:
                     after(p, s)
                 self.i += 1
                 return p
-            if self.graphs is None:
+            if self.serial_gathers:
+                # this batch samples beside the previous batch's gather; its
+                # own gather waits for that one
+                if self.graphs is None:
+                    p.load_sample(s)
+                    if p.backward:
+                        s.wait_event(p.ev_transposed)
+                else:
+                    self.graphs[k][0][0].replay()
+                s.wait_event(self.ev_gathered)
+                if self.graphs is None:
+                    p.load_gather(s)
+                else:
+                    self.graphs[k][0][1].replay()
+                self.ev_gathered.record(s)
+            elif self.graphs is None:
                 p.load(s, join=True)
             else:
                 self.graphs[k][0].replay()

@@ -481,20 +481,24 @@ def test_pipeline_cuda_graph_replay_with_new_batches():
         _check_pipeline_against_oracle(pipe, w, g, feat, seeds, w.sampler_seed(b))
 
 
-@pytest.mark.parametrize("depth,graphs,n_sub", [(2, True, 1), (3, False, 1), (2, True, 3), (1, True, 1)])
-def test_overlapped_pipeline_matches_batches_run_alone(depth, graphs, n_sub):
+@pytest.mark.parametrize("depth,graphs,n_sub,serial", [(2, True, 1, False), (3, False, 1, False),
+                                                      (2, True, 3, False), (1, True, 1, False),
+                                                      (2, True, 1, True), (3, False, 1, True)])
+def test_overlapped_pipeline_matches_batches_run_alone(depth, graphs, n_sub, serial):
     # Batches (or super-batches of n_sub mini-batches) overlapped on `depth`
     # pipelines (sampling and gather of one batch during the forward and
-    # backward of the previous) give, batch by batch, the same counts, sample,
-    # H_0 and input gradient, bit for bit, as the same batches run one at a
-    # time.
+    # backward of the previous; with serial gathers, one batch sampled during
+    # the previous batch's gather, the gathers one after another) give, batch
+    # by batch, the same counts, sample, H_0 and input gradient, bit for bit,
+    # as the same batches run one at a time.
     w, g, feat, single, host = _tiny_pipeline()
     H = single.H
     n = w.batch * n_sub
     bptr = [w.batch * k for k in range(n_sub + 1)] if n_sub > 1 else None
     if n_sub > 1:
         single = MiniBatchPipeline(single.graph, single.cache, w.fanouts, n, batch_ptr=bptr)
-    ov = OverlappedPipeline(single.graph, single.cache, w.fanouts, n, depth=depth, batch_ptr=bptr)
+    ov = OverlappedPipeline(single.graph, single.cache, w.fanouts, n, depth=depth, batch_ptr=bptr,
+                            serial_gathers=serial)
     batches = list(range(10, 17)) if n_sub == 1 else list(range(7))  # all within one epoch of the mask
     seeds = {b: dev_i32(np.concatenate([synth.batch_seeds(g.n, w.p_mask, b * n_sub + k, w.batch)
                                         for k in range(n_sub)])) for b in batches}
