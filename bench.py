@@ -53,6 +53,14 @@ def parse():
                     help="keep the original node IDs and a slot-map cache of the ranked rows")
     ap.add_argument("--omega", default="", help="layer weights of the access statistics, comma-separated (default 1s)")
     ap.add_argument("--w-in", type=int, default=1, help="input-node weight of the access statistics")
+    ap.add_argument("--presample", type=int, default=0,
+                    help="presampled batches for the cache ranking (0: the workload's own count, 64)")
+    ap.add_argument("--experiment", default="", choices=["", "next"],
+                    help="next: measure the dynamic cache and Match-Reorder on the workload instead of the headline")
+    ap.add_argument("--dyn-frac", type=float, default=0.1, help="share of the cache budget given to the dynamic cache")
+    ap.add_argument("--dyn-gamma", type=float, default=0.9, help="decay per batch of the dynamic cache's scores")
+    ap.add_argument("--dyn-window", type=int, default=16, help="batches per dynamic-cache update")
+    ap.add_argument("--group", type=int, default=16, help="batches per Match-Reorder group (<= 32)")
     ap.add_argument("--min-seconds", type=float, default=2.0,
                     help="the timed region of --steps steps is repeated (new batches each time) until this long")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="bound on the CPU-baseline sample")
@@ -258,29 +266,21 @@ def kernels_per_step(H: int, n_sub: int, by_region: bool = False, split: bool = 
     return (2 + 3 * H + (H if n_sub > 1 else 0)) + 5 + gathers + H + H
 
 
-def run_ours(args, rank, world, local):
-    import torch
-    from sampling_gnn_mini_gb300 import binding as sg
-    from sampling_gnn_mini_gb300.pipeline import MiniBatchPipeline, OverlappedPipeline, rank_by_access
-
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-    sg.load(build_if_missing=True)
+def setup_workload(args, sg, torch, dev, cache_rows=None):
+    """Graph in HBM (recoded by presampled statistics when the cache holds
+    part of the table), host feature table and cache, as the headline uses
+    them.  Returns (W, G, cache, presample)."""
+    from sampling_gnn_mini_gb300.pipeline import rank_by_access
     w0 = synth.workload(args.config)
     recode = w0.cache_rows < w0.n_nodes and not args.no_recode
     W = Workload(args.config, pinned_features=True, recode=recode)
     w, g = W.w, W.g
     H = w.n_hops
-    R = w.row_bytes
-    hbm_peak, peak_kind = peaks()
     log("workload %s: graph %.1fs, feature table %.1fs" % (w.name, W.t_graph, W.t_feat))
 
     # graph into HBM; int64 offsets where the config calls for them
     G = sg.sg_graph_load(g.indptr if w.offset_bits == 64 else g.indptr.astype(np.int32), g.indices, w.offset_bits)
-    cache_rows = w.cache_rows
+    cache_rows = w.cache_rows if cache_rows is None else int(cache_rows)
     omega = [int(x) for x in args.omega.split(",")] if args.omega else [1] * H
     presample = None
     # rank nodes by their full-link access statistics (Eq. (4)) over presampled
@@ -288,12 +288,12 @@ def run_ours(args, rank, world, local):
     # graph so that the hot nodes hold the smallest IDs (ID-range cache)
     if cache_rows < w.n_nodes:
         t0 = time.time()
-        pre_batches = ((torch.from_numpy(W.presample.seeds(b)).to(dev), w.presample_seed(b))
-                       for b in range(w.presample_batches))
+        n_pre = args.presample if args.presample > 0 else w.presample_batches
+        pre_batches = ((torch.from_numpy(W.presample.seeds(b)).to(dev), w.presample_seed(b)) for b in range(n_pre))
         order, rank_of = rank_by_access(G, pre_batches, w.fanouts, omega, args.w_in, device=dev)
         torch.cuda.synchronize(dev)
         sg.sg_stream_check()
-        presample = {"batches": w.presample_batches, "omega": omega, "w_in": args.w_in,
+        presample = {"batches": n_pre, "omega": omega, "w_in": args.w_in,
                      "statistics_and_rank_s": time.time() - t0}
         if recode:
             t0 = time.time()
@@ -316,6 +316,26 @@ def run_ours(args, rank, world, local):
     cache = sg.sg_cache_build(W.feat if w.host_features else None,
                               None if w.host_features else W.feat.to(dev), dtype_code, w.n_nodes, w.dim,
                               ranked, cache_rows)
+    return W, G, cache, presample
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    from sampling_gnn_mini_gb300 import binding as sg
+    from sampling_gnn_mini_gb300.pipeline import MiniBatchPipeline, OverlappedPipeline
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    sg.load(build_if_missing=True)
+    W, G, cache, presample = setup_workload(args, sg, torch, dev)
+    w, g = W.w, W.g
+    H = w.n_hops
+    R = w.row_bytes
+    hbm_peak, peak_kind = peaks()
+    cache_rows = w.cache_rows
     # a step is one batch, or one super-batch of w.n_sub mini-batches that
     # share the hash seed (mini-batches b * n_sub .. b * n_sub + n_sub - 1)
     n_sub = w.n_sub
@@ -810,6 +830,150 @@ def measure_e2e(sg, torch, ov, seeds_host, hseeds, dev, args, H, w):
                     "after enqueuing step j + %d" % (ov.depth, lag - 1)}
 
 
+# ------------------------------------------------------ NEXT rows measured
+def run_next_experiments(args):
+    """The dynamic cache (GARDEN Eq. (5)-(6)) and Match-Reorder (FastGL) on
+    the workload, against the static cache the headline uses, with the same
+    HBM budget: one JSON line with "impl": "experiment" (not the headline).
+    Each gather is timed alone with CUDA events (median over the batches)."""
+    import torch
+    from sampling_gnn_mini_gb300 import binding as sg
+    from sampling_gnn_mini_gb300.pipeline import MiniBatchPipeline
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    sg.load(build_if_missing=True)
+    W, G, cache, presample = setup_workload(args, sg, torch, dev)
+    w = W.w
+    H = w.n_hops
+    if w.n_sub != 1 or w.cache_rows >= w.n_nodes:
+        return {"impl": "experiment", "config": w.name, "skipped": "needs one mini-batch a step and a host table"}
+    pipe = MiniBatchPipeline(G, cache, w.fanouts, w.batch, backward=False, device=dev, split_gather=False)
+    cap = pipe.bounds.max_nodes[H]
+    ws = sg.aligned_workspace(sg.sg_gather_workspace(cache, cap)) if sg.sg_gather_workspace(cache, cap) else None
+    dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    outs = [torch.empty((cap, w.dim), dtype=dt, device=dev) for _ in range(2)]
+
+    def timed(fn):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        b.synchronize()
+        return a.elapsed_time(b)
+
+    def sample(b):
+        pipe.set_batch(torch.from_numpy(W.seeds(b)).to(dev), w.sampler_seed(b))
+        pipe.sample()
+        n = int(pipe.counts[H].item())
+        return pipe.buf.unique[:n].clone()
+
+    # ---- Match-Reorder over groups of batches
+    Gn = min(max(args.group, 2), 32)
+    groups = max(1, args.steps // Gn)
+    match_map = torch.full((w.n_nodes,), -1, dtype=torch.int32, device=dev)
+    mask = torch.zeros(w.n_nodes, dtype=torch.int32, device=dev)
+    pos = torch.empty(cap, dtype=torch.int32, device=dev)
+    stats = torch.zeros(2, dtype=torch.int64, device=dev)
+    reused = torch.zeros(1, dtype=torch.int64, device=dev)
+    mr = {"natural": {"overlap": [], "ms": [], "reused": 0, "misses": 0, "rows": 0},
+          "greedy": {"overlap": [], "ms": [], "reused": 0, "misses": 0, "rows": 0},
+          "plain": {"ms": [], "misses": 0, "rows": 0}}
+    t_overlap = []
+    for gi in range(groups):
+        lists = [sample(gi * Gn + k) for k in range(Gn)]
+        off = np.concatenate([[0], np.cumsum([x.numel() for x in lists])])
+        ids = torch.cat(lists)
+        O = None
+
+        def ov():
+            nonlocal O
+            O = sg.sg_overlap(ids, off, mask)
+        t_overlap.append(timed(ov))
+        Oh = O.cpu().numpy()
+        order = sg.sg_greedy_order(Oh, 0)
+        for name, seq in (("natural", list(range(Gn))), ("greedy", list(order))):
+            for k in range(1, Gn):
+                mr[name]["overlap"].append(Oh[seq[k - 1], seq[k]] / Oh[seq[k], seq[k]])
+            prev = None
+            for k, b in enumerate(seq):
+                cur, out = lists[b], outs[k % 2]
+                stats.zero_()
+                reused.zero_()
+                if prev is None:
+                    sg.sg_gather(cache, cur, cur.numel(), None, out, stats, workspace=ws)
+                else:
+                    def f():
+                        sg.sg_match(lists[prev], lists[prev].numel(), None, cur, cur.numel(), None, match_map, pos)
+                        sg.sg_gather_reuse(cache, cur, cur.numel(), None, pos, outs[(k - 1) % 2], out, stats, reused,
+                                           workspace=ws)
+                    mr[name]["ms"].append(timed(f))
+                    h, m = stats.cpu().tolist()
+                    mr[name]["reused"] += int(reused.item())
+                    mr[name]["misses"] += m
+                    mr[name]["rows"] += cur.numel()
+                prev = b
+        for b in range(1, Gn):  # the same batches without reuse
+            stats.zero_()
+            mr["plain"]["ms"].append(timed(lambda: sg.sg_gather(cache, lists[b], lists[b].numel(), None, outs[0],
+                                                               stats, workspace=ws)))
+            mr["plain"]["misses"] += int(stats[1].item())
+            mr["plain"]["rows"] += lists[b].numel()
+        del lists, ids
+    sg.sg_stream_check()
+    match_reorder = {"group": Gn, "groups": groups, "overlap_ms_median": float(np.median(t_overlap))}
+    for name in ("natural", "greedy"):
+        d = mr[name]
+        match_reorder[name] = {"mean_overlap_with_previous": float(np.mean(d["overlap"])),
+                               "reused_row_share": d["reused"] / max(1, d["rows"]),
+                               "host_misses_a_batch": d["misses"] / max(1, len(d["ms"])),
+                               "match_plus_gather_ms_median": float(np.median(d["ms"]))}
+    match_reorder["no_reuse"] = {"host_misses_a_batch": mr["plain"]["misses"] / max(1, len(mr["plain"]["ms"])),
+                                 "gather_ms_median": float(np.median(mr["plain"]["ms"]))}
+
+    # ---- dynamic cache: static C - K plus dynamic K against static C
+    C = w.cache_rows
+    K = max(1, int(args.dyn_frac * C))
+    g_q16 = max(1, min(65536, int(round(args.dyn_gamma * 65536))))
+    dtype_code = sg.SG_F32 if w.dtype == "f32" else sg.SG_BF16
+    cache2 = sg.sg_cache_build(W.feat, None, dtype_code, w.n_nodes, w.dim, None, C - K)
+    sg.sg_dyn_cache_create(cache2, K, g_q16, args.dyn_window)
+    ws2 = sg.aligned_workspace(sg.sg_gather_workspace(cache2, cap)) if ws is not None else None
+    n_b = max(args.dyn_window * 4, args.steps)
+    rows_s = {"static": [], "dynamic": []}
+    ms_s = {"static": [], "dynamic": []}
+    upd_ms = []
+    base = 100000  # batches after the Match-Reorder ones
+    for b in range(n_b):
+        cur = sample(base + b)
+        for name, c, wsx in (("static", cache, ws), ("dynamic", cache2, ws2)):
+            stats.zero_()
+            ms = timed(lambda: sg.sg_gather(c, cur, cur.numel(), None, outs[0], stats, workspace=wsx))
+            h, m = stats.cpu().tolist()
+            rows_s[name].append((h, m))
+            ms_s[name].append(ms)
+        t = timed(lambda: sg.sg_dyn_cache_batch(cache2, cur, cur.numel(), None))
+        if (b + 1) % args.dyn_window == 0:
+            upd_ms.append(t)
+    sg.sg_stream_check()
+    half = n_b // 2  # after the first windows have filled the dynamic set
+
+    def rate(v):
+        h = sum(x[0] for x in v[half:])
+        m = sum(x[1] for x in v[half:])
+        return h / max(1, h + m)
+    dyn = {"budget_rows": C, "dynamic_rows": K, "gamma": g_q16 / 65536.0, "window": args.dyn_window,
+           "batches": n_b, "hit_rate_static_only": rate(rows_s["static"]),
+           "hit_rate_static_plus_dynamic": rate(rows_s["dynamic"]),
+           "gather_ms_median_static_only": float(np.median(ms_s["static"][half:])),
+           "gather_ms_median_static_plus_dynamic": float(np.median(ms_s["dynamic"][half:])),
+           "window_update_ms_median": float(np.median(upd_ms)) if upd_ms else None,
+           "note": "rates and times over the second half of the batches; the window update (Eq. (5) fold, Top-K of "
+                   "Eq. (6) by a radix ranking of every node, admission of entering rows) runs once a window"}
+    return {"impl": "experiment", "config": w.name, "match_reorder": match_reorder, "dynamic_cache": dyn,
+            "presample": presample}
+
+
 # -------------------------------------------------------------- CPU baseline
 def run_oracle_steps(W, batches, budget_s):
     """The oracle's whole step (sample+relabel, gather, forward and backward
@@ -876,6 +1040,10 @@ def run_reference(args, rank, world):
 def main():
     args = parse()
     rank, world, local = dist_env()
+    if args.experiment == "next":
+        if rank == 0:
+            print(json.dumps(run_next_experiments(args)), flush=True)
+        return
     if args.impl == "reference":
         res = run_reference(args, rank, world)
         if res is not None:

@@ -169,15 +169,25 @@ __device__ __forceinline__ void gather_range(const int32_t* d_n, const int32_t* 
 }
 
 // Exclusive scan of the n_regions miss counts in place (one block); the
-// total goes to cnt[n_regions].  Each thread scans a contiguous run.
+// total goes to cnt[n_regions].  The counts are staged through shared memory
+// with coalesced loads and stores (kScanSmemMax of them at most); each thread
+// then scans a contiguous run of the staged copy.
 constexpr int kScanThreads = 1024;
+constexpr int64_t kScanSmemMax = 54 * 1024;  // counts staged in shared memory (216 KB)
 __global__ void __launch_bounds__(kScanThreads) k_region_scan(uint32_t* __restrict__ cnt, int64_t n_regions) {
     pdl_start();
+    extern __shared__ uint32_t staged[];
     __shared__ uint32_t sh[kScanThreads];
+    const bool smem = n_regions <= kScanSmemMax;
+    uint32_t* src = smem ? staged : cnt;
+    if (smem) {
+        for (int64_t r = threadIdx.x; r < n_regions; r += kScanThreads) staged[r] = cnt[r];
+        __syncthreads();
+    }
     const int64_t per = (n_regions + kScanThreads - 1) / kScanThreads;
     const int64_t a = min((int64_t)threadIdx.x * per, n_regions), b = min(a + per, n_regions);
     uint32_t sum = 0;
-    for (int64_t r = a; r < b; ++r) sum += cnt[r];
+    for (int64_t r = a; r < b; ++r) sum += src[r];
     sh[threadIdx.x] = sum;
     __syncthreads();
     for (int d = 1; d < kScanThreads; d <<= 1) {  // inclusive scan of the run totals
@@ -188,11 +198,15 @@ __global__ void __launch_bounds__(kScanThreads) k_region_scan(uint32_t* __restri
     }
     uint32_t run = sh[threadIdx.x] - sum;
     for (int64_t r = a; r < b; ++r) {
-        const uint32_t k = cnt[r];
-        cnt[r] = run;
+        const uint32_t k = src[r];
+        src[r] = run;
         run += k;
     }
     if (threadIdx.x == kScanThreads - 1) cnt[n_regions] = sh[kScanThreads - 1];
+    if (smem) {
+        __syncthreads();
+        for (int64_t r = threadIdx.x; r < n_regions; r += kScanThreads) cnt[r] = staged[r];
+    }
 }
 
 // Lists the missed rows i in [first, n) by region: list[pos] = i, pos taken
@@ -310,7 +324,18 @@ sg_status gather_impl(const sg_cache* c, const int32_t* d_ids, int64_t n_cap, co
                        (int32_t)row_vecs, stride / row_vecs, (int32_t)(stride % row_vecs), (uint4*)d_out, d_stats,
                        cnt, c->region_shift, dyn, reuse));
     if (!by_region) return SG_OK;
-    SG_CUDA(launch_pdl(k_region_scan, dim3(1), dim3(kScanThreads), 0, s, cnt, c->n_regions));
+    const size_t scan_smem = c->n_regions <= kScanSmemMax ? (size_t)c->n_regions * sizeof(uint32_t) : 0;
+    if (scan_smem > 48 * 1024) {
+        static bool attr_set[64] = {false};  // per device
+        int dev = 0;
+        SG_CUDA(cudaGetDevice(&dev));
+        if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+            SG_CUDA(cudaFuncSetAttribute(k_region_scan, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(kScanSmemMax * sizeof(uint32_t))));
+            attr_set[dev] = true;
+        }
+    }
+    SG_CUDA(launch_pdl(k_region_scan, dim3(1), dim3(kScanThreads), scan_smem, s, cnt, c->n_regions));
     int64_t sblocks = cdiv(n_cap, (int64_t)kThreads);
     if (sblocks > cap) sblocks = cap;
     SG_CUDA(launch_pdl(k_region_scatter, dim3((unsigned)sblocks), dim3(kThreads), 0, s, d_ids, d_n, d_first, n_cap,
