@@ -38,8 +38,8 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kUnroll = 8;
-constexpr int kListUnroll = 16;     // loads in flight a thread of k_gather_list
-constexpr int kListBlocksPerSm = 1;
+constexpr int kListUnroll = 8;      // loads in flight a thread of k_gather_list
+constexpr int kListBlocksPerSm = 8;
 
 // cache slot of node g, or -1 when it is read from the host table
 __device__ __forceinline__ int64_t slot_for(const int32_t* __restrict__ slot_of, int64_t n_cache, int32_t g) {
@@ -235,15 +235,13 @@ __global__ void __launch_bounds__(kThreads) k_region_scatter(const int32_t* __re
 }
 
 // Copies the listed rows from the host table, flattened over (entry,
-// vector) with kListUnroll loads in flight a thread, in list order.  The
-// launch is one block an SM: the list is in address order, and a narrower
-// window of rows in flight lets neighbouring rows share address
-// translations.  Measured on GB300 for region-sorted misses spread over a
-// 45 GB span of a registered huge-page table, 512-byte rows: 16 loads and 1
-// or 2 blocks an SM read at ~200 GB/s (the link's rate), 8 loads and 8
-// blocks an SM at ~65 GB/s; 2 KB rows behave alike (~207 GB/s).  One block
-// an SM leaves half of each SM's registers to kernels of another batch that
-// run beside the gather (the sampler of the next batch).
+// vector) with kListUnroll loads in flight a thread, in list order, at full
+// occupancy (eight blocks an SM).  Reads of rows not read before are bound by
+// address translation, and more requests in flight help: in the benchmark on
+// the 57 GB Billion-edge table (CUDA events, each gather reading new rows),
+// 8 loads x 8 blocks an SM gave 1.37 ms a step at the median against 1.38
+// (16 x 4), 1.39 (8 x 4) and 1.53 (16 x 1).  (Re-reading rows just read runs
+// several times faster; such repeated reads are not what a batch does.)
 __global__ void __launch_bounds__(kThreads, kListBlocksPerSm) k_gather_list(const int32_t* __restrict__ list,
                                                           const uint32_t* __restrict__ total,
                                                           const int32_t* __restrict__ ids,
