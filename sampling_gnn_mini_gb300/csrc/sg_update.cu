@@ -34,7 +34,7 @@ constexpr int kThreads = 128;          // 4 warps
 constexpr int kBM = 128;               // rows of a tile
 constexpr int kBN = 128;               // outputs (the hidden width)
 constexpr int kTileBytes = 128;        // K bytes of a stage (one 128-byte swizzle row)
-constexpr int kStages = 4;
+constexpr int kStages = 3;            // 96 KB of ring: two CTAs an SM (their epilogues overlap the other's loads)
 constexpr int kStageA = kBM * kTileBytes;  // 16 KB
 constexpr int kStageB = kBN * kTileBytes;  // 16 KB
 constexpr int kSmemTiles = kStages * (kStageA + kStageB);
@@ -146,7 +146,7 @@ struct UpdateMaps {
 };
 
 template <bool TF32>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     k_sage_fwd(const __grid_constant__ UpdateMaps maps, int32_t n_cap, const int32_t* __restrict__ d_n, int32_t kt_half,
                float* __restrict__ out, float* __restrict__ y) {
     extern __shared__ uint8_t dsm[];
@@ -266,7 +266,7 @@ struct GemmMaps {
 };
 
 template <bool TF32, int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     k_sage_gemm(const __grid_constant__ GemmMaps maps, int32_t m_cap, const int32_t* __restrict__ d_m_rows,
                 int32_t k_cap, const int32_t* __restrict__ d_k, int32_t n_cols, int32_t split_col, float* __restrict__ o0,
                 float* __restrict__ o1, int32_t ld1) {
