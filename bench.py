@@ -135,6 +135,28 @@ def sampler_traffic():
     return traffic if want == have else None
 
 
+def gather_traffic(hits: float, misses: float):
+    """DRAM bytes of the gather stage for the given hits and misses, scaled by
+    units from the committed ncu summary when the gather source is the one
+    that was profiled; else None."""
+    import hashlib
+    prof = os.path.join(ROOT, "profiles", "k_gather_host_misses.md")
+    src = os.path.join(ROOT, "sampling_gnn_mini_gb300", "csrc", "sg_gather.cu")
+    if not (os.path.exists(prof) and os.path.exists(src)):
+        return None
+    vals, want = {}, None
+    for line in open(prof):
+        for key in ("traffic_per_hit_bytes", "traffic_per_miss_bytes"):
+            if line.startswith(key + ":"):
+                vals[key] = float(line.split(":", 1)[1])
+        if line.startswith("sg_gather.cu sha256:"):
+            want = line.split(":", 1)[1].strip()
+    have = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    if want != have or len(vals) != 2:
+        return None
+    return hits * vals["traffic_per_hit_bytes"] + misses * vals["traffic_per_miss_bytes"]
+
+
 class Clocks:
     """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
 
@@ -652,7 +674,10 @@ def run_ours(args, rank, world, local):
                                                          "k_gather, k_region_scan, k_region_scatter, k_gather_list"),
                 "bound": stage_roof["gather"]["bound"],
                 "achieved": ach_bytes / (stage_ms["gather"] / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
-                "frac": stage_roof["gather"]["frac"], "traffic": None,
+                "frac": stage_roof["gather"]["frac"],
+                "traffic": gather_traffic(hits / args.steps, misses / args.steps),
+                "traffic_unit": "DRAM bytes per step of k_gather and k_gather_list, scaled per hit and per miss from "
+                                "the ncu capture in profiles/k_gather_host_misses.md",
                 "peak_kind": ("measured host link, same run (%s, the faster of zero-copy loads and the copy engine)"
                               % max(link, key=link.get)) if stage_roof["gather"]["bound"] == "host_link"
                 else "of " + peak_kind}
