@@ -54,7 +54,8 @@ namespace {
 
 constexpr int kNT = 256;             // threads of every sampler kernel (8 warps)
 constexpr int kTile = 1024;          // rows / edges per scan tile (4 per thread)
-constexpr int kCtrWords = 16;       // counters of one hop (see HopArgs::ctr)
+constexpr int kUnitQueues = 8;      // k_sample's warp units come from this many counters
+constexpr int kCtrWords = 32 + 32 * kUnitQueues;  // counters of one hop (see HopArgs::ctr)
 constexpr int kGroupLambdaMax = 64;  // short random rows go to 8-lane groups when f + 2 sqrt(f) + 4 <= this
 constexpr uint32_t kEmpty = 0xFFFFFFFFu;
 
@@ -170,7 +171,7 @@ struct HopArgs {
     // this hop's rows
     struct BinRec* brec;     // the four degree bins (see bin_slot)
     int64_t bin_cap;         // capacity of one half of brec (rows of the hop's bound)
-    uint32_t* ctr;           // [0] row tiles, [1] edge tiles, [2..9] bin sizes, [10] block rows, [11] units
+    uint32_t* ctr;           // [0] row tiles, [1] edge tiles, [2..9] bin sizes, [10] block rows, [32 + 32 q] unit queue q
     unsigned long long* row_status;
     unsigned long long* edge_status;
     int32_t* bindptr;
@@ -775,8 +776,11 @@ __global__ void __launch_bounds__(kNT, 4) k_sample(HopArgs a) {
     const Pool wpool{s_key + wib * kWarpPool, s_pos + wib * kWarpPool, s_sel + wib * kWarpSel, &s_n[4 * wib], kWarpPool};
     const Pool gpool{s_key + wib * kWarpPool + g * kGroupPool, s_pos + wib * kWarpPool + g * kGroupPool,
                      s_sel + wib * kWarpSel + g * kGroupSel, &s_n[4 * wib + g], kGroupPool};
+    // Units come from kUnitQueues counters, each in its own 128-byte line:
+    // queue q hands out units q, q + kUnitQueues, ... to the warps w with
+    // w mod kUnitQueues = q, so no single counter takes every warp's atomics.
     // The next unit is reserved while this one runs only when units are
-    // plentiful (more than two per warp left); near the end of the queue a warp
+    // plentiful (more than two per warp left); near the end of a queue a warp
     // takes its next unit once it is done, so that no unit waits behind a busy
     // warp while others are idle.
     auto unit_rec = [&](int32_t uu, BinRec& rc) {
@@ -789,12 +793,17 @@ __global__ void __launch_bounds__(kNT, 4) k_sample(HopArgs a) {
         }
     };
     const int32_t n_warps = (int32_t)(gridDim.x * (kNT / 32));
+    // this warp's queue and its next unit (lane 0 only)
+    auto take = [&]() -> uint32_t {
+        const uint32_t q = (blockIdx.x * (kNT / 32) + (threadIdx.x >> 5)) % kUnitQueues;
+        return (atomicAdd(a.ctr + 32 + 32 * q, 1u) + 1u) * kUnitQueues + q;
+    };
     uint32_t nxt = 0;
-    if (lane == 0) nxt = atomicAdd(a.ctr + 11, 1u) + 1u;
+    if (lane == 0) nxt = take();
     int32_t u = (int32_t)__shfl_sync(0xffffffffu, nxt, 0);
     while (u < units) {
         const bool ahead = u + 2 * n_warps < units;
-        if (ahead && lane == 0) nxt = atomicAdd(a.ctr + 11, 1u) + 1u;
+        if (ahead && lane == 0) nxt = take();
         BinRec rec;
         unit_rec(u, rec);
         if (u < u2) {
@@ -809,7 +818,7 @@ __global__ void __launch_bounds__(kNT, 4) k_sample(HopArgs a) {
             }
         }
         __syncwarp();
-        if (!ahead && lane == 0) nxt = atomicAdd(a.ctr + 11, 1u) + 1u;
+        if (!ahead && lane == 0) nxt = take();
         u = (int32_t)__shfl_sync(0xffffffffu, nxt, 0);
     }
 }
