@@ -730,6 +730,7 @@ def run_ours(args, rank, world, local):
         "host_table": None if not w.host_features else {
             "bytes": w.n_nodes * R,
             "huge_page_bytes": getattr(getattr(W.feat, "_sg_owner", None), "huge", 0),
+            "locked": getattr(getattr(W.feat, "_sg_owner", None), "locked", False),
             "allocation": "huge-page mmap + cudaHostRegister" if hasattr(W.feat, "_sg_owner") else "cudaHostAlloc"},
         "gathered_feature_gbs": n_H.sum() * R / (elapsed_ms / 1e3) / 1e9,
         "gather_kernel_gbs": n_H.sum() * R / t_gather / 1e9,

@@ -11,9 +11,18 @@ to address translation when it is backed by small pages.  Measured on GB300
 (a 16 GB table reads at ~208 GB/s either way).  pinned_table() therefore
 backs large tables with transparent huge pages and pins them with
 cudaHostRegister; small tables use torch's pinned allocator.
+
+The GPU reaches a registered table through the host's page tables, and every
+change the kernel makes to the table's entries (page aging clearing accessed
+bits, huge-page collapse scans) invalidates the GPU's cached translations:
+the gathers after it run cold, a single cold gather of 100K rows taking tens
+of ms.  A large table's pages are therefore also locked (mlock: they leave the
+reclaim lists, so aging skips them) and, once faulted in, marked no longer
+eligible for huge-page collapse, so that the background scanner skips them.
 """
 from __future__ import annotations
 
+import ctypes
 import mmap
 
 import torch
@@ -45,8 +54,18 @@ def _huge_bytes(addr: int) -> int:
         return 0
 
 
+def _lock_pages(addr: int, nbytes: int) -> bool:
+    """mlock(2) of [addr, addr + nbytes); False where it is refused."""
+    try:
+        libc = ctypes.CDLL(None, use_errno=True)
+        return int(libc.mlock(ctypes.c_void_p(addr), ctypes.c_size_t(nbytes))) == 0
+    except (OSError, AttributeError):
+        return False
+
+
 class _Registered:
-    """Owns a huge-page mapping pinned with cudaHostRegister."""
+    """Owns a huge-page mapping pinned with cudaHostRegister (and locked
+    where the process may lock it)."""
 
     def __init__(self, nbytes: int):
         self.registered = False
@@ -58,8 +77,12 @@ class _Registered:
         self.base.fill_(0)  # fault the pages in (as huge pages where the kernel allows)
         self.ptr = self.base.data_ptr()
         self.huge = _huge_bytes(self.ptr)
+        self.locked = False
         if self.huge < 0.9 * nbytes:  # the kernel gave mostly small pages: not worth registering
             return
+        self.locked = _lock_pages(self.ptr, nbytes)
+        if hasattr(mmap, "MADV_NOHUGEPAGE"):
+            self.map.madvise(mmap.MADV_NOHUGEPAGE)  # the pages are in: no collapse scans from here on
         err = torch.cuda.cudart().cudaHostRegister(self.ptr, nbytes, 0)
         if int(err) != 0:
             raise RuntimeError("cudaHostRegister of the host table failed: %s" % err)

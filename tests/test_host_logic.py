@@ -68,3 +68,32 @@ def test_huge_page_bytes_from_smaps():
     t.fill_(1)
     assert 0 <= hostmem._huge_bytes(t.data_ptr()) <= n
     del t
+
+
+def test_lock_pages_locks_a_mapping_or_reports_refusal():
+    # mlock of a small mapping: True where the process may lock memory (as root
+    # here), and a plain False, never an exception, where it is refused; the
+    # mapping stays readable and writable either way, and a locked one shows
+    # up in the process's locked total
+    n = 4 << 20
+    m = mmap.mmap(-1, n, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
+    t = torch.frombuffer(m, dtype=torch.uint8)
+    t.fill_(3)
+
+    def vm_lck_kb():
+        with open("/proc/self/status") as fh:
+            for line in fh:
+                if line.startswith("VmLck:"):
+                    return int(line.split()[1])
+        return 0
+
+    before = vm_lck_kb()
+    ok = hostmem._lock_pages(t.data_ptr(), n)
+    assert isinstance(ok, bool)
+    if ok:
+        assert vm_lck_kb() - before >= n // 1024
+    t[::4096] += 1
+    assert int(t[4096]) == 4 and int(t[1]) == 3
+    assert hostmem._lock_pages(0, 0) in (True, False)
+    del t
+    m.close()
