@@ -26,9 +26,8 @@ struct sg_dyn {
     int32_t* nodes = nullptr;    // device, k_dyn: node in each slot or -1
     uint32_t* S = nullptr;       // device, n_nodes: scores (Q8)
     uint32_t* A = nullptr;       // device, n_nodes: the window's weighted counts
-    int32_t* order = nullptr;    // device, n_nodes: ranking scratch
+    uint32_t* sel = nullptr;     // device, 512 words: the Top-K selection (histogram, then its parameters)
     int32_t* lists = nullptr;    // device, 2 k_dyn + 8: new nodes, free slots, counters
-    void* rank_ws = nullptr;     // device ranking workspace
 };
 
 struct sg_cache {
