@@ -1020,7 +1020,8 @@ def run_next_experiments(args):
            "gather_ms_median_static_plus_dynamic": float(np.median(ms_s["dynamic"][half:])),
            "window_update_ms_median": float(np.median(upd_ms)) if upd_ms else None,
            "note": "rates and times over the second half of the batches; the window update (Eq. (5) fold, Top-K of "
-                   "Eq. (6) by a radix ranking of every node, admission of entering rows) runs once a window"}
+                   "Eq. (6) by radix selection over the nonzero scores, admission of entering rows from the host "
+                   "table) runs once a window"}
     return {"impl": "experiment", "config": w.name, "match_reorder": match_reorder, "dynamic_cache": dyn,
             "presample": presample}
 
